@@ -1,0 +1,170 @@
+"""Reference paged-KV cache manager for the verification cycle (oracle).
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__``).
+
+Sources (page titles; paragraphs counted on the page):
+  [KV]  "Walk through KV-cache updates when speculative decoding rejects some
+        draft tokens": candidate K/V is appended provisionally during the
+        verify pass; after the first rejection the rejected positions are
+        removed -- free the pages on a paged cache, rewind the write pointer on
+        a contiguous one -- so the cache holds exactly the committed sequence.
+  [RJ]  "Rejected speculative tokens remain in KV" (interview question),
+        paragraphs 1-2: allocation is not acceptance; a physical block may stay
+        allocated with only part of it valid if attention cannot read the rest.
+  [CV]  "Keep cache validity aligned with the committed token history",
+        paragraphs 1-4: the pending-token convention (cache length = processed
+        tokens, the newest emitted token is pending), keep prefix plus the
+        accepted proposals and leave the correction pending; block tables,
+        ownership and reference counts decide which memory is valid; rollback of
+        one request must not mutate another request's committed prefix.
+
+State (all plain arrays, mirrored bit for bit by the CUDA path):
+  free_stack [num_blocks] int32, free_top, refcount [num_blocks] int32,
+  block_table [B][max_blocks] int32 (-1 = no block), seq_len [B] int32.
+
+Readings (listed in the design doc):
+  * seq_len S_b counts processed tokens; the pending token sits at position
+    S_b.  The verify pass processes positions S_b .. S_b + k_b, so it needs
+    blocks covering [0, S_b + k_b + 1).
+  * after a pass with a_b accepted drafts: seq_len <- S_b + 1 + a_b (the old
+    pending token and the accepted drafts are now processed; the correction or
+    bonus token is the new pending token).  a_b = -1 (bad input) keeps S_b.
+  * blocks j in [ceil(new/BS), ceil((S_b + k_b + 1)/BS)) are dropped: table
+    entry cleared, refcount decremented, pushed on the free stack when it
+    reaches 0.  A block with at least one valid slot is kept.
+  * order: requests ascending, j ascending, for pops and pushes alike; the
+    free stack starts as [n-1, ..., 1, 0] so that blocks pop as 0, 1, 2, ...
+  * a fork shares whole blocks only; appending into a partially filled block
+    whose refcount is above 1 is refused (copy-on-write is not provided).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+
+class CacheError(Exception):
+    pass
+
+
+class OutOfBlocks(CacheError):
+    pass
+
+
+def ceil_div(a: int, b: int) -> int:
+    return -(-a // b)
+
+
+class BlockPool:
+    """Free list + refcounts of a pool of num_blocks blocks of block_size slots."""
+
+    def __init__(self, num_blocks: int, block_size: int):
+        self.num_blocks = int(num_blocks)
+        self.block_size = int(block_size)
+        self.free_stack = np.arange(self.num_blocks - 1, -1, -1, dtype=np.int32)
+        self.free_top = self.num_blocks
+        self.refcount = np.zeros(self.num_blocks, np.int32)
+
+    def copy(self) -> "BlockPool":
+        c = BlockPool.__new__(BlockPool)
+        c.num_blocks, c.block_size = self.num_blocks, self.block_size
+        c.free_stack = self.free_stack.copy()
+        c.free_top = self.free_top
+        c.refcount = self.refcount.copy()
+        return c
+
+    def _pop(self) -> int:
+        self.free_top -= 1
+        blk = int(self.free_stack[self.free_top])
+        self.refcount[blk] = 1
+        return blk
+
+    def _drop(self, blk: int) -> bool:
+        """Decrement blk's refcount; push it on the free stack if it hit 0."""
+        if not (0 <= blk < self.num_blocks) or self.refcount[blk] <= 0:
+            raise CacheError(f"drop of unowned block {blk}")
+        self.refcount[blk] -= 1
+        if self.refcount[blk] == 0:
+            self.free_stack[self.free_top] = blk
+            self.free_top += 1
+            return True
+        return False
+
+    # ------------------------------------------------------------------ #
+    def reserve(self, seq_len, k, block_table) -> None:
+        """Lookahead allocation before the verify pass ([RJ] paragraph 1).
+
+        Covers positions [0, S_b + k_b + 1) for every request; all-or-nothing.
+        """
+        BS = self.block_size
+        B = len(seq_len)
+        need = []
+        for b in range(B):
+            S, kb = int(seq_len[b]), int(k[b])
+            have, want = ceil_div(S, BS), ceil_div(S + kb + 1, BS)
+            if S < 0 or kb < 0 or want > block_table.shape[1]:
+                raise CacheError(f"request {b}: bad sizes")
+            row = block_table[b]
+            if (row[:have] < 0).any() or (row[have:want] >= 0).any():
+                raise CacheError(f"request {b}: table does not match seq_len")
+            if S % BS and self.refcount[row[have - 1]] > 1:
+                raise CacheError(f"request {b}: append into a shared partial block")
+            need.append(want - have)
+        if sum(need) > self.free_top:
+            raise OutOfBlocks(f"need {sum(need)} blocks, {self.free_top} free")
+        for b in range(B):
+            have = ceil_div(int(seq_len[b]), BS)
+            for t in range(need[b]):
+                block_table[b, have + t] = self._pop()
+
+    def commit_rollback(self, k, accepted, seq_len, block_table):
+        """Commit the accepted prefix, roll back the rejected tail ([KV], [CV] 2-3).
+
+        Returns n_freed [B] (blocks pushed on the free stack per request).
+        """
+        BS = self.block_size
+        B = len(seq_len)
+        n_freed = np.zeros(B, np.int32)
+        for b in range(B):
+            S, kb, a = int(seq_len[b]), int(k[b]), int(accepted[b])
+            if not (-1 <= a <= kb):
+                raise CacheError(f"request {b}: accepted {a} outside [-1, {kb}]")
+            new = S if a < 0 else S + 1 + a
+            for j in range(ceil_div(new, BS), ceil_div(S + kb + 1, BS)):
+                blk = int(block_table[b, j])
+                block_table[b, j] = -1
+                n_freed[b] += self._drop(blk)
+            seq_len[b] = new
+        return n_freed
+
+    def fork_prefix(self, src, dst, n_blocks, block_table) -> None:
+        """Share the first n whole blocks of request src with request dst ([CV] 4)."""
+        for s, d, n in zip(src, dst, n_blocks):
+            if (block_table[d, :n] >= 0).any() or (block_table[s, :n] < 0).any():
+                raise CacheError(f"fork {s}->{d}: bad tables")
+            for j in range(int(n)):
+                blk = int(block_table[s, j])
+                block_table[d, j] = blk
+                self.refcount[blk] += 1
+
+    def release(self, req_ids, seq_len, block_table):
+        """Drop every block a finished request holds; shared blocks just lose a ref."""
+        n_freed = np.zeros(len(req_ids), np.int32)
+        for i, b in enumerate(req_ids):
+            row = block_table[b]
+            for j in range(row.shape[0]):
+                if row[j] < 0:
+                    break
+                blk = int(row[j])
+                row[j] = -1
+                n_freed[i] += self._drop(blk)
+            seq_len[b] = 0
+        return n_freed
+
+
+def rollback_contiguous(accepted, write_ptr) -> None:
+    """Contiguous cache: rewind the write pointer to S_b + 1 + a_b ([KV])."""
+    for b in range(len(write_ptr)):
+        a = int(accepted[b])
+        if a >= 0:
+            write_ptr[b] = int(write_ptr[b]) + 1 + a

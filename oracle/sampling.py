@@ -1,0 +1,272 @@
+"""Verification step of speculative decoding, written out plainly in fp64 (oracle).
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__``).
+
+Sources (page titles; sections as printed on the pages):
+  [SD]  "Speculative decoding: accelerate LLM generation without changing its
+        answers" -- section 2 "Draft, verify, correct", 3 "Why this preserves
+        the target distribution", 4 "Data flow and performance trade-offs",
+        5 "Reproducible toy lab", 6 "Production failures, debugging, and
+        security".
+  [KV]  "Walk through KV-cache updates when speculative decoding rejects some
+        draft tokens" (left-to-right acceptance, first rejection ends the run).
+
+Per request b with k_b drafts the walk is ([SD] section 2):
+  for i = 0 .. k_b - 1: accept draft y_i with probability min(1, p_i(y_i)/q_i(y_i));
+  the first rejection stops the walk and a correction is drawn from
+  normalize(max(0, p_i - q_i)); if every draft is accepted a bonus token is
+  drawn from p_{k_b}.  Both draws are exponential races argmax_x w_x / E_x,
+  which sample x with probability w_x / sum(w).
+
+Readings taken where the pages leave a step open (each also listed in the design doc):
+  * transforms ([SD] sections 3, 4, 6: acceptance uses "the exact transformed
+    distributions"): z = logit / T, or ln(prob) / T for draft probabilities;
+    dist = softmax(z).  T = 0 is the limit T -> 0+: uniform over the tied
+    maximum set.
+  * top-p: set-based nucleus.  tau = the largest value t with
+    sum_{x: dist_x >= t} dist_x >= top_p; keep every x with dist_x >= tau (all
+    ties at tau), renormalise.  Applied to p and to q alike; no effect at T = 0.
+  * accept test without division: accept iff u * q(y) < p(y); equal to
+    u < min(1, p/q) for q(y) > 0.  q(y) = 0 cannot happen for a proposal drawn
+    from q ([SD] section 5, variation 2); it is flagged ST_Q_ZERO and the rule
+    then accepts iff p(y) > 0.
+  * a rejected row whose residual is numerically empty samples from p and is
+    flagged ST_RESIDUAL_EMPTY.
+  * invalid input (NaN, +inf, a row with no support, bad T / top_p / k / token)
+    ends the request: accepted = -1, nothing emitted, ST_BAD_INPUT.
+  * absolute position of the token decided by row i: pos = S_b + 1 + i, where
+    S_b is the cache length before the pass and the pending token sits at S_b.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+from . import philox
+
+ST_Q_ZERO = 1
+ST_BAD_INPUT = 2
+ST_RESIDUAL_EMPTY = 4
+ST_TIMEOUT = 8
+
+
+# --------------------------------------------------------------------------- #
+# input decoding
+# --------------------------------------------------------------------------- #
+def decode_bf16(bits) -> np.ndarray:
+    """bfloat16 bit patterns (uint16) -> fp64 values (bf16 is the top half of fp32)."""
+    bits = np.asarray(bits, dtype=np.uint16)
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def decode(values, dtype: str) -> np.ndarray:
+    if dtype == "bf16":
+        return decode_bf16(values)
+    if dtype == "f32":
+        return np.asarray(values, dtype=np.float32).astype(np.float64)
+    raise ValueError(dtype)
+
+
+def row_is_valid(row: np.ndarray, kind: str) -> bool:
+    """A row the walk can read: no NaN, no +inf, some support ([SD] section 6,
+    "numerical edge cases"; reading: such rows are reported, never sampled)."""
+    if np.isnan(row).any() or np.isposinf(row).any():
+        return False
+    if kind == "probs":
+        return bool((row >= 0).all() and (row > 0).any())
+    return bool(np.isfinite(row).any())
+
+
+# --------------------------------------------------------------------------- #
+# transforms  ([SD] sections 3, 4, 6)
+# --------------------------------------------------------------------------- #
+def greedy_limit(row: np.ndarray) -> np.ndarray:
+    """softmax(row / T) as T -> 0+: uniform over {x : row_x = max row}."""
+    support = row == row.max()
+    return support / support.sum()
+
+
+def softmax_T(row: np.ndarray, kind: str, T: float) -> np.ndarray:
+    """Temperature transform followed by a max-shifted softmax ([SD] section 6:
+    "use stable softmax/log-probability calculations")."""
+    with np.errstate(divide="ignore"):
+        z = (np.log(row) if kind == "probs" else row) / T
+    e = np.exp(z - z.max())
+    return e / e.sum()
+
+
+def nucleus(dist: np.ndarray, top_p: float):
+    """Set-based top-p (reading; the pages name top-p without defining it).
+
+    Returns (filtered distribution, kept mask, tau).  tau is the largest
+    distinct value t of dist with mass{dist >= t} >= top_p; kept = dist >= tau.
+    """
+    if top_p >= 1.0:
+        return dist, dist > 0, float(dist[dist > 0].min())
+    vals, counts = np.unique(dist, return_counts=True)        # ascending
+    vals, counts = vals[::-1], counts[::-1]                    # descending
+    cum = np.cumsum(vals * counts)                             # mass of {dist >= vals[j]}
+    hit = np.nonzero(cum >= top_p)[0]
+    tau = float(vals[hit[0]]) if hit.size else float(vals[vals > 0].min())
+    kept = dist >= tau
+    out = np.where(kept, dist, 0.0)
+    return out / out.sum(), kept, tau
+
+
+def transform(row: np.ndarray, kind: str, T: float, top_p: float):
+    """The decoding transform applied identically to target and draft rows.
+
+    Returns (dist, info) where info holds the kept mask and the kept fraction of
+    the pre-filter mass (1 when no top-p filtering happens).
+    """
+    if T == 0.0:
+        dist = greedy_limit(row)
+        return dist, {"kept": dist > 0, "kept_mass": 1.0}
+    dist = softmax_T(row, kind, T)
+    if top_p < 1.0:
+        filt, kept, _ = nucleus(dist, top_p)
+        return filt, {"kept": kept, "kept_mass": float(dist[kept].sum())}
+    return dist, {"kept": dist > 0, "kept_mass": 1.0}
+
+
+# --------------------------------------------------------------------------- #
+# the acceptance law  ([SD] sections 2, 3, 5)
+# --------------------------------------------------------------------------- #
+def accept_probability(p_y: float, q_y: float) -> float:
+    """min(1, p(y)/q(y)) ([SD] section 2)."""
+    return 1.0 if q_y <= p_y else p_y / q_y
+
+
+def accepted_mass(p: np.ndarray, q: np.ndarray) -> np.ndarray:
+    """q(x) a(x) = min(q(x), p(x)) ([SD] section 3)."""
+    return np.minimum(p, q)
+
+
+def residual(p: np.ndarray, q: np.ndarray) -> np.ndarray:
+    """Unfilled target mass max(0, p - q) ([SD] section 3)."""
+    return np.maximum(0.0, p - q)
+
+
+def accepts(u: float, p_y: float, q_y: float) -> bool:
+    """Accept iff u * q(y) < p(y) -- u < min(1, p/q) without a division."""
+    return u * q_y < p_y
+
+
+def exponential_race(w: np.ndarray, E: np.ndarray) -> int:
+    """argmax_x w_x / E_x with E_x ~ Exp(1) i.i.d.: a draw from w / sum(w).
+
+    Ties go to the lowest index (np.argmax returns the first maximum).
+    """
+    with np.errstate(divide="ignore", invalid="ignore"):
+        keys = np.where(w > 0, w / E, 0.0)
+    return int(np.argmax(keys))
+
+
+# --------------------------------------------------------------------------- #
+# one request, left to right  ([SD] section 2, [KV])
+# --------------------------------------------------------------------------- #
+def verify_request(target_rows, draft_rows, tokens, k, T, top_p, draft_kind,
+                   seed, request_id, seq_len, force=None, keep_rows=False):
+    """Run the walk for one request on decoded fp64 rows.
+
+    target_rows [>= k+1][V], draft_rows [>= k][V], tokens [>= k] (ints).
+    force: optional {row: bool} that overrides the accept decision of a row
+    (the parity harness uses it to follow a counted near-tie flip).
+    Returns a dict: accepted (-1 on bad input), tokens (emitted list), status,
+    rows (per-row record: p_y, q_y, u, accept, kept masses, and p/q if keep_rows).
+    """
+    force = force or {}
+    V = target_rows.shape[-1]
+    status = 0
+    rows = []
+    T = float(np.float32(T))
+    top_p = float(np.float32(top_p))
+    bad = dict(accepted=-1, tokens=[], status=ST_BAD_INPUT, rows=rows)
+    if k < 0 or k > len(tokens):
+        return bad
+    if not (T >= 0.0) or not (0.0 < top_p <= 1.0):
+        return bad
+    for i in range(k + 1):
+        pos = int(seq_len) + 1 + i
+        trow = target_rows[i]
+        if not row_is_valid(trow, "logits"):
+            return bad
+        p, pinfo = transform(trow, "logits", T, top_p)
+        rec = {"pos": pos, "p_kept_mass": pinfo["kept_mass"]}
+        if keep_rows:
+            rec["p"] = p
+        rows.append(rec)
+        if i == k:                                   # bonus row ([SD] section 2)
+            E = philox.race_exponentials(seed, request_id, pos, V)
+            tok = exponential_race(p, E)
+            rec["race"] = {"w": p, "E": E, "token": tok}
+            return dict(accepted=k, tokens=[int(t) for t in tokens[:k]] + [tok],
+                        status=status, rows=rows)
+        drow = draft_rows[i]
+        y = int(tokens[i])
+        if not row_is_valid(drow, draft_kind) or not (0 <= y < V):
+            return bad
+        q, qinfo = transform(drow, draft_kind, T, top_p)
+        u = philox.accept_uniform(seed, request_id, pos)
+        rec.update(q_kept_mass=qinfo["kept_mass"], p_y=float(p[y]), q_y=float(q[y]), u=u)
+        if keep_rows:
+            rec["q"] = q
+        if q[y] == 0.0:
+            status |= ST_Q_ZERO
+        ok = accepts(u, p[y], q[y])
+        if i in force:
+            rec["forced_from"] = ok
+            ok = bool(force[i])
+        rec["accept"] = ok
+        if ok:
+            continue
+        # first rejection: correction from normalize(max(0, p - q))
+        w = residual(p, q)
+        if not (w > 0).any():
+            status |= ST_RESIDUAL_EMPTY
+            w = p
+        E = philox.race_exponentials(seed, request_id, pos, V)
+        tok = exponential_race(w, E)
+        rec["race"] = {"w": w, "E": E, "token": tok}
+        return dict(accepted=i, tokens=[int(t) for t in tokens[:i]] + [tok],
+                    status=status, rows=rows)
+    raise AssertionError("unreachable")
+
+
+def verify_batch(inp: dict, force=None, keep_rows=False):
+    """The batched verification step over every request of a workload dict.
+
+    inp keys: target [B][kmax+1][V] (bf16 bits or fp32), target_dtype,
+    draft [B][kmax][V], draft_dtype, draft_kind ('logits' | 'probs'),
+    tokens [B][kmax], k [B], temperature [B], top_p [B], seed, request_id [B],
+    seq_len [B].  force: optional {b: {row: bool}}.
+    Returns accepted [B], out_tokens [B][kmax+1] (-1 padded), num_emitted [B],
+    status [B] and the per-request records.
+    """
+    B = inp["k"].shape[0]
+    kmax = inp["tokens"].shape[1] if inp["tokens"].ndim == 2 else 0
+    accepted = np.zeros(B, np.int32)
+    out = np.full((B, kmax + 1), -1, np.int32)
+    nemit = np.zeros(B, np.int32)
+    status = np.zeros(B, np.uint32)
+    recs = []
+    for b in range(B):
+        kb = int(inp["k"][b])
+        if kb < 0 or kb > kmax:
+            r = dict(accepted=-1, tokens=[], status=ST_BAD_INPUT, rows=[])
+        else:
+            trows = decode(inp["target"][b, :kb + 1], inp["target_dtype"])
+            drows = decode(inp["draft"][b, :kb], inp["draft_dtype"]) if kb else \
+                np.zeros((0, trows.shape[-1]))
+            r = verify_request(trows, drows, inp["tokens"][b, :kb], kb,
+                               inp["temperature"][b], inp["top_p"][b],
+                               inp["draft_kind"], inp["seed"],
+                               int(inp["request_id"][b]), int(inp["seq_len"][b]),
+                               force=(force or {}).get(b), keep_rows=keep_rows)
+        accepted[b] = r["accepted"]
+        status[b] = r["status"]
+        nemit[b] = len(r["tokens"])
+        out[b, :len(r["tokens"])] = r["tokens"]
+        recs.append(r)
+    return dict(accepted=accepted, out_tokens=out, num_emitted=nemit,
+                status=status, records=recs)

@@ -1,0 +1,217 @@
+"""Pins of the reference cache manager: a hand-derived scenario, brute-force
+recounts of ownership, forced-rejection rounds checked through a toy attention
+model against a no-speculation recompute, and shared-prefix isolation."""
+
+import numpy as np
+import pytest
+
+from oracle.kvcache import BlockPool, CacheError, OutOfBlocks, ceil_div, rollback_contiguous
+from tests.toy_model import PagedPayload, ToyAttention
+
+
+def _check_invariants(pool: BlockPool, table, seq_len=None):
+    """Brute-force recount: refcount == table references; free set == unreferenced."""
+    refs = np.zeros(pool.num_blocks, np.int64)
+    for row in table:
+        live = row[row >= 0]
+        n = live.size
+        assert (row[:n] >= 0).all() and (row[n:] < 0).all(), "table rows must be prefixes"
+        np.add.at(refs, live, 1)
+    np.testing.assert_array_equal(refs, pool.refcount)
+    free = pool.free_stack[:pool.free_top]
+    assert len(set(free.tolist())) == free.size
+    assert set(free.tolist()) == set(np.flatnonzero(refs == 0).tolist())
+    assert pool.free_top + (refs > 0).sum() == pool.num_blocks
+    if seq_len is not None:
+        for b, S in enumerate(seq_len):
+            assert (table[b] >= 0).sum() >= ceil_div(int(S), pool.block_size)
+
+
+def test_hand_derived_scenario():
+    pool = BlockPool(6, 4)
+    np.testing.assert_array_equal(pool.free_stack, [5, 4, 3, 2, 1, 0])
+    table = np.full((3, 6), -1, np.int32)
+    seq = np.array([0, 0, 0], np.int32)
+    pool.reserve(seq[:2], [4, 6], table)                 # covers [0,5) and [0,7)
+    np.testing.assert_array_equal(table[:2], [[0, 1, -1, -1, -1, -1], [2, 3, -1, -1, -1, -1]])
+    assert pool.free_top == 2
+    freed = pool.commit_rollback([4, 6], [1, 6], seq[:2], table)
+    np.testing.assert_array_equal(seq[:2], [2, 7])
+    np.testing.assert_array_equal(freed, [1, 0])
+    assert pool.free_top == 3 and pool.free_stack[2] == 1
+    np.testing.assert_array_equal(pool.refcount, [1, 0, 1, 1, 0, 0])
+    pool.reserve(seq[:2], [3, 3], table)
+    np.testing.assert_array_equal(table[:2], [[0, 1, -1, -1, -1, -1], [2, 3, 4, -1, -1, -1]])
+    pool.commit_rollback([3, 3], [0, 3], seq[:2], table)
+    np.testing.assert_array_equal(seq[:2], [3, 11])
+    assert pool.free_top == 2
+    np.testing.assert_array_equal(pool.free_stack[:2], [5, 1])
+    np.testing.assert_array_equal(pool.refcount, [1, 0, 1, 1, 1, 0])
+    before = (pool.free_stack.copy(), pool.free_top, pool.refcount.copy(), table.copy())
+    with pytest.raises(OutOfBlocks):                      # needs 2 + 2 > 2 free
+        pool.reserve(seq[:2], [8, 8], table)
+    np.testing.assert_array_equal(pool.free_stack, before[0])
+    assert pool.free_top == before[1]
+    np.testing.assert_array_equal(table, before[3])
+    # fork one whole block of request 1 into request 2, then release both
+    pool.fork_prefix([1], [2], [1], table)
+    assert pool.refcount[2] == 2 and table[2, 0] == 2
+    pool.release([1], seq, table)
+    np.testing.assert_array_equal(pool.free_stack[:pool.free_top], [5, 1, 3, 4])
+    assert pool.refcount[2] == 1
+    pool.release([2], seq, table)
+    np.testing.assert_array_equal(pool.free_stack[:pool.free_top], [5, 1, 3, 4, 2])
+    _check_invariants(pool, table)
+
+
+def test_bad_accepted_and_shared_partial_append_are_refused():
+    pool = BlockPool(8, 4)
+    table = np.full((2, 4), -1, np.int32)
+    seq = np.array([0, 0], np.int32)
+    pool.reserve(seq, [5, 0], table)
+    with pytest.raises(CacheError):                        # accepted > k
+        pool.commit_rollback([5, 0], [6, 0], seq.copy(), table.copy())
+    with pytest.raises(CacheError):                        # fork onto an owned slot
+        pool.copy().fork_prefix([0], [1], [2], table.copy())
+    pool.commit_rollback([5, 0], [4, 0], seq, table)       # seq -> [5, 1]
+    np.testing.assert_array_equal(seq, [5, 1])
+    shared = pool.copy()
+    shared.refcount[table[0, 1]] += 1                      # block 1 of request 0 is partial
+    with pytest.raises(CacheError):
+        shared.reserve(seq, [1, 0], table.copy())
+
+
+def test_random_cycles_keep_ownership_consistent():
+    rng = np.random.default_rng(0)
+    BS, B = 16, 12
+    pool = BlockPool(400, BS)
+    table = np.full((B, 64), -1, np.int32)
+    seq = np.zeros(B, np.int32)
+    pre = rng.integers(1, 300, B)
+    pool.reserve(seq, pre - 1, table)                      # prefill [0, pre)
+    seq[:] = pre
+    _check_invariants(pool, table, seq)
+    for step in range(40):
+        k = rng.integers(0, 9, B)
+        pool.reserve(seq, k, table)
+        acc = np.array([rng.integers(-1, kb + 1) for kb in k])
+        pool.commit_rollback(k, acc, seq, table)
+        _check_invariants(pool, table, seq)
+        for b in range(B):
+            assert (table[b] >= 0).sum() == ceil_div(int(seq[b]), BS)
+        if step % 10 == 9:
+            gone = rng.choice(B, 3, replace=False)
+            pool.release(gone, seq, table)
+            _check_invariants(pool, table)
+            for b in gone:
+                n = int(rng.integers(1, 200))
+                pool.reserve(np.array([0]), [n - 1], table[b:b + 1])
+                seq[b] = n
+            _check_invariants(pool, table, seq)
+
+
+@pytest.mark.parametrize("reject_at", [0, 2, 4, None])
+@pytest.mark.parametrize("block_edge", [False, True])
+def test_rollback_matches_no_speculation_recompute(reject_at, block_edge):
+    """Forced rejection at the first / middle / last draft (None: all accepted,
+    bonus kept pending), optionally placed so the kept prefix ends on a block
+    boundary: the valid cache equals a recompute of the committed history and
+    the next-step distribution agrees."""
+    BS, k = 16, 5
+    m = ToyAttention(seed=1)
+    rng = np.random.default_rng(2)
+    pool = BlockPool(64, BS)
+    payload = PagedPayload(m, 64, BS)
+    table = np.full((1, 16), -1, np.int32)
+    S = 37
+    a = k if reject_at is None else reject_at
+    if block_edge:
+        S = 48 - 1 - a                                 # kept length S + 1 + a = 48
+    history = list(rng.integers(0, 1000, S + 1))       # S processed + 1 pending
+    seq = np.array([0], np.int32)
+    pool.reserve(seq, [S - 1], table)                  # prefill positions [0, S)
+    payload.write(table[0], history[:S], list(range(S)))
+    seq[0] = S
+    for rnd in range(3):
+        drafts = list(rng.integers(0, 1000, k))
+        pool.reserve(seq, [k], table)
+        S0 = int(seq[0])
+        # the verify pass writes K/V for [pending, y_1..y_k] at S0 .. S0 + k
+        payload.write(table[0], [history[-1]] + drafts, list(range(S0, S0 + k + 1)))
+        aa = a if rnd == 0 else int(rng.integers(0, k + 1))
+        corr = int(rng.integers(0, 1000))
+        pool.commit_rollback([k], [aa], seq, table)
+        history = history + drafts[:aa] + [corr]
+        assert seq[0] == S0 + 1 + aa == len(history) - 1
+        valid = payload.gather(table[0], int(seq[0]))
+        recompute = m.kv(history[:-1], list(range(len(history) - 1)))
+        np.testing.assert_array_equal(valid, recompute)
+        got = m.next_distribution(valid, history[-1], int(seq[0]))
+        want = m.next_distribution(recompute, history[-1], len(history) - 1)
+        np.testing.assert_array_equal(got, want)
+        _check_invariants(pool, table, seq)
+        if block_edge and rnd == 0:
+            assert (table[0] >= 0).sum() == 48 // BS   # no partially empty block kept
+
+
+def test_shared_prefix_is_never_mutated_by_rollback():
+    BS, G, k = 16, 4, 4
+    m = ToyAttention(seed=3)
+    rng = np.random.default_rng(4)
+    pool = BlockPool(200, BS)
+    payload = PagedPayload(m, 200, BS)
+    table = np.full((G, 32), -1, np.int32)
+    seq = np.zeros(G, np.int32)
+    prefix = 64                                          # 4 whole blocks
+    hist0 = list(rng.integers(0, 500, prefix))
+    pool.reserve(seq[:1], [prefix - 1], table[:1])
+    payload.write(table[0], hist0, list(range(prefix)))
+    pool.fork_prefix([0] * (G - 1), list(range(1, G)), [prefix // BS] * (G - 1), table)
+    shared = table[0, :prefix // BS].copy()
+    np.testing.assert_array_equal(pool.refcount[shared], G)
+    snap = payload.data[shared].copy()
+    seq[:] = prefix
+    hist = [hist0 + [int(rng.integers(0, 500))] for _ in range(G)]
+    for rnd in range(6):
+        pool.reserve(seq, [k] * G, table)
+        for b in range(G):
+            S0 = int(seq[b])
+            drafts = list(rng.integers(0, 500, k))
+            payload.write(table[b], [hist[b][-1]] + drafts, list(range(S0, S0 + k + 1)))
+            hist[b] = hist[b] + drafts
+        acc = rng.integers(0, k + 1, G)
+        pool.commit_rollback([k] * G, acc, seq, table)
+        for b in range(G):
+            S0 = len(hist[b]) - k - 1
+            hist[b] = hist[b][:S0 + 1 + acc[b]] + [int(rng.integers(0, 500))]
+            assert seq[b] == len(hist[b]) - 1
+            np.testing.assert_array_equal(payload.gather(table[b], int(seq[b])),
+                                          m.kv(hist[b][:-1], list(range(len(hist[b]) - 1))))
+        np.testing.assert_array_equal(table[:, :prefix // BS], np.tile(shared, (G, 1)))
+        np.testing.assert_array_equal(payload.data[shared], snap)
+        np.testing.assert_array_equal(pool.refcount[shared], G)
+        _check_invariants(pool, table, seq)
+    pool.release([1, 2], seq, table)
+    np.testing.assert_array_equal(pool.refcount[shared], G - 2)
+    pool.release([0, 3], seq, table)
+    assert pool.free_top == pool.num_blocks
+    _check_invariants(pool, table)
+
+
+def test_contiguous_write_pointer_rollback():
+    m = ToyAttention(seed=5)
+    rng = np.random.default_rng(6)
+    k, S = 5, 32
+    buf = np.zeros((64, m.L, 2, m.H, m.d), np.float32)
+    history = list(rng.integers(0, 1000, S + 1))
+    buf[:S] = m.kv(history[:S], list(range(S)))
+    wp = np.array([S], np.int32)
+    for a in (0, 3, 5, -1):
+        S0 = int(wp[0])
+        drafts = list(rng.integers(0, 1000, k))
+        buf[S0:S0 + k + 1] = m.kv([history[-1]] + drafts, list(range(S0, S0 + k + 1)))
+        rollback_contiguous([a], wp)
+        if a >= 0:
+            history = history + drafts[:a] + [int(rng.integers(0, 1000))]
+        assert wp[0] == len(history) - 1
+        np.testing.assert_array_equal(buf[:wp[0]], m.kv(history[:-1], list(range(wp[0]))))
