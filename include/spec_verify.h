@@ -1,0 +1,248 @@
+/*
+ * spec_verify.h -- C ABI of the batched verification step of speculative
+ * decoding and of the paged-KV commit / rollback that follows it.
+ *
+ * Sources (page titles; sections as printed on the pages):
+ *   [SD] "Speculative decoding: accelerate LLM generation without changing its
+ *        answers" -- section 2 "Draft, verify, correct", section 3 "Why this
+ *        preserves the target distribution", section 4 "Data flow and
+ *        performance trade-offs", section 5 "Reproducible toy lab",
+ *        section 6 "Production failures, debugging, and security".
+ *   [KV] "Walk through KV-cache updates when speculative decoding rejects some
+ *        draft tokens" (provisional append, left-to-right acceptance, free the
+ *        pages / rewind the write pointer, the cache invariant).
+ *   [RJ] "Rejected speculative tokens remain in KV", paragraphs 1-3
+ *        (allocation is not acceptance; partially valid blocks).
+ *   [CV] "Keep cache validity aligned with the committed token history",
+ *        paragraphs 1-4 (pending-token convention; block tables, ownership and
+ *        reference counts; shared-prefix isolation).
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is a DEVICE pointer owned by the caller, unless
+ *     the comment says "host".  The library keeps no pointer after a call.
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and is asynchronous.  No call synchronises, except
+ *     sv_get_error().  No call allocates device memory, except sv_create().
+ *   - Arguments the host can check (null pointers, sizes, alignment, dtype
+ *     combinations) are checked before anything is launched: a failing check
+ *     returns SV_ERR_INVALID / SV_ERR_UNSUPPORTED and launches nothing.
+ *   - Conditions only the device can see (a bad token id, NaN logits, an
+ *     exhausted block pool, inconsistent block tables) are reported through
+ *     per-request status bits and the handle's device error word, which
+ *     sv_get_error() reads and clears.  Nothing traps or asserts on the device.
+ *   - Only one call per handle may be in flight on the GPU at a time when it
+ *     uses the handle's workspace (calls that overlap race on it).
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* sv_stream_t; /* == cudaStream_t */
+typedef struct sv_handle sv_handle;      /* opaque: device error word + launch cache */
+
+typedef enum {
+  SV_OK = 0,
+  SV_ERR_INVALID = -1,     /* bad argument (host-checked) */
+  SV_ERR_OOM = -2,         /* block pool exhausted in bfl_reserve (device) */
+  SV_ERR_CUDA = -3,        /* a CUDA runtime call failed */
+  SV_ERR_TIMEOUT = -4,     /* a bounded device-side wait gave up (device) */
+  SV_ERR_UNSUPPORTED = -5, /* valid but not provided (dtype mix, V too large) */
+  SV_ERR_STATE = -6        /* block tables / refcounts inconsistent (device) */
+} sv_status;
+
+typedef enum { SV_BF16 = 0, SV_FP32 = 1 } sv_dtype;
+typedef enum { SV_DRAFT_LOGITS = 0, SV_DRAFT_PROBS = 1 } sv_draft_kind;
+
+/* per-request status bits (sv_verify_args.status) */
+#define SV_ST_Q_ZERO 1u         /* a tested draft had q(y) = 0 ([SD] s5, variation 2) */
+#define SV_ST_BAD_INPUT 2u      /* NaN/+inf/empty row, bad T, top_p, k or token id */
+#define SV_ST_RESIDUAL_EMPTY 4u /* rejected but max(0, p - q) == 0 numerically: drew from p */
+#define SV_ST_TIMEOUT 8u        /* the request's outcome was not resolved in time */
+
+/* sv_verify_args.flags */
+#define SV_FLAG_NO_SKIP 1u /* also process rows after a known rejection (debug) */
+
+/* sv_row_debug.state */
+#define SV_ROW_NONE 0
+#define SV_ROW_ACCEPTED 1
+#define SV_ROW_REJECTED 2
+#define SV_ROW_SKIPPED 3 /* not processed: an earlier row was already rejected */
+#define SV_ROW_INVALID 4
+#define SV_ROW_BONUS 5
+
+/* Optional per-row record, [B][kmax+1], written for every processed row. */
+typedef struct {
+  float p_y, q_y, u;    /* accept-test operands (draft rows only, else 0)   */
+  float p_kept, q_kept; /* kept fraction of the pre-filter mass after top-p  */
+  int32_t state;        /* SV_ROW_*                                          */
+  int32_t p_thr_key;    /* order key of the smallest kept target value, or -1 */
+  int32_t q_thr_key;    /* same for the draft row                             */
+} sv_row_debug;
+
+/*
+ * Arguments of spec_verify ([SD] s2-s4; [KV]).
+ *
+ * Row i of request b (i = 0 .. k_b) is the target's prediction for the token
+ * at absolute position S_b + 1 + i, where S_b = seq_len[b] is the number of
+ * processed tokens before the pass and the pending token sits at S_b ([CV] 1).
+ * Draft row i (i < k_b) is the draft distribution that proposed
+ * draft_tokens[b][i].
+ *
+ * target  [B][kmax+1][target_ld] logits, bf16 or fp32.  Elements >= V of a row
+ *         are never used but the caller must allocate the whole row: rows are
+ *         read in 16-byte vectors.  target_ld >= V, target_ld * elem % 16 == 0,
+ *         base 16-byte aligned.
+ * draft   [B][kmax][draft_ld]: logits (bf16/fp32) or probabilities (fp32,
+ *         non-negative, need not sum to 1).  Same layout rules.  May be NULL
+ *         when kmax == 0.
+ * draft_tokens [B][kmax] int32 proposals (entries >= k_b ignored).
+ * k            [B] int32 drafts per request, 0 <= k_b <= kmax (ragged); NULL = kmax.
+ * temperature  [B] fp32 >= 0; 0 = greedy limit (uniform over tied maxima).
+ * top_p        [B] fp32 in (0, 1]; NULL = 1.  Applied to p and q alike.
+ * request_id   [B] uint32 Philox stream id; NULL = b.
+ * seq_len      [B] int32 S_b (read only here); NULL = 0.
+ * seed         Philox4x32-10 key (lo, hi words).
+ * Outputs: accepted [B] (a_b in [0, k_b], or -1 when the request's input is
+ *   bad), out_tokens [B][kmax+1] (the a_b accepted drafts, then the correction
+ *   or bonus token, then -1), num_emitted [B] (a_b + 1, or 0), status [B].
+ * debug  optional [B][kmax+1] sv_row_debug.  probs_p / probs_q optional
+ *   [B][kmax+1][V] / [B][kmax][V] fp32 normalised transformed rows (debug
+ *   only: the kernel then writes 4 bytes per element of every processed row).
+ */
+typedef struct {
+  int32_t B, kmax, V;
+  uint32_t flags;
+  const void* target;
+  int64_t target_ld;
+  int32_t target_dtype; /* sv_dtype */
+  int32_t draft_dtype;  /* sv_dtype */
+  int32_t draft_kind;   /* sv_draft_kind */
+  int32_t reserved0;
+  const void* draft;
+  int64_t draft_ld;
+  const int32_t* draft_tokens;
+  const int32_t* k;
+  const float* temperature;
+  const float* top_p;
+  const uint32_t* request_id;
+  const int32_t* seq_len;
+  uint64_t seed;
+  int32_t* accepted;
+  int32_t* out_tokens;
+  int32_t* num_emitted;
+  uint32_t* status;
+  sv_row_debug* debug;
+  float* probs_p;
+  float* probs_q;
+} sv_verify_args;
+
+/* Paged block pool: a LIFO free stack plus per-block reference counts
+ * ([CV] 3: block tables, ownership and reference counts decide validity). */
+typedef struct {
+  int32_t num_blocks;  /* blocks in the pool                       */
+  int32_t block_size;  /* token slots per block (BS)               */
+  int32_t* free_stack; /* [num_blocks]; entries [0, *free_top) free */
+  int32_t* free_top;   /* [1]                                       */
+  int32_t* refcount;   /* [num_blocks]; 0 = free                    */
+} bfl_state;
+
+/* sizeof(sv_verify_args) as compiled, for bindings to check their layout. */
+size_t sv_verify_args_size(void);
+
+/* Create a handle on `device` (allocates a few device words: the error word).
+ * The device becomes current for the call.  Returns SV_ERR_CUDA on failure. */
+sv_status sv_create(int device, sv_handle** handle);
+sv_status sv_destroy(sv_handle* handle);
+
+/* Bytes of workspace spec_verify needs for these arguments (host only; reads
+ * B and kmax).  The workspace is caller-owned device memory, 256-byte aligned,
+ * zero-filled before its FIRST use; afterwards spec_verify leaves it ready for
+ * the next call.  Re-zero it after an SV_ERR_TIMEOUT or a CUDA error. */
+sv_status sv_workspace_size(const sv_verify_args* args, size_t* bytes);
+
+/* The verification step ([SD] s2 and s3; [KV]): for every request, the
+ * temperature / top-p transformed target p_i and draft q_i; accept draft i iff
+ * u_i * q_i(y_i) < p_i(y_i) (== u_i < min(1, p_i/q_i)), left to right; stop at
+ * the first rejection; there draw the correction by the exponential race
+ * argmax_x max(0, p_i - q_i)_x / E_x, or, when all k_b drafts are accepted,
+ * the bonus token argmax_x p_{k_b,x} / E_x.  u and E come from Philox4x32-10:
+ * key = (seed lo, seed hi), counter = (x >> 2, S_b + 1 + i, request_id_b,
+ * stream), word x & 3, stream 0 for E_x and 1 for u_i (x = 0);
+ * U = (2 * (r >> 9) + 1) * 2^-24, E = -ln U.
+ * Rows after a rejection that is already known are skipped (their output does
+ * not depend on them) unless SV_FLAG_NO_SKIP is set.
+ * Errors: SV_ERR_INVALID / SV_ERR_UNSUPPORTED (host checks, nothing launched),
+ * SV_ERR_CUDA (launch failed); device-side conditions go to status[] and the
+ * error word. */
+sv_status spec_verify(sv_handle* handle, const sv_verify_args* args, void* workspace,
+                      size_t workspace_bytes, sv_stream_t stream);
+
+/* stack = [n-1, ..., 1, 0] (blocks pop as 0, 1, 2, ...), free_top = n,
+ * refcount = 0. */
+sv_status bfl_init(sv_handle* handle, const bfl_state* st, sv_stream_t stream);
+
+/* Lookahead allocation before the verify pass ([RJ] 1: allocation is not
+ * acceptance): make request b's table cover positions [0, S_b + k_b + 1).
+ * Request b holds ceil(S_b/BS) blocks; it receives ceil((S_b+k_b+1)/BS) -
+ * ceil(S_b/BS) more, popped in request order.  All-or-nothing: on a shortage
+ * the device error word gets SV_ERR_OOM and nothing changes.  Appending into
+ * a partially filled block whose refcount is above 1 is refused
+ * (SV_ERR_STATE): copy-on-write is not provided.
+ * seq_len [B], k [B] (NULL = 0), block_table [B][max_blocks] in/out. */
+sv_status bfl_reserve(sv_handle* handle, const bfl_state* st, int32_t B, const int32_t* seq_len,
+                      const int32_t* k, int32_t* block_table, int32_t max_blocks,
+                      sv_stream_t stream);
+
+/* Share whole blocks ([CV] 4): for pair p, dst[p] gets the first n_blocks[p]
+ * blocks of src[p] (its entries must be -1) and each shared block's refcount
+ * grows by one.  The caller sets dst's seq_len.  src, dst, n_blocks [n_pairs];
+ * block_table [n_rows][max_blocks].  Ids outside [0, n_rows), src == dst, or a
+ * dst entry that is not -1: SV_ERR_STATE, nothing changes.  A dst must not be
+ * the src of another pair in the same call. */
+sv_status bfl_fork_prefix(sv_handle* handle, const bfl_state* st, int32_t n_pairs,
+                          const int32_t* src, const int32_t* dst, const int32_t* n_blocks,
+                          int32_t* block_table, int32_t n_rows, int32_t max_blocks,
+                          sv_stream_t stream);
+
+/* Drop every block the listed requests hold (their table rows become -1,
+ * seq_len 0).  Shared blocks lose one reference and stay intact; a block
+ * whose refcount reaches 0 is pushed on the free stack, in (list order, j)
+ * order.  req_ids [n] (distinct, in [0, n_rows)), block_table [n_rows][max_blocks],
+ * n_freed optional [n].  An id out of range: SV_ERR_STATE, nothing changes. */
+sv_status bfl_release(sv_handle* handle, const bfl_state* st, int32_t n, const int32_t* req_ids,
+                      int32_t* seq_len, int32_t* block_table, int32_t n_rows, int32_t max_blocks,
+                      int32_t* n_freed, sv_stream_t stream);
+
+/* Commit / rollback after the verify pass ([KV]; [CV] 2-3): seq_len_b becomes
+ * S_b + 1 + a_b (the old pending token and the a_b accepted drafts are now
+ * processed; the correction or bonus token stays pending), or stays S_b when
+ * a_b = -1.  Blocks j in [ceil(new/BS), ceil((S_b+k_b+1)/BS)) leave the
+ * table; each loses a reference and is pushed on the free stack when that
+ * reaches 0, in (request, j) order.  A block with at least one valid slot is
+ * kept ([RJ] 2).  K/V payload is never touched.  k [B] (NULL = 0), accepted
+ * [B], seq_len [B] in/out, block_table in/out, n_freed optional [B].
+ * Inconsistent tables or accepted > k: SV_ERR_STATE, nothing changes. */
+sv_status kv_commit_rollback(sv_handle* handle, const bfl_state* st, int32_t B, const int32_t* k,
+                             const int32_t* accepted, int32_t* seq_len, int32_t* block_table,
+                             int32_t max_blocks, int32_t* n_freed, sv_stream_t stream);
+
+/* Contiguous cache ([KV]: rewind the write pointer): write_ptr_b (in: S_b)
+ * becomes S_b + 1 + a_b, or stays S_b when a_b = -1.  [B] each. */
+sv_status kv_rollback_contig(sv_handle* handle, int32_t B, const int32_t* accepted,
+                             int32_t* write_ptr, sv_stream_t stream);
+
+/* Synchronise `stream`, then read and clear the handle's device error word
+ * (host *device_code = 0 or an sv_status).  Returns SV_ERR_CUDA if the sync
+ * itself failed. */
+sv_status sv_get_error(sv_handle* handle, sv_stream_t stream, int32_t* device_code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPEC_VERIFY_H */

@@ -98,19 +98,23 @@ def softmax_T(row: np.ndarray, kind: str, T: float) -> np.ndarray:
 def nucleus(dist: np.ndarray, top_p: float):
     """Set-based top-p (reading; the pages name top-p without defining it).
 
-    Returns (filtered distribution, kept mask, tau).  tau is the largest
-    distinct value t of dist with mass{dist >= t} >= top_p; kept = dist >= tau.
+    Returns (filtered distribution, kept mask, tau, margin).  tau is the
+    largest distinct value t of dist with mass{dist >= t} >= top_p; kept =
+    dist >= tau.  margin = distance of top_p to the nearer edge of the step
+    of the cumulative mass at tau (how close the boundary decision was).
     """
     if top_p >= 1.0:
-        return dist, dist > 0, float(dist[dist > 0].min())
+        return dist, dist > 0, float(dist[dist > 0].min()), np.inf
     vals, counts = np.unique(dist, return_counts=True)        # ascending
     vals, counts = vals[::-1], counts[::-1]                    # descending
     cum = np.cumsum(vals * counts)                             # mass of {dist >= vals[j]}
     hit = np.nonzero(cum >= top_p)[0]
     tau = float(vals[hit[0]]) if hit.size else float(vals[vals > 0].min())
+    j = int(hit[0]) if hit.size else len(vals) - 1
+    margin = min(cum[j] - top_p, top_p - (cum[j - 1] if j else 0.0))
     kept = dist >= tau
     out = np.where(kept, dist, 0.0)
-    return out / out.sum(), kept, tau
+    return out / out.sum(), kept, tau, float(abs(margin))
 
 
 def transform(row: np.ndarray, kind: str, T: float, top_p: float):
@@ -121,12 +125,12 @@ def transform(row: np.ndarray, kind: str, T: float, top_p: float):
     """
     if T == 0.0:
         dist = greedy_limit(row)
-        return dist, {"kept": dist > 0, "kept_mass": 1.0}
+        return dist, {"kept": dist > 0, "kept_mass": 1.0, "margin": np.inf}
     dist = softmax_T(row, kind, T)
     if top_p < 1.0:
-        filt, kept, _ = nucleus(dist, top_p)
-        return filt, {"kept": kept, "kept_mass": float(dist[kept].sum())}
-    return dist, {"kept": dist > 0, "kept_mass": 1.0}
+        filt, kept, _, margin = nucleus(dist, top_p)
+        return filt, {"kept": kept, "kept_mass": float(dist[kept].sum()), "margin": margin}
+    return dist, {"kept": dist > 0, "kept_mass": 1.0, "margin": np.inf}
 
 
 # --------------------------------------------------------------------------- #
@@ -192,7 +196,7 @@ def verify_request(target_rows, draft_rows, tokens, k, T, top_p, draft_kind,
         if not row_is_valid(trow, "logits"):
             return bad
         p, pinfo = transform(trow, "logits", T, top_p)
-        rec = {"pos": pos, "p_kept_mass": pinfo["kept_mass"]}
+        rec = {"pos": pos, "p_kept_mass": pinfo["kept_mass"], "p_margin": pinfo["margin"]}
         if keep_rows:
             rec["p"] = p
         rows.append(rec)
@@ -208,7 +212,8 @@ def verify_request(target_rows, draft_rows, tokens, k, T, top_p, draft_kind,
             return bad
         q, qinfo = transform(drow, draft_kind, T, top_p)
         u = philox.accept_uniform(seed, request_id, pos)
-        rec.update(q_kept_mass=qinfo["kept_mass"], p_y=float(p[y]), q_y=float(q[y]), u=u)
+        rec.update(q_kept_mass=qinfo["kept_mass"], q_margin=qinfo["margin"],
+                   p_y=float(p[y]), q_y=float(q[y]), u=u)
         if keep_rows:
             rec["q"] = q
         if q[y] == 0.0:

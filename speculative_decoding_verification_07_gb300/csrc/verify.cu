@@ -1,0 +1,133 @@
+// Host entry of the batched verification step: argument checks, cluster
+// sizing and the launch (see verify_kernel.cuh for the device design).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "verify_kernel.cuh"
+
+namespace sv {
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+struct Variant {
+  KernelFn fn;
+  int eb_t, eb_d;
+  bool probs;
+  int ng_max;
+};
+
+static const Variant kVariants[] = {
+    {kernel_bf16_bf16_logits(), 2, 2, false, 8},  // bf16 target, bf16 draft logits
+    {kernel_bf16_f32_probs(), 2, 4, true, 4},     // bf16 target, fp32 draft probabilities
+    {kernel_bf16_f32_logits(), 2, 4, false, 4},   // bf16 target, fp32 draft logits
+    {kernel_f32_f32_logits(), 4, 4, false, 4},    // fp32 target, fp32 draft logits
+    {kernel_f32_f32_probs(), 4, 4, true, 4},      // fp32 target, fp32 draft probabilities
+    {kernel_f32_bf16_logits(), 4, 2, false, 4},   // fp32 target, bf16 draft logits
+};
+
+static int elem_bytes(int dt) { return dt == SV_BF16 ? 2 : 4; }
+
+size_t workspace_bytes_for(int B, int kmax) {
+  const size_t rows = (size_t)B * (size_t)(kmax + 1);
+  return kHdrBytes + ((rows * 4 + 255) / 256) * 256;
+}
+
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" size_t sv_verify_args_size(void) { return sizeof(sv_verify_args); }
+
+extern "C" sv_status sv_workspace_size(const sv_verify_args* a, size_t* bytes) {
+  if (!a || !bytes || a->B < 0 || a->kmax < 0) return SV_ERR_INVALID;
+  *bytes = workspace_bytes_for(a->B, a->kmax);
+  return SV_OK;
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+extern "C" sv_status spec_verify(sv_handle* h, const sv_verify_args* a, void* ws, size_t ws_bytes,
+                                 sv_stream_t stream) {
+  if (!h || !a) return SV_ERR_INVALID;
+  if (a->B < 0 || a->kmax < 0 || a->kmax > kMaxK || a->V < 1) return SV_ERR_INVALID;
+  if (a->B == 0) return SV_OK;
+  if (a->target_dtype != SV_BF16 && a->target_dtype != SV_FP32) return SV_ERR_INVALID;
+  if (a->draft_dtype != SV_BF16 && a->draft_dtype != SV_FP32) return SV_ERR_INVALID;
+  if (a->draft_kind != SV_DRAFT_LOGITS && a->draft_kind != SV_DRAFT_PROBS) return SV_ERR_INVALID;
+  if (a->draft_kind == SV_DRAFT_PROBS && a->draft_dtype != SV_FP32) return SV_ERR_UNSUPPORTED;
+  const int ebt = elem_bytes(a->target_dtype), ebd = elem_bytes(a->draft_dtype);
+  if (!a->target || !a->temperature || !a->accepted || !a->out_tokens || !a->num_emitted ||
+      !a->status)
+    return SV_ERR_INVALID;
+  if (a->kmax > 0 && (!a->draft || !a->draft_tokens)) return SV_ERR_INVALID;
+  if (a->target_ld < a->V || (a->target_ld * ebt) % 16 || !aligned16(a->target))
+    return SV_ERR_INVALID;
+  if (a->kmax > 0 && (a->draft_ld < a->V || (a->draft_ld * ebd) % 16 || !aligned16(a->draft)))
+    return SV_ERR_INVALID;
+  if (!ws || ((uintptr_t)ws & 255u) || ws_bytes < workspace_bytes_for(a->B, a->kmax))
+    return SV_ERR_INVALID;
+  const size_t n_tickets = (size_t)a->B * (size_t)(a->kmax + 1);
+  if (n_tickets > 0x7FFFFFFF) return SV_ERR_UNSUPPORTED;
+
+  const bool probs = a->draft_kind == SV_DRAFT_PROBS;
+  const Variant* var = nullptr;
+  for (const Variant& v : kVariants)
+    if (v.eb_t == ebt && v.eb_d == ebd && v.probs == probs) var = &v;
+  if (!var) return SV_ERR_UNSUPPORTED;
+
+  // Cluster size: smallest power of two whose register capacity covers V,
+  // then grown while the grid would leave SMs idle.
+  const int cap = kThreads * kGroup * var->ng_max;
+  int C = 1;
+  while (C < kMaxCluster && (size_t)C * cap < (size_t)a->V) C <<= 1;
+  if ((size_t)C * cap < (size_t)a->V) return SV_ERR_UNSUPPORTED;
+  const size_t rows = n_tickets;
+  while (C < 8 && rows * (size_t)C < (size_t)h->num_sms * 2) C <<= 1;
+  int slice = (int)(((size_t)a->V + C - 1) / C);
+  slice = (slice + kGroup - 1) / kGroup * kGroup;
+  const int ng = (slice + kThreads * kGroup - 1) / (kThreads * kGroup);
+
+  KParams P;
+  P.B = a->B, P.kmax = a->kmax, P.V = a->V, P.flags = a->flags;
+  P.target = (const char*)a->target, P.t_ld = a->target_ld;
+  P.draft = (const char*)a->draft, P.d_ld = a->draft_ld;
+  P.tokens = a->draft_tokens, P.k = a->k, P.temperature = a->temperature, P.top_p = a->top_p;
+  P.request_id = a->request_id, P.seq_len = a->seq_len;
+  P.seed_lo = (uint32_t)(a->seed & 0xFFFFFFFFu), P.seed_hi = (uint32_t)(a->seed >> 32);
+  P.accepted = a->accepted, P.out_tokens = a->out_tokens, P.num_emitted = a->num_emitted;
+  P.status = a->status, P.debug = a->debug, P.probs_p = a->probs_p, P.probs_q = a->probs_q;
+  P.hdr = (uint32_t*)ws;
+  P.row_state = (uint32_t*)((char*)ws + kHdrBytes);
+  P.err = h->d_err;
+  P.slice = slice, P.ng = ng, P.n_tickets = (int)n_tickets;
+  P.spin_limit = kDefaultSpin;
+
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = (cudaStream_t)stream;
+  if (C > 8)
+    SV_CUDA_TRY(cudaFuncSetAttribute(var->fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
+  cfg.gridDim = dim3((unsigned)C);
+  int max_clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&max_clusters, var->fn, &cfg) != cudaSuccess ||
+      max_clusters < 1) {
+    (void)cudaGetLastError();
+    return SV_ERR_UNSUPPORTED;
+  }
+  const size_t nclusters = rows < (size_t)max_clusters ? rows : (size_t)max_clusters;
+  cfg.gridDim = dim3((unsigned)(nclusters * C));
+  if (cudaLaunchKernelEx(&cfg, var->fn, P) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return SV_ERR_CUDA;
+  }
+  return SV_OK;
+}

@@ -1,0 +1,7 @@
+// Instantiations of the verification kernel (one nvcc process per file).
+#include "verify_kernel.cuh"
+
+namespace sv {
+KernelFn kernel_bf16_f32_probs() { return &verify_kernel<2, 4, true, 4>; }
+KernelFn kernel_bf16_f32_logits() { return &verify_kernel<2, 4, false, 4>; }
+}  // namespace sv

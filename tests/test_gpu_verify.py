@@ -1,0 +1,257 @@
+"""GPU parity of spec_verify against the fp64 oracle, through the C ABI.
+
+Every configuration of the method's benchmark set is run at full size and
+compared request by request (accepted counts, emitted tokens and status bits
+bit-exact; near-tie flips counted under the rules in tests/parity.py), plus
+edge cases, distribution tests and the normalised rows on small vocabularies.
+"""
+
+import os
+
+import numpy as np
+import pytest
+import torch
+from scipy import stats
+
+from oracle import sampling as S
+from speculative_decoding_verification_07_gb300 import binding, device_io
+from speculative_decoding_verification_07_gb300 import workloads as W
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ver():
+    if not os.path.exists(binding.LIB_PATH):
+        from speculative_decoding_verification_07_gb300 import build
+        build.build()
+    v = binding.Verifier(0)
+    yield v
+    v.close()
+
+
+def run(ver, inp, flags=0, debug=False, probs=False):
+    dev = device_io.to_device(inp, "cuda:0")
+    B, kmax, V = inp["tokens"].shape[0], inp["tokens"].shape[1], inp["target"].shape[-1]
+    dbg = torch.zeros(B, kmax + 1, 8, dtype=torch.int32, device="cuda:0") if debug else None
+    pp = torch.full((B, kmax + 1, V), -1.0, device="cuda:0") if probs else None
+    pq = torch.full((B, max(kmax, 1), V), -1.0, device="cuda:0") if probs else None
+    out = ver.verify(**dev, flags=flags, debug=dbg, probs_p=pp, probs_q=pq)
+    torch.cuda.synchronize()
+    assert ver.error() == 0
+    return out, dbg, pp, pq
+
+
+def report(name, rep):
+    print(f"{name}: {rep['exact']}/{rep['B']} exact, accept flips {rep['accept_flips']}, "
+          f"race near-ties {rep['race_ties']}, top-p boundary {rep['topp_boundary']}")
+
+
+# --------------------------------------------------------------------------- #
+# the benchmark configurations at full size
+# --------------------------------------------------------------------------- #
+def test_small_fp32_many_seeds(ver):
+    total = dict(exact=0, B=0)
+    for s in range(24):
+        inp = W.small_fp32()
+        inp["seed"] = 2000 + s
+        inp["request_id"][:] = s
+        out, dbg, _, _ = run(ver, inp, debug=True)
+        rep = parity.compare(inp, out)
+        parity.compare_debug(inp, dbg)
+        total["exact"] += rep["exact"]
+        total["B"] += rep["B"]
+    assert total["exact"] == total["B"]
+
+
+def test_paged_bf16_forced_scenarios(ver):
+    inp = W.paged_bf16()
+    out, dbg, _, _ = run(ver, inp, debug=True)
+    report("paged_bf16", parity.compare(inp, out))
+    parity.compare_debug(inp, dbg)
+    acc = out["accepted"].cpu().numpy()
+    for b, r in inp["forced_reject_at"].items():
+        assert acc[b] == (inp["k"][b] if r is None else r), (b, acc[b], r)
+
+
+def test_ragged_probs_top_p(ver):
+    inp = W.ragged_probs()
+    out, dbg, _, _ = run(ver, inp, debug=True)
+    report("ragged_probs", parity.compare(inp, out))
+    assert parity.compare_debug(inp, dbg) > 0
+
+
+@pytest.mark.parametrize("top_p", [0.95, 1.0])
+def test_verify_b64_k4(ver, top_p):
+    inp = W.verify_b64_k4(top_p=top_p)
+    out, dbg, _, _ = run(ver, inp, debug=True)
+    report(f"verify_b64_k4 top_p={top_p}", parity.compare(inp, out))
+    assert parity.compare_debug(inp, dbg) > 0
+
+
+def test_greedy_shared(ver):
+    inp = W.greedy_shared()
+    out, _, _, _ = run(ver, inp)
+    report("greedy_shared", parity.compare(inp, out))
+
+
+@pytest.mark.parametrize("V,sigma", [(32000, 0.25), (32000, 4.0), (128256, 1.0), (256000, 0.25)])
+def test_sweep_subset(ver, V, sigma):
+    inp = W.sweep(B=16, V=V, sigma=sigma)
+    out, _, _, _ = run(ver, inp)
+    report(f"sweep V={V} sigma={sigma}", parity.compare(inp, out))
+
+
+# --------------------------------------------------------------------------- #
+# normalised rows, skipping, repeat calls
+# --------------------------------------------------------------------------- #
+@pytest.mark.parametrize("top_p", [1.0, 0.9])
+def test_normalised_rows_match_oracle(ver, top_p):
+    inp = W.paged_bf16(V=4093, forced=False)       # ragged tail: 4093 is not a multiple of 8
+    inp["top_p"][:] = top_p
+    inp["temperature"][::3] = 0.0
+    _, _, pp, pq = run(ver, inp, flags=binding.FLAG_NO_SKIP, probs=True)
+    pp, pq = pp.cpu().numpy(), pq.cpu().numpy()
+    for b in range(inp["k"].shape[0]):
+        T, tp = inp["temperature"][b], inp["top_p"][b]
+        for i in range(int(inp["k"][b]) + 1):
+            p, info = S.transform(S.decode(inp["target"][b, i], "bf16"), "logits", T, tp)
+            if info["margin"] < parity.TOL:
+                continue
+            np.testing.assert_allclose(pp[b, i], p, atol=parity.PROB_TOL, rtol=0)
+            if i < inp["k"][b]:
+                q, info = S.transform(S.decode(inp["draft"][b, i], "bf16"), "logits", T, tp)
+                if info["margin"] >= parity.TOL:
+                    np.testing.assert_allclose(pq[b, i], q, atol=parity.PROB_TOL, rtol=0)
+
+
+def test_skipping_does_not_change_outputs(ver):
+    inp = W.verify_b64_k4(B=32, V=32000)
+    a, _, _, _ = run(ver, inp)
+    b, dbg, _, _ = run(ver, inp, flags=binding.FLAG_NO_SKIP, debug=True)
+    for key in ("accepted", "out_tokens", "num_emitted", "status"):
+        assert torch.equal(a[key], b[key])
+    states = dbg.cpu().numpy()[:, :, 5]
+    assert (states != binding.ROW_SKIPPED).all()
+
+
+def test_repeated_calls_reuse_workspace(ver):
+    inp = W.paged_bf16(V=8192, forced=False)
+    first, _, _, _ = run(ver, inp)
+    first = {k: v.clone() for k, v in first.items()}
+    for _ in range(3):
+        again, _, _, _ = run(ver, inp)
+        for key in first:
+            assert torch.equal(first[key], again[key])
+    small = W.small_fp32()
+    out, _, _, _ = run(ver, small)
+    parity.compare(small, out)
+
+
+# --------------------------------------------------------------------------- #
+# laws on small vocabularies
+# --------------------------------------------------------------------------- #
+def test_toy_lab_acceptance_rate_and_residual(ver):
+    """p = [.5,.3,.2], q = [.2,.5,.3]: acceptance 0.7 and every rejection emits
+    token 0 (section 5 toy lab), over 10^6 seeded trials."""
+    n = 1_000_000
+    p = np.array([0.5, 0.3, 0.2])
+    q = np.array([0.2, 0.5, 0.3])
+    rng = np.random.default_rng(0)
+    target = torch.tensor(np.log(p), dtype=torch.float32).repeat(n, 2, 1)
+    target = torch.nn.functional.pad(target, (0, 1), value=float("-inf")).cuda()
+    draft = torch.nn.functional.pad(torch.tensor(q, dtype=torch.float32).repeat(n, 1, 1),
+                                    (0, 1)).cuda()
+    tokens = torch.tensor(rng.choice(3, size=(n, 1), p=q), dtype=torch.int32).cuda()
+    out = ver.verify(target=target, draft=draft, draft_tokens=tokens, V=3,
+                     temperature=torch.ones(n, device="cuda"), draft_kind="probs", seed=99,
+                     request_id=torch.arange(n, dtype=torch.int32, device="cuda"))
+    acc = out["accepted"].cpu().numpy()
+    tok = out["out_tokens"].cpu().numpy()
+    rate = acc.mean()
+    assert abs(rate - 0.7) < 5 * np.sqrt(0.21 / n)
+    assert (tok[acc == 0, 0] == 0).all()
+    counts = np.bincount(tok[:, 0], minlength=3)
+    assert stats.chisquare(counts, p * n).pvalue > 1e-4
+
+
+@pytest.mark.parametrize("V,T,top_p,kind", [(3, 1.0, 1.0, "logits"), (8, 0.7, 1.0, "probs"),
+                                            (16, 1.3, 0.9, "logits")])
+def test_emitted_law_chi_square(ver, V, T, top_p, kind):
+    n = 200_000
+    inp = W.tiny(V=V, k=2, B=n, T=T, top_p=top_p, seed=21 + V, draft_kind=kind)
+    out, _, _, _ = run(ver, inp)
+    tok = out["out_tokens"].cpu().numpy()
+    nem = out["num_emitted"].cpu().numpy()
+    for i in range(2):
+        reach = nem > i
+        p, _ = S.transform(inp["target"][0, i].astype(np.float64), "logits", T, top_p)
+        counts = np.bincount(tok[reach, i], minlength=V)
+        sup = p > 0
+        assert counts[~sup].sum() == 0
+        assert stats.chisquare(counts[sup], p[sup] / p[sup].sum() * reach.sum()).pvalue > 1e-4
+    sub = {k: (v[:3000] if isinstance(v, np.ndarray) and v.shape[:1] == (n,) else v)
+           for k, v in inp.items()}
+    parity.compare(sub, {k: v[:3000] for k, v in out.items()})
+
+
+# --------------------------------------------------------------------------- #
+# edge cases
+# --------------------------------------------------------------------------- #
+def test_plain_decode_k0_and_ragged(ver):
+    inp = W.ragged_probs(B=12, kmax=5, V=1000)
+    inp["k"][:4] = 0
+    out, _, _, _ = run(ver, inp)
+    parity.compare(inp, out)
+    assert (out["num_emitted"].cpu().numpy()[:4] == 1).all()
+
+
+def test_greedy_ties(ver):
+    inp = W.tiny(V=64, k=3, B=512, T=0.0, seed=5, target_dtype="bf16", draft_dtype="bf16")
+    t = inp["target"]
+    top = W.to_bf16_bits(np.float32(W.bf16_bits_to_f32(t).max() + 1.0))
+    t[:, :, 7] = t[:, :, 11] = top          # tied maxima in every target row
+    out, _, _, _ = run(ver, inp)
+    parity.compare(inp, out)
+    tok = out["out_tokens"].cpu().numpy()
+    last = tok[np.arange(512), out["accepted"].cpu().numpy()]
+    assert set(np.unique(last)) <= {7, 11}
+
+
+def test_bad_inputs_are_flagged(ver):
+    inp = W.tiny(V=40, k=2, B=8, seed=3, target_dtype="bf16", draft_dtype="bf16")
+    inp["target"][0, 0, 5] = 0x7FC0                       # NaN
+    inp["target"][1, 0, :] = W.BF16_NEG_INF               # no support
+    inp["draft"][2, 0, 3] = 0x7F80                        # +inf
+    inp["temperature"][3] = -1.0
+    inp["top_p"][4] = 0.0
+    inp["tokens"][5, 0] = 40                              # token id == V
+    inp["k"][6] = 7                                       # k > kmax
+    out, _, _, _ = run(ver, inp)
+    acc = out["accepted"].cpu().numpy()
+    st = out["status"].cpu().numpy()
+    for b in range(7):
+        assert acc[b] == -1 and st[b] == binding.ST_BAD_INPUT, b
+        assert (out["out_tokens"][b] == -1).all()
+    parity.compare(inp, out)
+
+
+def test_q_zero_flag(ver):
+    inp = W.tiny(V=16, k=1, B=4, seed=8, draft_kind="probs")
+    for b in range(4):
+        inp["draft"][b, 0, int(inp["tokens"][b, 0])] = 0.0
+    out, _, _, _ = run(ver, inp)
+    assert (out["status"].cpu().numpy() & binding.ST_Q_ZERO).all()
+    parity.compare(inp, out)
+
+
+def test_host_checks_launch_nothing(ver):
+    inp = W.tiny(V=16, k=1, B=4, seed=8)
+    dev = device_io.to_device(inp, "cuda:0")
+    bad = dev["target"][:, :, 1:]                         # misaligned base pointer
+    with pytest.raises(binding.SvError) as e:
+        ver.verify(**{**dev, "target": bad, "V": 3})
+    assert e.value.code == binding.SV_ERR_INVALID
+    empty = {k: (v[:0] if isinstance(v, torch.Tensor) else v) for k, v in dev.items()}
+    ver.verify(**empty)                                   # B = 0 is a no-op

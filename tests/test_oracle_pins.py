@@ -148,7 +148,7 @@ def test_top_p_against_brute_force():
             dist = np.round(dist * 8) + 1
             dist = dist / dist.sum()
         top_p = float(np.float32(rng.uniform(0.05, 0.999)))
-        _, kept, tau = S.nucleus(dist, top_p)
+        _, kept, tau, margin = S.nucleus(dist, top_p)
         np.testing.assert_array_equal(kept, _brute_force_nucleus(dist, top_p))
         assert dist[kept].sum() >= top_p - 1e-15
     # top_p = 1 is the plain softmax
