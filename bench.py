@@ -1,0 +1,434 @@
+"""Throughput of the speculative-decoding verification cycle on GB300.
+
+One step = one pass of the whole hot path over one batch of the throughput
+workload (B = 64 requests, k = 4 drafts, V = 128256, bf16 target and draft
+logits, T = 0.8, top-p 0.95 on p and q, paged KV with 16-slot blocks,
+S_b ~ U[128, 8192]):
+    bfl_reserve  (lookahead blocks for the verify pass)
+    spec_verify  (accept / reject / correction or bonus per request)
+    kv_commit_rollback (commit the accepted prefix, free the rejected tail)
+The metric is verified rows per second (sum_b (k_b + 1) target rows per
+step).  Inputs rotate over 4 independent batches (4 x 148 MB, larger than L2).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle on this host as the reference arm
+(a bounded sample of the same workload per step).  Under torchrun (N > 1)
+every rank runs its own batch (the path shards by request; no collective on
+the data path); rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = dict(workload="verify_b64_k4", B=64, k=4, V=128256, input_dtype="bf16",
+                temperature=0.8, top_p=0.95, block_size=16, prefix="U[128,8192]")
+METRIC = "verify rows/s & HBM GB/s vs 8 TB/s at B=64 k=4 V=128256 bf16"
+N_SETS = 4
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 20):
+        self.cmd = ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                    "--format=csv,noheader,nounits", "-lms", str(period_ms)]
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+                self.lines = [l for l in out.splitlines() if l.strip()]
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def build_sets(n_sets):
+    from speculative_decoding_verification_07_gb300 import workloads as W
+    sets = []
+    for s in range(n_sets):
+        inp = W.verify_b64_k4(index=5 + 97 * s)
+        inp["seed"] = 2005 + s
+        sets.append(inp)
+    return sets
+
+
+def rows_per_step(inp):
+    return int((inp["k"].astype(np.int64) + 1).sum())
+
+
+def full_bytes(inp):
+    """B_full: every target row (k_b + 1) and draft row (k_b) of the batch, plus
+    the per-request metadata read and written (tokens, k, T, top_p, ids,
+    seq_len, outputs)."""
+    V = inp["target"].shape[-1]
+    k = inp["k"].astype(np.int64)
+    rows = ((k + 1) * V * 2 + k * V * 2).sum()
+    meta = (4 * k + 4 * (k + 1) + 24).sum()
+    return int(rows + meta)
+
+
+def needed_bytes(inp, accepted):
+    """B_min: the rows the method must read -- target rows 0..a_b and draft rows
+    0..min(a_b, k_b - 1) (every row after the first rejection is discarded)."""
+    V = inp["target"].shape[-1]
+    k = inp["k"].astype(np.int64)
+    a = np.asarray(accepted, np.int64)
+    return int(((a + 1) * V * 2 + np.minimum(a + 1, k) * V * 2).sum())
+
+
+# --------------------------------------------------------------------------- #
+# reference arm: the fp64 oracle on the host
+# --------------------------------------------------------------------------- #
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from oracle import sampling as S
+    inp = build_sets(1)[0]
+    B = inp["k"].shape[0]
+
+    def step(t):
+        b = t % B
+        kb = int(inp["k"][b])
+        tr = S.decode(inp["target"][b, :kb + 1], "bf16")
+        dr = S.decode(inp["draft"][b, :kb], "bf16")
+        S.verify_request(tr, dr, inp["tokens"][b, :kb], kb, inp["temperature"][b],
+                         inp["top_p"][b], "logits", inp["seed"], int(inp["request_id"][b]),
+                         int(inp["seq_len"][b]))
+        return kb + 1
+
+    t0 = time.perf_counter()
+    step(0)
+    per = time.perf_counter() - t0
+    budget = 180.0
+    steps = args.steps
+    if (args.steps + args.warmup) * per > budget:
+        steps = max(3, int(budget / per) - args.warmup)
+    for t in range(args.warmup):
+        step(t)
+    rows = 0
+    t0 = time.perf_counter()
+    for t in range(steps):
+        rows += step(t)
+    el = time.perf_counter() - t0
+    value = rows / el
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
+            "n_gpus": ws, "steps": steps, "steps_requested": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": dict(WORKLOAD, sample="one request of the batch per step (k_b + 1 rows)",
+                           parallelism="single host process"),
+            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{steps} requests of one verify_b64_k4 batch"},
+            "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def cpu_baseline(inp, seconds=12.0):
+    """The oracle as it stands on this host, bounded to about `seconds`."""
+    from oracle import sampling as S
+    B = inp["k"].shape[0]
+    rows = n = 0
+    t0 = time.perf_counter()
+    while (time.perf_counter() - t0 < seconds or n < 2) and n < B:
+        b = n
+        kb = int(inp["k"][b])
+        S.verify_request(S.decode(inp["target"][b, :kb + 1], "bf16"),
+                         S.decode(inp["draft"][b, :kb], "bf16"), inp["tokens"][b, :kb], kb,
+                         inp["temperature"][b], inp["top_p"][b], "logits", inp["seed"],
+                         int(inp["request_id"][b]), int(inp["seq_len"][b]))
+        rows += kb + 1
+        n += 1
+    el = time.perf_counter() - t0
+    return {"value": rows / el, "unit": "rows/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {n} of {B} requests of one verify_b64_k4 batch "
+                      f"({rows} rows, {el:.1f} s, numpy fp64, one thread)"}
+
+
+# --------------------------------------------------------------------------- #
+# our arm
+# --------------------------------------------------------------------------- #
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from speculative_decoding_verification_07_gb300 import binding, device_io
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+
+    sets = build_sets(N_SETS)
+    B, k, V = 64, 4, 128256
+    rows = rows_per_step(sets[0])
+    ver = binding.Verifier(local)
+    dsets = [device_io.to_device(s, dev) for s in sets]
+    for d, s in zip(dsets, sets):
+        d["request_id"] = d["request_id"] + rank * 1000003
+    BS = 16
+    steps_total = args.warmup + args.steps + 64 * 4 + 16
+    max_blocks = (8192 + (k + 1) * steps_total) // BS + 4
+    pool = binding.BlockPool(ver.handle, B * max_blocks, BS)
+    table = torch.full((B, max_blocks), -1, dtype=torch.int32, device=dev)
+    seq = torch.zeros(B, dtype=torch.int32, device=dev)
+    S0 = torch.tensor(sets[0]["seq_len"], dtype=torch.int32, device=dev)
+    pool.reserve(seq, S0 - 1, table)
+    seq.copy_(S0)
+    kk = dsets[0]["k"]
+    outs = [ver.outputs(B, k) for _ in range(N_SETS)]
+    ev = {}
+
+    def step(i, stream=None, timed_verify=False):
+        d = dsets[i % N_SETS]
+        o = outs[i % N_SETS]
+        pool.reserve(seq, kk, table, stream=stream)
+        a = binding.make_args(target=d["target"], draft=d["draft"], draft_tokens=d["draft_tokens"],
+                              temperature=d["temperature"], k=d["k"], top_p=d["top_p"],
+                              seed=d["seed"], request_id=d["request_id"], seq_len=seq,
+                              draft_kind="logits", **o)
+        wsp = ver.ensure_workspace(a)
+        if timed_verify:
+            # keep the stream busy while the host enqueues event, kernel, event,
+            # so the events bracket the kernel alone
+            torch.cuda._sleep(200_000)
+            ev[i][0].record()
+        binding.spec_verify(ver.handle, a, wsp, stream)
+        if timed_verify:
+            ev[i][1].record()
+        pool.commit_rollback(kk, o["accepted"], seq, table, stream=stream)
+
+    # warm-up (eager), then capture a graph of G steps cycling the input sets
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize()
+    assert ver.error() == 0, "device error during warm-up"
+    G = 8
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            for i in range(G):
+                step(i, stream=s)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for _ in range(2):
+            graph.replay()
+    torch.cuda.synchronize()
+
+    reps = max(1, args.steps // G)
+    K = reps * G
+    t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk, torch.cuda.stream(s):
+        t0e.record(s)
+        for _ in range(reps):
+            graph.replay()      # replays on the current stream, s
+        t1e.record(s)
+        torch.cuda.synchronize()
+    barrier()
+    ms = t0e.elapsed_time(t1e)
+    assert ver.error() == 0, "device error in the timed region"
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = ws * rows * K / (ms / 1e3)
+
+    # verify-kernel duration: CUDA events around each launch of G more steps
+    nv = 4 * G
+    for i in range(nv):
+        ev[i] = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    for i in range(nv):
+        step(i, timed_verify=True)
+    torch.cuda.synchronize()
+    vms = float(np.mean([ev[i][0].elapsed_time(ev[i][1]) for i in range(nv)]))
+    bfull = float(np.mean([full_bytes(sets[i % N_SETS]) for i in range(N_SETS)]))
+    bmin = float(np.mean([needed_bytes(sets[i % N_SETS], outs[i % N_SETS]["accepted"].cpu().numpy())
+                          for i in range(N_SETS)]))
+    peak, peak_src = measured_peaks()
+    achieved = bfull / (vms / 1e3) / 1e9
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "verify_traffic.json")
+    if os.path.exists(tpath):
+        try:
+            tj = json.load(open(tpath))
+            if tj.get("kernel_source_sha") == kernel_source_sha():
+                traffic = tj.get("bytes_per_launch")
+        except Exception:
+            traffic = None
+
+    # end to end through the public API with host buffers (pinned)
+    e2e = e2e_run(ver, sets, dev, args, pool, table, seq, kk, B, k)
+
+    line = {"metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": ws, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": dict(WORKLOAD, parallelism=f"replicas x{ws} (requests shard, no collective)",
+                           step="bfl_reserve + spec_verify + kv_commit_rollback",
+                           launch=f"CUDA graph of {G} steps",
+                           l2=f"inputs rotate over {N_SETS} batches of "
+                              f"{full_bytes(sets[0]) / 1e6:.1f} MB (> L2)"),
+            "gpu_launches": 3 * K,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "kernel": "verify_kernel<bf16,bf16>",
+                         "kernel_ms": vms, "bytes_full_per_launch": bfull,
+                         "bytes_needed_per_launch": bmin,
+                         "achieved_needed": bmin / (vms / 1e3) / 1e9,
+                         "peak_source": peak_src,
+                         "frac_of_8tbs": achieved / 8000.0},
+            "clocks": clk.summary(),
+            "e2e": e2e}
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(sets[0])
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    ver.close()
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def e2e_run(ver, sets, dev, args, pool, table, seq, kk, B, k):
+    """rows/s through the public API with the step's inputs in pinned host
+    memory: H2D copies, reserve + verify + commit, D2H of the outputs, per step."""
+    import torch
+
+    from speculative_decoding_verification_07_gb300 import binding, device_io
+    hsets = [device_io.to_device(s, None, pin=True) for s in sets]
+    dbuf = device_io.to_device(sets[0], dev)
+    o = ver.outputs(B, k)
+    ho = {key: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for key, v in o.items()}
+    keys = ("target", "draft", "draft_tokens", "k", "temperature", "top_p", "request_id")
+    h2d = sum(hsets[0][key].numel() * hsets[0][key].element_size() for key in keys)
+    d2h = sum(v.numel() * v.element_size() for v in ho.values())
+    n = max(8, min(64, args.steps // 20))
+
+    def one(i):
+        h = hsets[i % N_SETS]
+        for key in keys:
+            dbuf[key].copy_(h[key], non_blocking=True)
+        pool.reserve(seq, dbuf["k"], table)
+        ver.verify(target=dbuf["target"], draft=dbuf["draft"], draft_tokens=dbuf["draft_tokens"],
+                   temperature=dbuf["temperature"], k=dbuf["k"], top_p=dbuf["top_p"],
+                   seed=h["seed"], request_id=dbuf["request_id"], seq_len=seq, out=o)
+        pool.commit_rollback(dbuf["k"], o["accepted"], seq, table)
+        for key in o:
+            ho[key].copy_(o[key], non_blocking=True)
+
+    for i in range(3):
+        one(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(n):
+        one(i)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    rows = rows_per_step(sets[0])
+    return {"value": rows * n / (ms / 1e3), "unit": "rows/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": n}
+
+
+def kernel_source_sha():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("verify_kernel.cuh", "verify.cu", "verify_bf16.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "speculative_decoding_verification_07_gb300", "csrc", f),
+                  "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

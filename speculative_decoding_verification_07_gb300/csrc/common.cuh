@@ -12,6 +12,14 @@ struct sv_handle {
   int device;
   int num_sms;
   int* d_err;  // device error word: 0 or the first sv_status a kernel reported
+  // launch cache: co-resident clusters per (kernel, cluster size), filled on
+  // first use so later calls (and stream capture) make no occupancy query
+  static constexpr int kCache = 32;
+  const void* occ_fn[kCache];
+  int occ_c[kCache];
+  size_t occ_smem[kCache];
+  int occ_val[kCache];
+  int occ_n;
 };
 
 namespace sv {

@@ -14,16 +14,15 @@ struct Variant {
   KernelFn fn;
   int eb_t, eb_d;
   bool probs;
-  int ng_max;
 };
 
 static const Variant kVariants[] = {
-    {kernel_bf16_bf16_logits(), 2, 2, false, 8},  // bf16 target, bf16 draft logits
-    {kernel_bf16_f32_probs(), 2, 4, true, 4},     // bf16 target, fp32 draft probabilities
-    {kernel_bf16_f32_logits(), 2, 4, false, 4},   // bf16 target, fp32 draft logits
-    {kernel_f32_f32_logits(), 4, 4, false, 4},    // fp32 target, fp32 draft logits
-    {kernel_f32_f32_probs(), 4, 4, true, 4},      // fp32 target, fp32 draft probabilities
-    {kernel_f32_bf16_logits(), 4, 2, false, 4},   // fp32 target, bf16 draft logits
+    {kernel_bf16_bf16_logits(), 2, 2, false},  // bf16 target, bf16 draft logits
+    {kernel_bf16_f32_probs(), 2, 4, true},     // bf16 target, fp32 draft probabilities
+    {kernel_bf16_f32_logits(), 2, 4, false},   // bf16 target, fp32 draft logits
+    {kernel_f32_f32_logits(), 4, 4, false},    // fp32 target, fp32 draft logits
+    {kernel_f32_f32_probs(), 4, 4, true},      // fp32 target, fp32 draft probabilities
+    {kernel_f32_bf16_logits(), 4, 2, false},   // fp32 target, bf16 draft logits
 };
 
 static int elem_bytes(int dt) { return dt == SV_BF16 ? 2 : 4; }
@@ -76,9 +75,9 @@ extern "C" sv_status spec_verify(sv_handle* h, const sv_verify_args* a, void* ws
     if (v.eb_t == ebt && v.eb_d == ebd && v.probs == probs) var = &v;
   if (!var) return SV_ERR_UNSUPPORTED;
 
-  // Cluster size: smallest power of two whose register capacity covers V,
+  // Cluster size: smallest power of two whose slices fit kMaxBlk TMA blocks,
   // then grown while the grid would leave SMs idle.
-  const int cap = kThreads * kGroup * var->ng_max;
+  const int cap = kMaxBlk * kBlk;
   int C = 1;
   while (C < kMaxCluster && (size_t)C * cap < (size_t)a->V) C <<= 1;
   if ((size_t)C * cap < (size_t)a->V) return SV_ERR_UNSUPPORTED;
@@ -86,7 +85,8 @@ extern "C" sv_status spec_verify(sv_handle* h, const sv_verify_args* a, void* ws
   while (C < 8 && rows * (size_t)C < (size_t)h->num_sms * 2) C <<= 1;
   int slice = (int)(((size_t)a->V + C - 1) / C);
   slice = (slice + kGroup - 1) / kGroup * kGroup;
-  const int ng = (slice + kThreads * kGroup - 1) / (kThreads * kGroup);
+  const int d_off = (slice * ebt + 127) / 128 * 128;
+  const size_t dyn = (size_t)d_off + (size_t)slice * ebd;
 
   KParams P;
   P.B = a->B, P.kmax = a->kmax, P.V = a->V, P.flags = a->flags;
@@ -100,7 +100,7 @@ extern "C" sv_status spec_verify(sv_handle* h, const sv_verify_args* a, void* ws
   P.hdr = (uint32_t*)ws;
   P.row_state = (uint32_t*)((char*)ws + kHdrBytes);
   P.err = h->d_err;
-  P.slice = slice, P.ng = ng, P.n_tickets = (int)n_tickets;
+  P.slice = slice, P.d_off = d_off, P.n_tickets = (int)n_tickets;
   P.spin_limit = kDefaultSpin;
 
   cudaLaunchConfig_t cfg = {};
@@ -112,16 +112,31 @@ extern "C" sv_status spec_verify(sv_handle* h, const sv_verify_args* a, void* ws
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = dyn;
   cfg.stream = (cudaStream_t)stream;
-  if (C > 8)
-    SV_CUDA_TRY(cudaFuncSetAttribute(var->fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
-  cfg.gridDim = dim3((unsigned)C);
   int max_clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&max_clusters, var->fn, &cfg) != cudaSuccess ||
-      max_clusters < 1) {
-    (void)cudaGetLastError();
-    return SV_ERR_UNSUPPORTED;
+  for (int i = 0; i < h->occ_n; ++i)
+    if (h->occ_fn[i] == (const void*)var->fn && h->occ_c[i] == C && h->occ_smem[i] == dyn)
+      max_clusters = h->occ_val[i];
+  // the attribute is per function: set it for every launch (other shapes may
+  // have lowered it since the occupancy of this shape was cached)
+  SV_CUDA_TRY(cudaFuncSetAttribute(var->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
+  if (max_clusters == 0) {
+    if (C > 8)
+      SV_CUDA_TRY(cudaFuncSetAttribute(var->fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
+    cfg.gridDim = dim3((unsigned)C);
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, var->fn, &cfg) != cudaSuccess ||
+        max_clusters < 1) {
+      (void)cudaGetLastError();
+      return SV_ERR_UNSUPPORTED;
+    }
+    if (h->occ_n < sv_handle::kCache) {
+      h->occ_fn[h->occ_n] = (const void*)var->fn;
+      h->occ_c[h->occ_n] = C;
+      h->occ_smem[h->occ_n] = dyn;
+      h->occ_val[h->occ_n] = max_clusters;
+      ++h->occ_n;
+    }
   }
   const size_t nclusters = rows < (size_t)max_clusters ? rows : (size_t)max_clusters;
   cfg.gridDim = dim3((unsigned)(nclusters * C));

@@ -11,29 +11,37 @@
 //
 // GB300 design
 //  * One thread-block cluster of C CTAs owns one (request, position) row pair:
-//    the target row and, for i < k_b, the draft row.  Each CTA streams its
-//    1/C vocabulary slice once from HBM with 128-bit coalesced loads straight
-//    into registers and keeps it there, so every later sweep (top-p histogram,
-//    accept test, race) runs on-chip.  Row statistics are combined through
-//    distributed shared memory (DSMEM) across the cluster.
-//  * Single-sweep statistics: an online (max, sum of 2^((v-m)c)) per thread,
-//    combined by rescaling; greedy rows (T = 0) count tied maxima instead.
-//  * Top-p: a 256-bin histogram over the order-key distance from the row
-//    maximum; for bf16 rows the first window is exact (one bin per bf16 value,
-//    integer counts, deterministic).  Wider ranges descend radix-wise.
+//    the target row and, for i < k_b, the draft row.  Each CTA pulls its 1/C
+//    vocabulary slice of both rows from HBM once, with 1-D TMA bulk copies
+//    (cp.async.bulk, one mbarrier per 2048-element block) into shared memory,
+//    and every pass (statistics, top-p histogram, race) then reads shared
+//    memory in compact rolled loops; the statistics sweep starts on each block
+//    as soon as it lands.  Row statistics are combined across the cluster
+//    through distributed shared memory (DSMEM), one warp gathering the C
+//    partials in parallel.
+//  * One sweep for the statistics: per 8-element group a packed bf16x2 max,
+//    then an online sum of 2^((v - m) c) with paired fp32 (f32x2) add/multiply;
+//    NaN / +inf inputs surface in the sums, so no per-element check is paid.
+//    Greedy rows (T = 0) count tied maxima instead.
+//  * Top-p: for bf16 rows an exact 256-bin count histogram of the bf16 order
+//    key below the row maximum, filled through a packed window compare; rows
+//    whose boundary lies deeper (and fp32 rows) descend radix-wise.
 //  * Rows are handed out by a ticket counter in (position, request) order, so
-//    a row only ever waits on rows with earlier tickets, which are already
-//    held by running clusters (no deadlock); every wait is bounded.  A row
-//    whose request already has a known earlier rejection is skipped without
-//    being loaded.  Exactly one row per request -- the first rejection, or the
-//    bonus row -- runs the race, and writes the request's outputs.
-//  * The race prunes 4-token Philox groups that cannot beat the running best
-//    (w / E_min below it) and evaluates an accurate logf only for candidates
-//    the fast MUFU estimate cannot rule out.
+//    a row only ever waits on rows with earlier tickets, which running
+//    clusters already hold (no deadlock); every wait is bounded.  A row whose
+//    request already has a known earlier rejection is skipped without being
+//    loaded, so the bytes read approach the rows the method needs.  Exactly
+//    one row per request -- the first rejection, or the bonus row -- runs the
+//    race and writes the request's outputs.
+//  * The race filters whole 8-element groups by one value threshold (the
+//    top-p boundary, or the bound w / E_min below the running best) before
+//    any Philox work, and evaluates an accurate logf only for candidates the
+//    fast MUFU estimate cannot rule out.
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <float.h>
 #include <math.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include "common.cuh"
@@ -44,11 +52,14 @@ namespace sv {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kGroup = 8;               // elements per register group (one 16-byte bf16 vector)
+constexpr int kGroup = 8;  // elements per group (one 16-byte bf16 vector)
+constexpr int kBlk = kThreads * kGroup;  // elements per TMA block (one group per thread)
+constexpr int kMaxBlk = 8;               // blocks per slice: slices hold <= 16384 elements
 constexpr uint32_t kNoFilter = 0xFFFFFFFFu;
 constexpr int kMaxCluster = 16;
 constexpr int kMaxK = 64;
 constexpr int kDefaultSpin = 1 << 20;
+constexpr float kEminSafe = 5.9604e-8f;  // <= -ln(1 - 2^-24), the smallest E
 
 // workspace header words
 constexpr int kHdrEpoch = 0, kHdrTicket = 1, kHdrDone = 2;
@@ -81,14 +92,35 @@ struct KParams {
   uint32_t* hdr;
   uint32_t* row_state;
   int* err;
-  int slice;      // elements per CTA (multiple of 8)
-  int ng;         // register groups per thread in use (<= NG)
+  int slice;      // elements per CTA (multiple of 8, <= kMaxBlk * kBlk)
+  int d_off;      // byte offset of the draft slice in dynamic shared memory
   int n_tickets;  // (kmax + 1) * B
   int spin_limit;
 };
 
 // ---------------------------------------------------------------------------
-// Register groups of 8 elements: 4 words of bf16 pairs or 8 fp32 words.
+// packed arithmetic (sm_100+: f32x2; sm_90+: bf16x2)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float2 f2add(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 f2mul(float2 a, float2 b) { return __fmul2_rn(a, b); }
+
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// bit 0: low half >= thr, bit 1: high half >= thr (NaN compares false)
+__device__ __forceinline__ uint32_t bge2(uint32_t a, uint32_t thr2) {
+  uint32_t r;
+  asm("{.reg .pred p, q; setp.ge.bf16x2 p|q, %1, %2; selp.u32 %0, 1, 0, p; @q or.b32 %0, %0, 2;}"
+      : "=r"(r)
+      : "r"(a), "r"(thr2));
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// Groups of 8 elements in registers: 4 words of bf16 pairs or 8 fp32 words.
 // ---------------------------------------------------------------------------
 template <int EB>
 struct Grp {
@@ -103,6 +135,44 @@ __device__ __forceinline__ float gval(const Grp<EB>& g, int e) {
   } else {
     return __uint_as_float(g.w[e]);
   }
+}
+
+// elements (2p, 2p+1) of a group as a float pair
+template <int EB>
+__device__ __forceinline__ float2 gpair(const Grp<EB>& g, int p) {
+  if constexpr (EB == 2) {
+    const uint32_t x = g.w[p];
+    return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
+  } else {
+    return make_float2(__uint_as_float(g.w[2 * p]), __uint_as_float(g.w[2 * p + 1]));
+  }
+}
+
+template <int EB>
+__device__ __forceinline__ float group_max(const Grp<EB>& g) {
+  if constexpr (EB == 2) {
+    const uint32_t m = bmax2(bmax2(g.w[0], g.w[1]), bmax2(g.w[2], g.w[3]));
+    return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
+  } else {
+    float m = __uint_as_float(g.w[0]);
+#pragma unroll
+    for (int e = 1; e < 8; ++e) m = fmaxf(m, __uint_as_float(g.w[e]));
+    return m;
+  }
+}
+
+// 8-bit mask of the group's elements >= thr (thr2 = thr as a packed bf16 pair)
+template <int EB>
+__device__ __forceinline__ uint32_t group_ge(const Grp<EB>& g, float thr, uint32_t thr2) {
+  uint32_t m = 0;
+  if constexpr (EB == 2) {
+#pragma unroll
+    for (int p = 0; p < 4; ++p) m |= bge2(g.w[p], thr2) << (2 * p);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) m |= (__uint_as_float(g.w[e]) >= thr ? 1u : 0u) << e;
+  }
+  return m;
 }
 
 // Key used for top-p distances: bf16 rows use the 16-bit bf16 order key,
@@ -121,33 +191,24 @@ __device__ __forceinline__ float vkey_value(uint32_t k) {
   }
 }
 
-// Streaming 16-byte load (read once; do not keep in L1).
-__device__ __forceinline__ uint4 ld_stream(const void* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
+// Packed bf16 pair of the largest bf16 value <= v (v itself when v is a bf16
+// value), so that "x >= pair" over bf16 x never drops an x >= v.
+__device__ __forceinline__ uint32_t bf16_pair_of(float v) {
+  const uint32_t u = __float_as_uint(v);
+  uint32_t h = u >> 16;
+  if ((u & 0x8000FFFFu) > 0x80000000u) h += 1u;  // negative with dropped bits: round down
+  return h | (h << 16);
 }
 
-// Load one group of 8 elements starting at absolute element x of a row; lanes
-// at or beyond `end` get the neutral value (-inf logits / 0 probabilities).
 template <int EB, bool PROBS>
-__device__ __forceinline__ void load_group(Grp<EB>& g, const char* row, int x, int end) {
-  const uint32_t neutral = PROBS ? 0u : (EB == 2 ? 0xFF80FF80u : 0xFF800000u);
-#pragma unroll
-  for (int j = 0; j < EB * 2; ++j) g.w[j] = neutral;
-  if (x >= end) return;
-  const char* p = row + (size_t)x * EB;
-  uint4 a = ld_stream(p);
-  g.w[0] = a.x, g.w[1] = a.y, g.w[2] = a.z, g.w[3] = a.w;
-  if constexpr (EB == 4) {
-    if (x + 4 < end) {
-      uint4 b2 = ld_stream(p + 16);
-      g.w[4] = b2.x, g.w[5] = b2.y, g.w[6] = b2.z, g.w[7] = b2.w;
-    }
-  }
-  if (x + kGroup > end) {  // ragged tail of the row: neutralise lanes >= end
+__device__ __forceinline__ uint32_t neutral_word() {
+  return PROBS ? 0u : (EB == 2 ? 0xFF80FF80u : 0xFF800000u);
+}
+
+// Neutralise lanes at or beyond `end` (only the group holding the row's end).
+template <int EB, bool PROBS>
+__device__ __forceinline__ void mask_group(Grp<EB>& g, int x, int end) {
+  if (x < end && x + kGroup > end) {
 #pragma unroll
     for (int e = 0; e < kGroup; ++e) {
       if (x + e >= end) {
@@ -156,7 +217,7 @@ __device__ __forceinline__ void load_group(Grp<EB>& g, const char* row, int x, i
           uint32_t& w = g.w[e >> 1];
           w = (e & 1) ? ((w & 0x0000FFFFu) | (n16 << 16)) : ((w & 0xFFFF0000u) | n16);
         } else {
-          g.w[e] = neutral;
+          g.w[e] = neutral_word<EB, PROBS>();
         }
       }
     }
@@ -167,16 +228,17 @@ __device__ __forceinline__ void load_group(Grp<EB>& g, const char* row, int x, i
 // Per-row transform parameters (identical in every CTA of the cluster).
 // ---------------------------------------------------------------------------
 struct RowP {
-  float m;          // maximum raw value (logit, or probability)
-  float mz;         // maximum in the weight domain (logit, or lg2(prob)/T)
-  float c;          // weight scale: log2(e)/T for logits, 1 for probabilities
-  float invT;       // 1/T (probabilities)
-  bool greedy;      // T == 0
-  float S;          // sum of weights over the row (T > 0) / tie count (T == 0)
-  float Z;          // normaliser of the kept set
+  float m;         // maximum raw value (logit, or probability)
+  float mz;        // maximum in the weight domain (logit, or lg2(prob)/T)
+  float c;         // weight scale: log2(e)/T for logits, 1 for probabilities
+  float invT;      // 1/T (probabilities)
+  bool greedy;     // T == 0
+  float S;         // sum of weights over the row (T > 0) / tie count (T == 0)
+  float Z;         // normaliser of the kept set
   float invZ;
-  uint32_t kmax;    // vkey(m)
-  uint32_t Dstar;   // kept iff vkey(m) - vkey(v) <= Dstar; kNoFilter = all
+  uint32_t kmax;   // vkey(m)
+  uint32_t Dstar;  // kept iff vkey(m) - vkey(v) <= Dstar; kNoFilter = all
+  float vstar;     // smallest kept raw value (-inf / 0 when nothing is filtered)
 };
 
 // Unnormalised weight of a value: 2^((z - mz) c), or [v == m] for T = 0.
@@ -209,21 +271,45 @@ struct RacePart {
   int idx;
 };
 
+// State of one row's top-p search.
+struct TopLv {
+  uint32_t lo;  // distance offset of the current level's bin 0
+  int shift;    // bin width 2^shift (0: exact keys)
+  float above;  // mass of bins above the current range
+  float R;      // target mass top_p * S
+  int window;   // the current level is the exact bf16 count window
+  int done;
+};
+
+struct RowRes {
+  uint32_t Dstar;
+  float Z, invZ, vstar;
+};
+using TopLvSlot = TopLv;
+
 struct Smem {
-  int bcast[2][4];             // [iteration parity] ticket, kind (rank 0 only)
-  int decide[4];               // resolver decision (rank 0 only)
-  float st_m[2], st_s[2];      // stats partials: target, draft
-  float st_raw;                // raw maximum of the draft row
-  int st_bad[2];
-  uint32_t hist[2][2][256];    // [buffer][row][bin]: counts or float bits
-  RacePart race[2];            // [slot]
+  unsigned long long bar[2][kMaxBlk];  // TMA completion: [target / draft][block]
+  int bcast[2][4];           // [iteration parity] ticket, kind (rank 0 only)
+  float vy[2];               // target / draft value at the proposed token
+  int decide[4];             // resolver decision (rank 0 only)
+  float st_m[2], st_s[2];    // stats partials: target, draft
+  float st_raw;              // raw maximum of the draft row
+  alignas(16) uint32_t hist[2][2][256];  // [buffer][row][bin]; read as uint4 over DSMEM
+  RacePart race[2];          // [slot]
+  uint16_t wbuf[kWarps][256];  // per-warp compaction buffer (window bins / race candidates)
+  float comb[5];             // cluster-combined stats (local broadcast)
+  TopLvSlot lv[2];           // top-p search state (local broadcast)
+  RowRes rres[2];            // top-p results (local broadcast)
+  int comb_bad;              // some CTA's TMA never landed
+  int st_bad;                // this CTA's TMA never landed
+  RacePart win;              // cluster race winner (local broadcast)
   float scratch_f[kWarps][4];
-  int scratch_i[kWarps][4];
   RacePart scratch_r[kWarps];
   int bin_pick;
 };
+static_assert(offsetof(Smem, hist) % 16 == 0, "16-byte DSMEM loads of the histograms");
 
-enum : int { kDone = 0, kNone = 1, kWork = 2 };
+enum : int { kDone = 0, kWork = 2 };
 
 __device__ __forceinline__ bool better(float w1, float E1, int i1, float w2, float E2, int i2) {
   const float a = w1 * E2, b = w2 * E1;
@@ -250,21 +336,14 @@ __device__ __forceinline__ void combine_ms(float& m, float& s, float m2, float s
   }
 }
 
-// Per-row request parameters (uniform across the cluster).
-struct Req {
-  int b, i, kb;
-  bool has_d;
-  float T, top_p;
-  bool params_ok;
-  int y;
-  int pos;
-  uint32_t rid;
-};
+__device__ __forceinline__ void combine_ties(float& m, float& s, float m2, float s2) {
+  if (m2 > m) m = m2, s = s2;
+  else if (m2 == m) s += s2;
+}
 
 __device__ __forceinline__ uint32_t epoch_tag(uint32_t epoch) { return (epoch & 0x0FFFFFFFu) << 4; }
 
-// Row-0 style check used by the ticket dispenser: has any earlier row of b
-// already been decided as not accepted?
+// Has any earlier row of b already been decided as not accepted?
 static __device__ bool earlier_not_accepted(const KParams& P, int b, int i, uint32_t epoch) {
   const uint32_t* rs = P.row_state + (size_t)b * (P.kmax + 1);
   for (int j = 0; j < i; ++j) {
@@ -283,30 +362,277 @@ static __device__ void write_bad_outputs(const KParams& P, int b, uint32_t st) {
   for (int j = 0; j <= P.kmax; ++j) P.out_tokens[(size_t)b * (P.kmax + 1) + j] = -1;
 }
 
-// Histogram level for top-p: every element whose distance D = kmax - key lies
-// in [lo, lo + 256 << shift) adds its count (COUNT) or weight to bin
-// (D - lo) >> shift.
-template <int EB, bool PROBS, bool COUNT, int NG>
-__device__ __forceinline__ void hist_level(const Grp<EB> (&g)[NG], int ng, const RowP& r,
-                                           uint32_t lo, int shift, uint32_t* hist) {
-  const uint32_t span = shift >= 24 ? 0xFFFFFFFFu : ((256u << shift) - 1u);
+// ---------------------------------------------------------------------------
+// TMA bulk copies and mbarriers (1-D, no tensor map, no multicast)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(unsigned long long* bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(unsigned long long* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         unsigned long long* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{.reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p;}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok;
+}
+
+// Bounded wait for a TMA block; returns false (and reports) if it never lands.
+__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, uint32_t parity, int* err) {
+  for (int it = 0; it < (1 << 22); ++it)
+    if (mbar_try_wait(bar, parity)) return true;
+  report(err, SV_ERR_TIMEOUT);
+  return false;
+}
+
+// One 8-element group of this thread from the shared-memory slice starting at
+// element x0 (lanes at or beyond x1 neutralised).
+template <int EB, bool PROBS>
+__device__ __forceinline__ void lds_group(Grp<EB>& g, const char* sbase, int x0, int x, int x1) {
+  const uint4* p = reinterpret_cast<const uint4*>(sbase + (size_t)(x - x0) * EB);
+  const uint4 a = p[0];
+  g.w[0] = a.x, g.w[1] = a.y, g.w[2] = a.z, g.w[3] = a.w;
+  if constexpr (EB == 4) {
+    const uint4 b = p[1];
+    g.w[4] = b.x, g.w[5] = b.y, g.w[6] = b.z, g.w[7] = b.w;
+  }
+  mask_group<EB, PROBS>(g, x, x1);
+}
+
+template <int EB, bool PROBS>
+__device__ __forceinline__ void lds_group_or_neutral(Grp<EB>& g, const char* sbase, int x0, int x,
+                                                     int x1) {
+  if (x < x1) {
+    lds_group<EB, PROBS>(g, sbase, x0, x, x1);
+  } else {
 #pragma unroll
-  for (int gi = 0; gi < NG; ++gi) {
-    if (gi >= ng) break;
+    for (int j = 0; j < EB * 2; ++j) g.w[j] = neutral_word<EB, PROBS>();
+  }
+}
+
+// The thread's groups of a slice: group k starts at element x0 + k*kBlk + tid*8.
+struct SliceIter {
+  int x0, x1, nblk, V;
+  __device__ __forceinline__ int x(int blk) const { return x0 + blk * kBlk + (int)threadIdx.x * kGroup; }
+};
+
+// ---------------------------------------------------------------------------
+// per-group passes
+// ---------------------------------------------------------------------------
+struct Online {
+  float m, raw, s;
+  float2 acc;
+};
+
+__device__ __forceinline__ void online_init(Online& o, bool probs) {
+  o.m = -INFINITY, o.raw = probs ? 0.0f : -INFINITY, o.s = 0.0f, o.acc = make_float2(0.0f, 0.0f);
+}
+
+// Online (max, sum of weights).  Logit rows: weight 2^((v - m) c).
+// Probability rows: z = lg2(v)/T first.  Greedy rows: count elements equal to
+// the running maximum.
+template <int EB, bool PROBS>
+__device__ __forceinline__ void stats_group(const Grp<EB>& g, bool greedy, float c, float invT,
+                                            Online& o) {
+  const float gm = group_max<EB>(g);
+  o.raw = fmaxf(o.raw, gm);
+  if (greedy) {
+    if (gm > o.m) o.m = gm, o.s = 0.0f;
 #pragma unroll
-    for (int e = 0; e < kGroup; ++e) {
-      const float v = gval<EB>(g[gi], e);
-      const uint32_t D = r.kmax - vkey<EB>(v);
-      const uint32_t u = D - lo;
-      if (D >= lo && u <= span && v > (PROBS ? 0.0f : -INFINITY)) {
-        const uint32_t bin = u >> shift;
-        if (COUNT) {
-          atomicAdd(&hist[bin], 1u);
-        } else {
-          atomicAdd(reinterpret_cast<float*>(&hist[bin]), weight<PROBS>(v, r));
-        }
+    for (int e = 0; e < kGroup; ++e) o.s += gval<EB>(g, e) == o.m ? 1.0f : 0.0f;
+  } else if (!PROBS) {
+    if (gm > o.m) {
+      const float sc = o.m == -INFINITY ? 0.0f : ex2((o.m - gm) * c);
+      o.acc.x *= sc, o.acc.y *= sc;
+      o.m = gm;
+    }
+    if (o.m != -INFINITY) {
+      const float2 nm = make_float2(-o.m, -o.m), cc = make_float2(c, c);
+      const float2 d0 = f2mul(f2add(gpair<EB>(g, 0), nm), cc);
+      const float2 d1 = f2mul(f2add(gpair<EB>(g, 1), nm), cc);
+      const float2 d2 = f2mul(f2add(gpair<EB>(g, 2), nm), cc);
+      const float2 d3 = f2mul(f2add(gpair<EB>(g, 3), nm), cc);
+      const float2 e01 = f2add(make_float2(ex2(d0.x), ex2(d0.y)), make_float2(ex2(d1.x), ex2(d1.y)));
+      const float2 e23 = f2add(make_float2(ex2(d2.x), ex2(d2.y)), make_float2(ex2(d3.x), ex2(d3.y)));
+      o.acc = f2add(o.acc, f2add(e01, e23));
+    }
+  } else {
+    const float gz = gm > 0.0f ? lg2(gm) * invT : -INFINITY;
+    if (gz > o.m) {
+      const float sc = o.m == -INFINITY ? 0.0f : ex2(o.m - gz);
+      o.acc.x *= sc, o.acc.y *= sc;
+      o.m = gz;
+    }
+    if (o.m != -INFINITY) {
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const float2 v = gpair<EB>(g, p);
+        o.acc.x += ex2(lg2(v.x) * invT - o.m);
+        o.acc.y += ex2(lg2(v.y) * invT - o.m);
       }
     }
+  }
+}
+
+__device__ __forceinline__ float online_sum(const Online& o, bool greedy) {
+  return greedy ? o.s : o.acc.x + o.acc.y;
+}
+
+// Warp-inclusive scan of a per-lane count.
+__device__ __forceinline__ int warp_incl_scan(int v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
+
+// bf16 order key of the low (h = 0) or high (h = 1) half of a packed word
+__device__ __forceinline__ uint32_t half_key(uint32_t w, int h) {
+  uint32_t b16 = h ? (w >> 16) : (w & 0xFFFFu);
+  if (b16 == 0x8000u) b16 = 0u;  // -0 keys like +0
+  return b16 ^ ((b16 & 0x8000u) ? 0xFFFFu : 0x8000u);
+}
+
+// Exact window histogram for bf16 rows: count elements by bf16 order-key
+// distance D = kmax - key(v) for keys in [lo_key, kmax] (one bin per bf16
+// value, at most 256).  Masks of all of the thread's groups come first, then
+// one warp scan places the in-window bins in the warp's buffer and the atomics
+// run on full warps; a window too dense for the buffer goes group by group.
+__device__ __forceinline__ uint32_t group_mask_bf16(const Grp<2>& g, uint32_t thr2) {
+  uint32_t msk = 0;
+#pragma unroll
+  for (int p = 0; p < 4; ++p) msk |= bge2(g.w[p], thr2) << (2 * p);
+  return msk;
+}
+
+__device__ __forceinline__ void put_bins_bf16(const Grp<2>& g, uint32_t msk, uint32_t kmax,
+                                              uint16_t* wb, int pos) {
+#pragma unroll
+  for (int e = 0; e < kGroup; ++e)  // static element index: the group stays in registers
+    if ((msk >> e) & 1u) wb[pos++] = (uint16_t)(kmax - half_key(g.w[e >> 1], e & 1));
+}
+
+__device__ __forceinline__ void flush_bins(uint32_t* hist, const uint16_t* wb, int total) {
+  __syncwarp();
+  for (int j = threadIdx.x & 31; j < total; j += 32) {
+    const uint32_t bin = wb[j];
+    if (bin < 256u) atomicAdd(&hist[bin], 1u);  // always true for keys in the window
+  }
+  __syncwarp();
+}
+
+__device__ __forceinline__ void window_row_bf16(const char* s, const SliceIter& it, uint32_t kmax,
+                                                uint32_t lo_key, uint32_t* hist, uint16_t* wb) {
+  const uint32_t thr2 = bf16_pair_of(vkey_value<2>(lo_key));
+  uint32_t m_lo = 0, m_hi = 0;  // 8-bit masks of groups 0-3 and 4-7
+  int cnt = 0;
+#pragma unroll
+  for (int blk = 0; blk < kMaxBlk; ++blk) {
+    if (blk < it.nblk) {
+      Grp<2> g;
+      const int x = it.x(blk);
+      lds_group_or_neutral<2, false>(g, s, it.x0, x, it.x1);
+      uint32_t m = group_mask_bf16(g, thr2);
+      if (x + kGroup > it.x1) m &= x < it.x1 ? (1u << (it.x1 - x)) - 1u : 0u;  // past the row end
+      cnt += __popc(m);
+      if (blk < 4) m_lo |= m << (8 * blk);
+      else m_hi |= m << (8 * (blk - 4));
+    }
+  }
+  const int incl = warp_incl_scan(cnt);
+  const int total = __shfl_sync(0xffffffffu, incl, 31);
+  if (total == 0) return;
+  if (total <= 256) {
+    // walk the set bits only (about one per thread): each hit is re-read from
+    // shared memory by index, so no lane replays the other lanes' groups
+    int pos = incl - cnt;
+    const uint16_t* sv = reinterpret_cast<const uint16_t*>(s);
+    const int base = (int)threadIdx.x * kGroup;  // slice offset of this thread's group 0
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      uint32_t m = half ? m_hi : m_lo;
+      while (m) {
+        const int bit = __ffs(m) - 1;
+        m &= m - 1;
+        const int off = base + (half * 4 + (bit >> 3)) * kBlk + (bit & 7);
+        uint32_t b16 = sv[off];
+        if (b16 == 0x8000u) b16 = 0u;  // -0 keys like +0
+        const uint32_t key = b16 ^ ((b16 & 0x8000u) ? 0xFFFFu : 0x8000u);
+        wb[pos++] = (uint16_t)(kmax - key);
+      }
+    }
+    flush_bins(hist, wb, total);
+    return;
+  }
+#pragma unroll 1
+  for (int blk = 0; blk < it.nblk; ++blk) {  // dense window: one group at a time
+    const uint32_t m = ((blk < 4 ? m_lo : m_hi) >> (8 * (blk & 3))) & 0xFFu;
+    const int n = __popc(m);
+    const int inc = warp_incl_scan(n);
+    const int tot = __shfl_sync(0xffffffffu, inc, 31);
+    if (tot == 0) continue;
+    if (m) {
+      Grp<2> g;
+      lds_group<2, false>(g, s, it.x0, it.x(blk), it.x1);
+      put_bins_bf16(g, m, kmax, wb, inc - n);
+    }
+    flush_bins(hist, wb, tot);
+  }
+}
+
+// Lowest key a top-p boundary can have: every element below value v_lo weighs
+// at most w(v_lo) = (1 - top_p) S / (2 V), so they hold at most half the
+// excluded mass and the boundary lies at or above v_lo.  Clamped to the
+// 256-bin window below kmax.
+__device__ __forceinline__ uint32_t window_lo_key(const RowP& r, float top_p, int V) {
+  const uint32_t floor_key = r.kmax >= 255u ? r.kmax - 255u : 0u;
+  const float wlo = (1.0f - top_p) * r.S / (2.0f * (float)V);
+  if (!(wlo > 0.0f)) return floor_key;
+  const float vlo = r.m + lg2(wlo) / r.c - 1.0f / r.c;  // one log2 unit of slack
+  if (!(vlo > -FLT_MAX)) return floor_key;
+  // bf16 value at or below vlo, as a key
+  const uint32_t pair = bf16_pair_of(vlo);
+  const uint32_t k = vkey<2>(__uint_as_float(pair << 16));
+  return k > floor_key ? k : floor_key;
+}
+
+// General histogram level: every element whose distance D lies in
+// [lo, lo + 256 << shift) adds its weight to bin (D - lo) >> shift.
+template <int EB, bool PROBS>
+__device__ __forceinline__ void level_group(const Grp<EB>& g, const RowP& r, uint32_t lo, int shift,
+                                            uint32_t* hist) {
+  const uint32_t span = shift >= 24 ? 0xFFFFFFFFu : ((256u << shift) - 1u);
+#pragma unroll
+  for (int e = 0; e < kGroup; ++e) {
+    const float v = gval<EB>(g, e);
+    const uint32_t D = r.kmax - vkey<EB>(v);
+    const uint32_t u = D - lo;
+    if (D >= lo && u <= span && v > (PROBS ? 0.0f : -INFINITY))
+      atomicAdd(reinterpret_cast<float*>(&hist[u >> shift]), weight<PROBS>(v, r));
   }
 }
 
@@ -326,163 +652,363 @@ __device__ __forceinline__ float block_scan(float v, Smem& sm) {
   return v + off;
 }
 
-// Top-p threshold of one or two rows (target and, if has_d, draft) held in
-// registers across the cluster.  Sets r.Dstar and r.Z.  All control flow
-// depends only on cluster-reduced values, so every CTA takes the same path.
-template <int EBT, int EBD, bool PROBS, int NG>
-__device__ void top_p_rows(cg::cluster_group& cluster, Smem& sm, const Grp<EBT> (&tg)[NG],
-                           const Grp<EBD> (&dg)[NG], int ng, bool has_d, float top_p, RowP& rt,
-                           RowP& rd) {
+
+// One warp resolves one level of one row: gathers the C ranks' 256-bin
+// histograms (lane l owns bins 8l .. 8l+7, all remote loads in flight
+// together), scans them in the warp, and picks the boundary bin.  Every CTA
+// runs the same arithmetic on the same data, so all reach the same result.
+template <int EB, bool PROBS>
+__device__ __forceinline__ void resolve_level(cg::cluster_group& cluster, const uint32_t* hist, int C,
+                                              TopLv& lv, RowP& r) {
+  const int lane = threadIdx.x & 31;
+  float h[8];  // counts (exact in fp32 below 2^24) or weights per bin
+#pragma unroll
+  for (int k = 0; k < 8; ++k) h[k] = 0.0f;
+#pragma unroll
+  for (int q0 = 0; q0 < kMaxCluster; q0 += 2) {
+    if (q0 < C) {
+      uint4 a[2], b[2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        if (q0 + q < C) {
+          const uint4* src = reinterpret_cast<const uint4*>(cluster.map_shared_rank(hist, q0 + q)) + 2 * lane;
+          a[q] = src[0], b[q] = src[1];
+        } else {
+          a[q] = make_uint4(0u, 0u, 0u, 0u), b[q] = a[q];
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {  // rank order
+        const uint32_t w[8] = {a[q].x, a[q].y, a[q].z, a[q].w, b[q].x, b[q].y, b[q].z, b[q].w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) h[k] += lv.window ? (float)w[k] : __uint_as_float(w[k]);
+      }
+    }
+  }
+  if (lv.window) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      h[k] = h[k] > 0.0f ? h[k] * weight<PROBS>(vkey_value<2>(r.kmax - (uint32_t)(8 * lane + k)), r) : 0.0f;
+  }
+  float inc[8], t = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) t += h[k], inc[k] = t;
+  float off = t;  // warp exclusive scan of the lane totals
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float v = __shfl_up_sync(0xffffffffu, off, o);
+    if (lane >= o) off += v;
+  }
+  off -= t;
+  int first = 8;
+#pragma unroll
+  for (int k = 7; k >= 0; --k)
+    if (lv.above + off + inc[k] >= lv.R) first = k;
+  const uint32_t hit = __ballot_sync(0xffffffffu, first < 8);
+  int c;
+  float cexcl, ch;
+  if (hit) {
+    const int src = __ffs(hit) - 1;
+    float my_excl = off, my_h = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (k == first) my_h = h[k], my_excl = off + inc[k] - h[k];
+    c = 8 * src + __shfl_sync(0xffffffffu, first, src);
+    cexcl = __shfl_sync(0xffffffffu, my_excl, src);
+    ch = __shfl_sync(0xffffffffu, my_h, src);
+  } else if (lv.window) {  // boundary beyond the exact window: full radix descent
+    lv.window = 0;
+    lv.lo = 0u;
+    lv.above = 0.0f;
+    lv.shift = EB == 2 ? 8 : 24;
+    return;
+  } else {  // rounding left the target mass unreachable: keep through the last non-empty bin
+    int last = -1;
+    float my_excl = 0.0f, my_h = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (h[k] > 0.0f) last = k, my_h = h[k], my_excl = off + inc[k] - h[k];
+    const uint32_t any = __ballot_sync(0xffffffffu, last >= 0);
+    const int src = any ? 31 - __clz(any) : 0;
+    c = any ? 8 * src + __shfl_sync(0xffffffffu, last, src) : 0;
+    cexcl = __shfl_sync(0xffffffffu, my_excl, src);
+    ch = __shfl_sync(0xffffffffu, my_h, src);
+  }
+  lv.above += cexcl;
+  lv.lo += (uint32_t)c << lv.shift;
+  if (lv.shift == 0) {
+    r.Dstar = lv.lo;
+    r.Z = lv.above + ch;
+    r.invZ = 1.0f / r.Z;
+    r.vstar = vkey_value<EB>(r.kmax - r.Dstar);
+    lv.done = 1;
+  } else {
+    lv.shift -= 8;
+  }
+}
+
+// Top-p threshold of the target row and (if has_d) the draft row held in
+// shared memory across the cluster.  Sets Dstar, Z, invZ, vstar.  All control
+// flow depends only on cluster-reduced values, so every CTA takes the same path.
+template <int EBT, int EBD, bool PROBS>
+__device__ __noinline__ void top_p_rows(cg::cluster_group& cluster, Smem& sm, const char* st,
+                                        const char* sd, const SliceIter& it, bool has_d,
+                                        float top_p, RowP& rt, RowP& rd) {
   const int C = cluster.num_blocks();
   const int tid = threadIdx.x;
-  struct Lv {
-    uint32_t lo;
-    int shift;
-    float above;
-    bool window, done;
-    float R;
-  } L[2];
-  L[0] = {0u, EBT == 2 ? 0 : 24, 0.0f, EBT == 2, false, top_p * rt.S};
-  L[1] = {0u, EBD == 2 ? 0 : 24, 0.0f, EBD == 2, !has_d, top_p * rd.S};
+  TopLv L[2];
+  L[0] = {0u, EBT == 2 ? 0 : 24, 0.0f, top_p * rt.S, EBT == 2, 0};
+  L[1] = {0u, EBD == 2 ? 0 : 24, 0.0f, top_p * rd.S, EBD == 2 && !PROBS, !has_d};
+  // window floors as distances below the row maxima (bf16 rows only)
+  uint32_t lo_t = 255u, lo_d = 255u;
+  if constexpr (EBT == 2) lo_t = rt.kmax - window_lo_key(rt, top_p, it.V);
+  if constexpr (EBD == 2 && !PROBS) lo_d = rd.kmax - window_lo_key(rd, top_p, it.V);
   int buf = 0;
   while (!(L[0].done && L[1].done)) {
-    // 1. local histograms
     for (int j = tid; j < 512; j += kThreads) (&sm.hist[buf][0][0])[j] = 0u;
     __syncthreads();
-    if (!L[0].done) {
-      if (L[0].window && EBT == 2)
-        hist_level<EBT, false, true>(tg, ng, rt, L[0].lo, L[0].shift, sm.hist[buf][0]);
-      else
-        hist_level<EBT, false, false>(tg, ng, rt, L[0].lo, L[0].shift, sm.hist[buf][0]);
+    if constexpr (EBT == 2) {
+      if (!L[0].done && L[0].window)
+        window_row_bf16(st, it, rt.kmax, rt.kmax - lo_t, sm.hist[buf][0], sm.wbuf[tid >> 5]);
     }
-    if (!L[1].done) {
-      if (L[1].window && EBD == 2)
-        hist_level<EBD, PROBS, true>(dg, ng, rd, L[1].lo, L[1].shift, sm.hist[buf][1]);
-      else
-        hist_level<EBD, PROBS, false>(dg, ng, rd, L[1].lo, L[1].shift, sm.hist[buf][1]);
+    if constexpr (EBD == 2 && !PROBS) {
+      if (!L[1].done && L[1].window)
+        window_row_bf16(sd, it, rd.kmax, rd.kmax - lo_d, sm.hist[buf][1], sm.wbuf[tid >> 5]);
+    }
+    const bool gen_t = !L[0].done && !(EBT == 2 && L[0].window);
+    const bool gen_d = !L[1].done && !(EBD == 2 && !PROBS && L[1].window);
+    if (gen_t || gen_d) {
+#pragma unroll 1
+      for (int blk = 0; blk < it.nblk; ++blk) {
+        const int x = it.x(blk);
+        if (x >= it.x1) break;
+        if (gen_t) {
+          Grp<EBT> g;
+          lds_group<EBT, false>(g, st, it.x0, x, it.x1);
+          level_group<EBT, false>(g, rt, L[0].lo, L[0].shift, sm.hist[buf][0]);
+        }
+        if (gen_d) {
+          Grp<EBD> g;
+          lds_group<EBD, PROBS>(g, sd, it.x0, x, it.x1);
+          level_group<EBD, PROBS>(g, rd, L[1].lo, L[1].shift, sm.hist[buf][1]);
+        }
+      }
     }
     __syncthreads();
     cluster.sync();
-    // 2. cluster-reduce bin t in thread t, then scan and pick the boundary bin
-#pragma unroll
-    for (int row = 0; row < 2; ++row) {
-      Lv& lv = L[row];
-      if (lv.done) continue;
-      const RowP& r = row == 0 ? rt : rd;
-      const bool count = row == 0 ? (lv.window && EBT == 2) : (lv.window && EBD == 2);
-      float h = 0.0f;
-      if (count) {
-        uint32_t n = 0;
-        for (int q = 0; q < C; ++q) n += cluster.map_shared_rank(&sm.hist[buf][row][0], q)[tid];
-        if (n) {
-          const float v = row == 0 ? vkey_value<EBT>(r.kmax - lv.lo - (uint32_t)tid)
-                                   : vkey_value<EBD>(r.kmax - lv.lo - (uint32_t)tid);
-          h = (float)n * (row == 0 ? weight<false>(v, r) : weight<PROBS>(v, r));
-        }
-      } else {
-        for (int q = 0; q < C; ++q)
-          h += __uint_as_float(cluster.map_shared_rank(&sm.hist[buf][row][0], q)[tid]);
-      }
-      const float incl = block_scan(h, sm);
-      if (tid == 0) sm.bin_pick = 256;
-      __syncthreads();
-      const float excl = incl - h;
-      if (lv.above + incl >= lv.R && lv.above + excl < lv.R) atomicMin(&sm.bin_pick, tid);
-      __syncthreads();
-      int c = sm.bin_pick;
-      if (c == 256) {
-        if (lv.window) {  // boundary lies beyond the exact window: full radix descent
-          lv.window = false;
-          lv.lo = 0u;
-          lv.above = 0.0f;
-          lv.shift = (row == 0 ? EBT : EBD) == 2 ? 8 : 24;
-          __syncthreads();
-          continue;
-        }
-        // rounding left the target mass unreachable: keep through the last non-empty bin
-        if (tid == 0) sm.bin_pick = -1;
-        __syncthreads();
-        if (h > 0.0f) atomicMax(&sm.bin_pick, tid);
-        __syncthreads();
-        c = sm.bin_pick < 0 ? 0 : sm.bin_pick;
-      }
-      // broadcast the picked bin's exclusive prefix and mass from thread c
-      if (tid == c) {
-        sm.scratch_f[0][2] = excl;
-        sm.scratch_f[0][3] = h;
-      }
-      __syncthreads();
-      const float cexcl = sm.scratch_f[0][2], ch = sm.scratch_f[0][3];
-      __syncthreads();
-      lv.above += cexcl;
-      lv.lo += (uint32_t)c << lv.shift;
-      if (lv.shift == 0) {
-        RowP& w = row == 0 ? rt : rd;
-        w.Dstar = lv.lo;
-        w.Z = lv.above + ch;
-        w.invZ = 1.0f / w.Z;
-        lv.done = true;
-      } else {
-        lv.shift -= 8;
-      }
+    // warp 0 resolves the target row, warp 1 the draft row; one barrier
+    // publishes both results to the whole CTA
+    const int warp = tid >> 5;
+    if (warp == 0 && !L[0].done) {
+      resolve_level<EBT, false>(cluster, &sm.hist[buf][0][0], C, L[0], rt);
+      if ((tid & 31) == 0) sm.lv[0] = L[0], sm.rres[0] = {rt.Dstar, rt.Z, rt.invZ, rt.vstar};
     }
+    if (warp == 1 && !L[1].done) {
+      resolve_level<EBD, PROBS>(cluster, &sm.hist[buf][1][0], C, L[1], rd);
+      if ((tid & 31) == 0) sm.lv[1] = L[1], sm.rres[1] = {rd.Dstar, rd.Z, rd.invZ, rd.vstar};
+    }
+    __syncthreads();
+    if (!L[0].done) {
+      L[0] = sm.lv[0];
+      rt.Dstar = sm.rres[0].Dstar, rt.Z = sm.rres[0].Z, rt.invZ = sm.rres[0].invZ, rt.vstar = sm.rres[0].vstar;
+    }
+    if (!L[1].done) {
+      L[1] = sm.lv[1];
+      rd.Dstar = sm.rres[1].Dstar, rd.Z = sm.rres[1].Z, rd.invZ = sm.rres[1].invZ, rd.vstar = sm.rres[1].vstar;
+    }
+    __syncthreads();  // sm.lv / sm.rres are rewritten by the next level
     buf ^= 1;
   }
 }
 
-// Exponential race over the thread's register-resident slice.
-//   bonus: w_x = kept p weight (unnormalised); residual: w_x = max(0, p_x - q_x).
-template <int EBT, int EBD, bool PROBS, int NG>
-__device__ __forceinline__ void race_slice(const Grp<EBT> (&tg)[NG], const Grp<EBD> (&dg)[NG],
-                                           int ng, int x_base, bool residual, const RowP& rt,
-                                           const RowP& rd, uint32_t pos, uint32_t rid,
-                                           uint32_t k0, uint32_t k1, float& bw, float& bE,
-                                           int& bidx) {
-  // E >= E_min = -ln(1 - 2^-24) = 5.96e-8; a group whose largest w satisfies
-  // w / E_min < best cannot win.
-  constexpr float kEminSafe = 5.9604e-8f;
-#pragma unroll
-  for (int gi = 0; gi < NG; ++gi) {
-    if (gi >= ng) break;
-    const int x = x_base + gi * kThreads * kGroup;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      float w[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int e = h * 4 + j;
-        const float vp = gval<EBT>(tg[gi], e);
-        if (residual) {
-          const float vq = gval<EBD>(dg[gi], e);
-          w[j] = fmaxf(0.0f, prob<EBT, false>(vp, rt) - prob<EBD, PROBS>(vq, rd));
-        } else {
-          w[j] = kept<EBT>(vp, rt) ? weight<false>(vp, rt) : 0.0f;
-        }
-      }
-      const float wm = fmaxf(fmaxf(w[0], w[1]), fmaxf(w[2], w[3]));
-      if (!(wm * bE > bw * kEminSafe)) continue;
-      const int x4 = x + h * 4;
-      const uint4 r = philox4x32_10(make_uint4((uint32_t)x4 >> 2, pos, rid, 0u), k0, k1);
-      const uint32_t rr[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (!(w[j] > 0.0f)) continue;
-        const float U = uniform_from_bits(rr[j]);
-        const float Ef = -lg2(U) * kLn2;
-        const float Elo = Ef * (1.0f - 2e-6f) - 2e-7f;  // lower bound of the exact E
-        if (Elo <= 0.0f || w[j] * bE > bw * Elo) {
-          const float E = -logf(U);
-          if (w[j] * bE > bw * E) bw = w[j], bE = E, bidx = x4 + j;
-        }
+// Smallest target value that can still beat the running best (bw / bE): its
+// weight must reach bw E_min / bE (bonus) or that times Z (residual, w <= p).
+__device__ __forceinline__ float race_threshold(const RowP& rt, bool residual, float bw, float bE) {
+  if (rt.greedy) return rt.m;  // only tied maxima carry weight
+  const float base = rt.vstar;
+  if (!(bw > 0.0f)) return base;
+  float theta = bw * kEminSafe / bE;  // a smaller w cannot win
+  if (residual) theta *= rt.Z;        // p = weight / Z >= w
+  const float v = rt.m + lg2(theta) / rt.c - 1.0f / rt.c;  // one log2 unit of slack
+  return fmaxf(base, v);
+}
+
+// Race weight of slice element j: bonus w = kept target weight (unnormalised),
+// residual w = max(0, p - q).
+template <int EBT, int EBD, bool PROBS>
+__device__ __forceinline__ float race_weight(const char* st, const char* sd, int j, bool residual,
+                                             const RowP& rt, const RowP& rd) {
+  const float vp = EBT == 2 ? __uint_as_float((uint32_t)((const uint16_t*)st)[j] << 16)
+                            : ((const float*)st)[j];
+  if (!residual) return kept<EBT>(vp, rt) ? weight<false>(vp, rt) : 0.0f;
+  const float vq = EBD == 2 ? __uint_as_float((uint32_t)((const uint16_t*)sd)[j] << 16)
+                            : ((const float*)sd)[j];
+  return fmaxf(0.0f, prob<EBT, false>(vp, rt) - prob<EBD, PROBS>(vq, rd));
+}
+
+// Exponential race over this warp's groups of the shared-memory slices.  The
+// warp compacts candidate elements (target value >= the running threshold)
+// into its buffer and processes them one per lane: one Philox draw per
+// candidate, the fast E first and an accurate logf only for contenders.  The
+// threshold rises with the warp's best after every flush.
+template <int EBT, int EBD, bool PROBS>
+__device__ __noinline__ void race_slice(const char* st, const char* sd, const SliceIter& it,
+                                        bool residual, const RowP& rt, const RowP& rd,
+                                        uint32_t pos, uint32_t rid, uint32_t k0, uint32_t k1,
+                                        uint16_t* wb, RacePart& best) {
+  const int lane = threadIdx.x & 31;
+  float bw = best.w, bE = best.E;
+  int bidx = best.idx;
+  float vthr = race_threshold(rt, residual, bw, bE);
+  int fill = 0;
+  auto flush = [&]() {  // process wb[0, fill) one candidate per lane
+    __syncwarp();
+    for (int j = lane; j < fill; j += 32) {
+      const int e = wb[j];
+      const float w = race_weight<EBT, EBD, PROBS>(st, sd, e, residual, rt, rd);
+      if (!(w * bE > bw * kEminSafe)) continue;
+      const int x = it.x0 + e;
+      const uint4 r = philox4x32_10(make_uint4((uint32_t)x >> 2, pos, rid, 0u), k0, k1);
+      const uint32_t sel = (x & 3) == 0 ? r.x : (x & 3) == 1 ? r.y : (x & 3) == 2 ? r.z : r.w;
+      const float U = uniform_from_bits(sel);
+      const float Ef = -lg2(U) * kLn2;
+      const float Elo = Ef * (1.0f - 2e-6f) - 2e-7f;  // lower bound of the exact E
+      if (Elo <= 0.0f || w * bE > bw * Elo) {
+        const float E = -logf(U);
+        if (better(w, E, x, bw, bE, bidx)) bw = w, bE = E, bidx = x;
       }
     }
+    __syncwarp();
+    warp_race(bw, bE, bidx);  // the warp shares its best: a tighter threshold
+    vthr = race_threshold(rt, residual, bw, bE);
+    fill = 0;
+  };
+  // candidate masks of all of this thread's groups, then one warp scan
+  uint32_t m_lo = 0, m_hi = 0;
+  int cnt = 0;
+#pragma unroll
+  for (int blk = 0; blk < kMaxBlk; ++blk) {
+    if (blk < it.nblk) {
+      const int x = it.x(blk);
+      uint32_t msk = 0;
+      if (x < it.x1) {
+        Grp<EBT> tg;
+        lds_group<EBT, false>(tg, st, it.x0, x, it.x1);
+        msk = group_ge<EBT>(tg, vthr, bf16_pair_of(vthr));
+        // candidates are re-read from shared memory by index: drop lanes past the row end
+        if (x + kGroup > it.x1) msk &= (1u << (it.x1 - x)) - 1u;
+      }
+      cnt += __popc(msk);
+      if (blk < 4) m_lo |= msk << (8 * blk);
+      else m_hi |= msk << (8 * (blk - 4));
+    }
+  }
+  const int base = (int)threadIdx.x * kGroup;  // slice offset of this thread's group 0
+  auto emit = [&](uint32_t m, int half, int pos) {
+    while (m) {
+      const int bit = __ffs(m) - 1;
+      m &= m - 1;
+      wb[pos++] = (uint16_t)(base + (half * 4 + (bit >> 3)) * kBlk + (bit & 7));
+    }
+  };
+  const int incl = warp_incl_scan(cnt);
+  const int total = __shfl_sync(0xffffffffu, incl, 31);
+  if (total <= 256) {
+    if (total) {
+      const int pos = incl - cnt;
+      emit(m_lo, 0, pos);
+      emit(m_hi, 1, pos + __popc(m_lo));
+      fill = total;
+      flush();
+    }
+  } else {
+    // dense candidates (no top-p filter yet): one group column at a time, the
+    // threshold rising after each flush
+#pragma unroll 1
+    for (int blk = 0; blk < it.nblk; ++blk) {
+      uint32_t m = ((blk < 4 ? m_lo : m_hi) >> (8 * (blk & 3))) & 0xFFu, keep = 0;
+      while (m) {
+        const int bit = __ffs(m) - 1;
+        m &= m - 1;
+        const int j = base + blk * kBlk + bit;
+        const float vp = EBT == 2 ? __uint_as_float((uint32_t)((const uint16_t*)st)[j] << 16)
+                                  : ((const float*)st)[j];
+        if (vp >= vthr) keep |= 1u << bit;
+      }
+      const int n = __popc(keep);
+      const int inc = warp_incl_scan(n);
+      const int tot = __shfl_sync(0xffffffffu, inc, 31);
+      if (tot == 0) continue;
+      int pos = inc - n;
+      while (keep) {
+        const int bit = __ffs(keep) - 1;
+        keep &= keep - 1;
+        wb[pos++] = (uint16_t)(base + blk * kBlk + bit);
+      }
+      fill = tot;
+      flush();
+    }
+  }
+  best = {bw, bE, bidx};
+}
+
+// Block + cluster argmax of the race partials (slot `slot` of sm.race).  One
+// warp reads the C partials in parallel (lane r <- rank r); `better` is a
+// total order, so the winner does not depend on the reduction order.
+__device__ __forceinline__ RacePart race_reduce(cg::cluster_group& cluster, Smem& sm, RacePart p,
+                                                int slot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float bw = p.w, bE = p.E;
+  int bidx = p.idx;
+  warp_race(bw, bE, bidx);
+  if (lane == 0) sm.scratch_r[warp] = {bw, bE, bidx};
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    RacePart a = sm.scratch_r[0];
+    for (int w = 1; w < kWarps; ++w) {
+      const RacePart o = sm.scratch_r[w];
+      if (better(o.w, o.E, o.idx, a.w, a.E, a.idx)) a = o;
+    }
+    sm.race[slot] = a;
+  }
+  cluster.sync();
+  if (warp == 0) {
+    float w = 0.0f, E = 1.0f;
+    int idx = 0x7FFFFFFF;
+    if (lane < (int)cluster.num_blocks()) {
+      const RacePart o = cluster.map_shared_rank(&sm, lane)->race[slot];
+      w = o.w, E = o.E, idx = o.idx;
+    }
+    warp_race(w, E, idx);
+    if (lane == 0) sm.win = {w, E, idx};
+  }
+  __syncthreads();
+  return sm.win;
+}
+
+// Debug output: normalised probabilities of this thread's groups.
+template <int EB, bool PROBS>
+__device__ __noinline__ void write_probs(float* out, const char* s, const SliceIter& it,
+                                         const RowP& r) {
+#pragma unroll 1
+  for (int blk = 0; blk < it.nblk; ++blk) {
+    const int x = it.x(blk);
+    if (x >= it.x1) break;
+    Grp<EB> g;
+    lds_group<EB, PROBS>(g, s, it.x0, x, it.x1);
+#pragma unroll
+    for (int e = 0; e < kGroup; ++e)
+      if (x + e < it.x1) out[x + e] = prob<EB, PROBS>(gval<EB>(g, e), r);
   }
 }
 
-template <int EBT, int EBD, bool PROBS, int NG>
-__global__ void __launch_bounds__(kThreads, 2) verify_kernel(const KParams P) {
+template <int EBT, int EBD, bool PROBS>
+__global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
   cg::cluster_group cluster = cg::this_cluster();
   __shared__ Smem sm;
+  extern __shared__ __align__(128) char dyn[];
+  char* s_t = dyn;              // target slice
+  char* s_d = dyn + P.d_off;    // draft slice
   const int C = (int)cluster.num_blocks();
   const int rank = (int)cluster.block_rank();
   const int tid = threadIdx.x;
@@ -490,290 +1016,276 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const KParams P) {
   const uint32_t epoch = *(volatile const uint32_t*)(P.hdr + kHdrEpoch);
   const uint32_t tag = epoch_tag(epoch);
   const uint32_t k0 = P.seed_lo, k1 = P.seed_hi;
+  const bool lead = rank == 0 && tid == 0;
+  const int nblk_max = (P.slice + kBlk - 1) / kBlk;
+  uint32_t phase_t = 0u, phase_d = 0u;  // mbarrier parity per block (bit blk)
 
-  // rank 0 hands out tickets in (position, request) order
-  auto grab = [&](int parity) {
-    if (rank == 0 && tid == 0) {
-      int kind = kDone, t = 0;
-      for (;;) {
-        t = (int)atomicAdd(P.hdr + kHdrTicket, 1u);
-        if (t >= P.n_tickets) { kind = kDone; break; }
-        const int i = t / P.B, b = t - i * P.B;
-        const int kb = P.k ? P.k[b] : P.kmax;
-        if (kb < 0 || kb > P.kmax) {
-          if (i == 0) write_bad_outputs(P, b, SV_ST_BAD_INPUT);
-          continue;
-        }
-        if (i > kb) continue;
-        if (!(P.flags & SV_FLAG_NO_SKIP) && earlier_not_accepted(P, b, i, epoch)) {
-          st_release(P.row_state + (size_t)b * (P.kmax + 1) + i, tag | SV_ROW_SKIPPED);
-          if (P.debug) P.debug[(size_t)b * (P.kmax + 1) + i].state = SV_ROW_SKIPPED;
-          continue;
-        }
-        kind = kWork;
-        break;
+  if (tid == 0) {
+    for (int j = 0; j < kMaxBlk; ++j) mbar_init(&sm.bar[0][j]), mbar_init(&sm.bar[1][j]);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  // Rank 0 hands out tickets in (position, request) order.  `t` is a ticket
+  // already taken from the counter; rows that do not exist or whose request
+  // already has a known earlier rejection are consumed here.
+  auto settle = [&](int t, int parity) {
+    int kind = kDone;
+    for (;; t = (int)atomicAdd(P.hdr + kHdrTicket, 1u)) {
+      if (t >= P.n_tickets) break;
+      const int i = t / P.B, b = t - i * P.B;
+      const int kb = P.k ? P.k[b] : P.kmax;
+      if (kb < 0 || kb > P.kmax) {
+        if (i == 0) write_bad_outputs(P, b, SV_ST_BAD_INPUT);
+        continue;
       }
-      sm.bcast[parity][0] = t;
-      sm.bcast[parity][1] = kind;
+      if (i > kb) continue;
+      if (!(P.flags & SV_FLAG_NO_SKIP) && earlier_not_accepted(P, b, i, epoch)) {
+        st_release(P.row_state + (size_t)b * (P.kmax + 1) + i, tag | SV_ROW_SKIPPED);
+        if (P.debug) P.debug[(size_t)b * (P.kmax + 1) + i].state = SV_ROW_SKIPPED;
+        continue;
+      }
+      kind = kWork;
+      break;
     }
+    sm.bcast[parity][0] = t;
+    sm.bcast[parity][1] = kind;
   };
 
-  grab(0);
+  if (lead) settle((int)atomicAdd(P.hdr + kHdrTicket, 1u), 0);
   cluster.sync();
-  for (int it = 0;; ++it) {
-    const int parity = it & 1;
+  for (int iter = 0;; ++iter) {
+    const int parity = iter & 1;
     const int* bc = cluster.map_shared_rank(&sm.bcast[parity][0], 0);
     const int t = bc[0], kind = bc[1];
     if (kind == kDone) break;
+    // take the next ticket now; its checks wait until this row is done
+    int next_t = 0;
+    if (lead) next_t = (int)atomicAdd(P.hdr + kHdrTicket, 1u);
 
     // ---------------------------------------------------------------- row setup
-    Req q;
-    q.i = t / P.B;
-    q.b = t - q.i * P.B;
-    q.kb = P.k ? P.k[q.b] : P.kmax;
-    q.has_d = q.i < q.kb;
-    q.T = P.temperature[q.b];
-    q.top_p = P.top_p ? P.top_p[q.b] : 1.0f;
-    q.params_ok = (q.T >= 0.0f) && (q.T <= FLT_MAX) && (q.top_p > 0.0f) && (q.top_p <= 1.0f);
-    q.y = q.has_d ? P.tokens[(size_t)q.b * P.kmax + q.i] : 0;
-    q.pos = (P.seq_len ? P.seq_len[q.b] : 0) + 1 + q.i;
-    q.rid = P.request_id ? P.request_id[q.b] : (uint32_t)q.b;
-    const bool y_ok = !q.has_d || (q.y >= 0 && q.y < P.V);
-    const size_t row_t = (size_t)q.b * (P.kmax + 1) + q.i;
-    const size_t row_d = (size_t)q.b * P.kmax + q.i;
+    const int i = t / P.B, b = t - i * P.B;
+    const int kb = P.k ? P.k[b] : P.kmax;
+    const bool has_d = i < kb;
+    const float T = P.temperature[b];
+    const float top_p = P.top_p ? P.top_p[b] : 1.0f;
+    const bool params_ok = (T >= 0.0f) && (T <= FLT_MAX) && (top_p > 0.0f) && (top_p <= 1.0f);
+    const int y = has_d ? P.tokens[(size_t)b * P.kmax + i] : 0;
+    const int pos = (P.seq_len ? P.seq_len[b] : 0) + 1 + i;
+    const uint32_t rid = P.request_id ? P.request_id[b] : (uint32_t)b;
+    const bool y_ok = !has_d || (y >= 0 && y < P.V);
+    const size_t row_t = (size_t)b * (P.kmax + 1) + i;
+    const size_t row_d = (size_t)b * P.kmax + i;
     const char* trow = P.target + row_t * P.t_ld * EBT;
-    const char* drow = q.has_d ? P.draft + row_d * P.d_ld * EBD : nullptr;
-    const int x0 = rank * P.slice;
-    const int x1 = min(P.V, x0 + P.slice);
-    const int xt = x0 + tid * kGroup;  // first element of this thread's group 0
+    const char* drow = has_d ? P.draft + row_d * P.d_ld * EBD : nullptr;
+    SliceIter it;
+    it.x0 = rank * P.slice;
+    it.x1 = min(P.V, it.x0 + P.slice);
+    it.nblk = it.x1 > it.x0 ? (it.x1 - it.x0 + kBlk - 1) / kBlk : 0;
+    it.V = P.V;
 
-    // ---------------------------------------------------------------- load slice
-    Grp<EBT> tg[NG];
-    Grp<EBD> dg[NG];
-#pragma unroll
-    for (int gi = 0; gi < NG; ++gi) {
-      const int x = xt + gi * kThreads * kGroup;
-      const int end = gi < P.ng ? x1 : 0;
-      load_group<EBT, false>(tg[gi], trow, x, end);
-      if (q.has_d) load_group<EBD, PROBS>(dg[gi], drow, x, end);
-      else load_group<EBD, PROBS>(dg[gi], drow, x, 0);
+    // ------------------------------------ TMA: this CTA's slice of both rows
+    if (tid == 0) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // prior reads before new writes
+      for (int blk = 0; blk < it.nblk; ++blk) {
+        const int e0 = it.x0 + blk * kBlk, e1 = min(it.x1, e0 + kBlk);
+        const uint32_t bt = (uint32_t)(((e1 - e0) * EBT + 15) & ~15);
+        mbar_expect_tx(&sm.bar[0][blk], bt);
+        bulk_g2s(s_t + (size_t)blk * kBlk * EBT, trow + (size_t)e0 * EBT, bt, &sm.bar[0][blk]);
+        if (has_d) {
+          const uint32_t bd = (uint32_t)(((e1 - e0) * EBD + 15) & ~15);
+          mbar_expect_tx(&sm.bar[1][blk], bd);
+          bulk_g2s(s_d + (size_t)blk * kBlk * EBD, drow + (size_t)e0 * EBD, bd, &sm.bar[1][blk]);
+        }
+      }
+      // the accept-test operands
+      float vt = 0.0f, vd = 0.0f;
+      if (has_d && y_ok) {
+        vt = EBT == 2 ? __uint_as_float((uint32_t)((const uint16_t*)trow)[y] << 16)
+                      : ((const float*)trow)[y];
+        vd = EBD == 2 ? __uint_as_float((uint32_t)((const uint16_t*)drow)[y] << 16)
+                      : ((const float*)drow)[y];
+      }
+      sm.vy[0] = vt, sm.vy[1] = vd;
     }
 
-    const bool greedy = q.T == 0.0f;
+    const bool greedy = T == 0.0f;
     RowP rt, rd;
     rt.greedy = rd.greedy = greedy;
-    rt.c = greedy ? 0.0f : kLog2e / q.T;
-    rt.invT = rd.invT = greedy ? 0.0f : 1.0f / q.T;
+    rt.c = greedy ? 0.0f : kLog2e / T;
+    rt.invT = rd.invT = greedy ? 0.0f : 1.0f / T;
     rd.c = PROBS ? 1.0f : rt.c;
     rt.Dstar = rd.Dstar = kNoFilter;
 
-    // ----------------------------------------------- sweep 1: max + sum (or ties)
-    float mt = -INFINITY, st = 0.0f, md = -INFINITY, sd = 0.0f, rmd = -INFINITY;
-    bool bad = false;
-#pragma unroll
-    for (int gi = 0; gi < NG; ++gi) {
-      if (gi >= P.ng) break;
-      float gmt = -INFINITY, gmd = -INFINITY;
-#pragma unroll
-      for (int e = 0; e < kGroup; ++e) {
-        const float v = gval<EBT>(tg[gi], e);
-        bad |= !(v <= FLT_MAX);
-        gmt = fmaxf(gmt, v);
-        if (q.has_d) {
-          const float vd = gval<EBD>(dg[gi], e);
-          bad |= PROBS ? !(vd >= 0.0f && vd <= FLT_MAX) : !(vd <= FLT_MAX);
-          gmd = fmaxf(gmd, vd);
-        }
-      }
-      rmd = fmaxf(rmd, gmd);
-      if (greedy) {
-        // st / sd count ties at the running maximum
-        if (gmt > mt) mt = gmt, st = 0.0f;
-        if (gmd > md) md = gmd, sd = 0.0f;
-#pragma unroll
-        for (int e = 0; e < kGroup; ++e) {
-          st += gval<EBT>(tg[gi], e) == mt ? 1.0f : 0.0f;
-          if (q.has_d) sd += gval<EBD>(dg[gi], e) == md ? 1.0f : 0.0f;
-        }
-      } else {
-        if (gmt > mt) {
-          st = mt == -INFINITY ? 0.0f : st * ex2((mt - gmt) * rt.c);
-          mt = gmt;
-        }
-        if (mt != -INFINITY) {
-#pragma unroll
-          for (int e = 0; e < kGroup; ++e) st += ex2((gval<EBT>(tg[gi], e) - mt) * rt.c);
-        }
-        if (q.has_d) {
-          // draft weights live in the z domain: lg2(prob)/T, or the logit itself
-          float gz = PROBS ? (gmd > 0.0f ? lg2(gmd) * rd.invT : -INFINITY) : gmd;
-          if (gz > md) {
-            sd = md == -INFINITY ? 0.0f : sd * ex2((md - gz) * rd.c);
-            md = gz;
-          }
-          if (md != -INFINITY) {
-#pragma unroll
-            for (int e = 0; e < kGroup; ++e) {
-              const float vd = gval<EBD>(dg[gi], e);
-              const float z = PROBS ? lg2(vd) * rd.invT : vd;
-              sd += ex2((z - md) * rd.c);
-            }
-          }
+    // -------------------------- sweep as blocks land: max + sum (or ties)
+    Online ot, od;
+    online_init(ot, false);
+    online_init(od, PROBS);
+    bool landed = true;
+#pragma unroll 1
+    for (int blk = 0; blk < it.nblk; ++blk) {
+      landed &= mbar_wait(&sm.bar[0][blk], (phase_t >> blk) & 1u, P.err);
+      if (has_d) landed &= mbar_wait(&sm.bar[1][blk], (phase_d >> blk) & 1u, P.err);
+      const int x = it.x(blk);
+      if (x < it.x1) {
+        Grp<EBT> g;
+        lds_group<EBT, false>(g, s_t, it.x0, x, it.x1);
+        stats_group<EBT, false>(g, greedy, rt.c, rt.invT, ot);
+        if (has_d) {
+          Grp<EBD> h;
+          lds_group<EBD, PROBS>(h, s_d, it.x0, x, it.x1);
+          stats_group<EBD, PROBS>(h, greedy, rd.c, rd.invT, od);
         }
       }
     }
-    // warp + block combine
+    phase_t ^= (1u << it.nblk) - 1u;
+    if (has_d) phase_d ^= (1u << it.nblk) - 1u;
+    float mt = ot.m, st = online_sum(ot, greedy), md = od.m, sd = online_sum(od, greedy);
+    float rmd = od.raw;
     const float cc_t = rt.c, cc_d = rd.c;
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
       const float m2 = __shfl_xor_sync(0xffffffffu, mt, o), s2 = __shfl_xor_sync(0xffffffffu, st, o);
       const float m3 = __shfl_xor_sync(0xffffffffu, md, o), s3 = __shfl_xor_sync(0xffffffffu, sd, o);
+      rmd = fmaxf(rmd, __shfl_xor_sync(0xffffffffu, rmd, o));
       if (greedy) {
-        if (m2 > mt) mt = m2, st = s2; else if (m2 == mt) st += s2;
-        if (m3 > md) md = m3, sd = s3; else if (m3 == md) sd += s3;
+        combine_ties(mt, st, m2, s2);
+        combine_ties(md, sd, m3, s3);
       } else {
         combine_ms(mt, st, m2, s2, cc_t);
         combine_ms(md, sd, m3, s3, cc_d);
       }
     }
-    bad = __any_sync(0xffffffffu, bad);
-#pragma unroll
-    for (int o = 16; o; o >>= 1) rmd = fmaxf(rmd, __shfl_xor_sync(0xffffffffu, rmd, o));
     if (lane == 0) {
       sm.scratch_f[warp][0] = mt, sm.scratch_f[warp][1] = st;
       sm.scratch_f[warp][2] = md, sm.scratch_f[warp][3] = sd;
-      sm.scratch_i[warp][0] = bad;
-      sm.scratch_i[warp][1] = __float_as_int(rmd);
+      sm.scratch_r[warp].w = rmd;
     }
     __syncthreads();
     if (tid == 0) {
-      float a = sm.scratch_f[0][0], s = sm.scratch_f[0][1], c2 = sm.scratch_f[0][2], d2 = sm.scratch_f[0][3];
-      int bd = sm.scratch_i[0][0];
-      float rm = __int_as_float(sm.scratch_i[0][1]);
+      float a = sm.scratch_f[0][0], s = sm.scratch_f[0][1];
+      float c2 = sm.scratch_f[0][2], d2 = sm.scratch_f[0][3], rm = sm.scratch_r[0].w;
       for (int w = 1; w < kWarps; ++w) {
-        rm = fmaxf(rm, __int_as_float(sm.scratch_i[w][1]));
+        rm = fmaxf(rm, sm.scratch_r[w].w);
         if (greedy) {
-          if (sm.scratch_f[w][0] > a) a = sm.scratch_f[w][0], s = sm.scratch_f[w][1];
-          else if (sm.scratch_f[w][0] == a) s += sm.scratch_f[w][1];
-          if (sm.scratch_f[w][2] > c2) c2 = sm.scratch_f[w][2], d2 = sm.scratch_f[w][3];
-          else if (sm.scratch_f[w][2] == c2) d2 += sm.scratch_f[w][3];
+          combine_ties(a, s, sm.scratch_f[w][0], sm.scratch_f[w][1]);
+          combine_ties(c2, d2, sm.scratch_f[w][2], sm.scratch_f[w][3]);
         } else {
           combine_ms(a, s, sm.scratch_f[w][0], sm.scratch_f[w][1], cc_t);
           combine_ms(c2, d2, sm.scratch_f[w][2], sm.scratch_f[w][3], cc_d);
         }
-        bd |= sm.scratch_i[w][0];
       }
       sm.st_m[0] = a, sm.st_s[0] = s, sm.st_m[1] = c2, sm.st_s[1] = d2;
-      sm.st_bad[0] = bd;
       sm.st_raw = rm;
+      sm.st_bad = landed ? 0 : 1;
     }
     cluster.sync();  // partials visible cluster-wide
-    {
-      float a = -INFINITY, s = 0.0f, c2 = -INFINITY, d2 = 0.0f, rm = -INFINITY;
-      int bd = 0;
+    if (warp == 0) {
+      // lane r fetches rank r's partials (all remote loads in flight at once),
+      // lane 0 combines them in rank order so every CTA gets identical values
+      float pm0 = -INFINITY, ps0 = 0.0f, pm1 = -INFINITY, ps1 = 0.0f;
+      float praw = PROBS ? 0.0f : -INFINITY;
+      int pbad = 0;
+      if (lane < C) {
+        const Smem* o = cluster.map_shared_rank(&sm, lane);
+        pm0 = o->st_m[0], ps0 = o->st_s[0], pm1 = o->st_m[1], ps1 = o->st_s[1], praw = o->st_raw;
+        pbad = o->st_bad;
+      }
+      float a = -INFINITY, s2 = 0.0f, c2 = -INFINITY, d2 = 0.0f, rm = PROBS ? 0.0f : -INFINITY;
       for (int r = 0; r < C; ++r) {
-        const Smem* o = cluster.map_shared_rank(&sm, r);
-        const float ma = o->st_m[0], sa = o->st_s[0], mb = o->st_m[1], sb = o->st_s[1];
+        const float ma = __shfl_sync(0xffffffffu, pm0, r), sa = __shfl_sync(0xffffffffu, ps0, r);
+        const float mb = __shfl_sync(0xffffffffu, pm1, r), sb = __shfl_sync(0xffffffffu, ps1, r);
+        rm = fmaxf(rm, __shfl_sync(0xffffffffu, praw, r));
         if (greedy) {
-          if (ma > a) a = ma, s = sa; else if (ma == a) s += sa;
-          if (mb > c2) c2 = mb, d2 = sb; else if (mb == c2) d2 += sb;
+          combine_ties(a, s2, ma, sa);
+          combine_ties(c2, d2, mb, sb);
         } else {
-          combine_ms(a, s, ma, sa, cc_t);
+          combine_ms(a, s2, ma, sa, cc_t);
           combine_ms(c2, d2, mb, sb, cc_d);
         }
-        bd |= o->st_bad[0];
-        rm = fmaxf(rm, o->st_raw);
       }
-      rt.m = a, rt.mz = a, rt.S = s;
-      rd.S = d2;
-      rd.m = rm;    // raw maximum (logit or probability): defines the top-p keys
-      rd.mz = c2;   // maximum in the weight domain (== rm except for probabilities, T > 0)
-      bad = bd != 0;
+      const int anybad = __any_sync(0xffffffffu, pbad);
+      if (lane == 0) {
+        sm.comb[0] = a, sm.comb[1] = s2, sm.comb[2] = c2, sm.comb[3] = d2, sm.comb[4] = rm;
+        sm.comb_bad = anybad;
+      }
     }
+    __syncthreads();
+    rt.m = sm.comb[0], rt.mz = sm.comb[0], rt.S = sm.comb[1];
+    rd.S = sm.comb[3];
+    rd.m = sm.comb[4];   // raw maximum (logit or probability): defines the top-p keys
+    rd.mz = sm.comb[2];  // maximum in the weight domain (== raw max except probabilities, T > 0)
     rt.kmax = vkey<EBT>(rt.m);
     rd.kmax = vkey<EBD>(rd.m);
     rt.Z = rt.S, rd.Z = rd.S;
     rt.invZ = 1.0f / rt.Z, rd.invZ = 1.0f / rd.Z;
+    rt.vstar = -INFINITY;
+    rd.vstar = PROBS ? 0.0f : -INFINITY;
+    const float vty = sm.vy[0], vdy = sm.vy[1];
 
-    bool row_bad = bad || !q.params_ok || !y_ok || rt.m == -INFINITY ||
-                   (q.has_d && (PROBS ? !(rd.m > 0.0f) : rd.m == -INFINITY));
+    // NaN / +inf inputs surface as a non-finite sum or maximum
+    const bool bad_t = !(rt.S >= 1.0f && rt.S <= FLT_MAX) || !(rt.m <= FLT_MAX) ||
+                       rt.m == -INFINITY;
+    const bool bad_d = has_d && (!(rd.S >= 1.0f && rd.S <= FLT_MAX) || !(rd.m <= FLT_MAX) ||
+                                 (PROBS ? !(rd.m > 0.0f) : rd.m == -INFINITY));
+    const bool row_bad = bad_t || bad_d || !params_ok || !y_ok || sm.comb_bad;
 
     // ---------------------------------------------------------------- top-p
-    if (!row_bad && !greedy && q.top_p < 1.0f) {
-      top_p_rows<EBT, EBD, PROBS, NG>(cluster, sm, tg, dg, P.ng, q.has_d, q.top_p, rt, rd);
-    }
+    if (!row_bad && !greedy && top_p < 1.0f)
+      top_p_rows<EBT, EBD, PROBS>(cluster, sm, s_t, s_d, it, has_d, top_p, rt, rd);
 
     // ---------------------------------------------------------- accept test
-    // Every CTA evaluates the test identically from the same global values.
+    // Every CTA evaluates the test identically from the same values.
     int state;
     bool qzero = false;
     float p_y = 0.0f, q_y = 0.0f, u = 0.0f;
     if (row_bad) {
       state = SV_ROW_INVALID;
-    } else if (q.has_d) {
-      const float vt = EBT == 2 ? __uint_as_float((uint32_t)((const uint16_t*)trow)[q.y] << 16)
-                                : ((const float*)trow)[q.y];
-      const float vd = EBD == 2 ? __uint_as_float((uint32_t)((const uint16_t*)drow)[q.y] << 16)
-                                : ((const float*)drow)[q.y];
-      p_y = prob<EBT, false>(vt, rt);
-      q_y = prob<EBD, PROBS>(vd, rd);
-      const uint4 r = philox4x32_10(make_uint4(0u, (uint32_t)q.pos, q.rid, 1u), k0, k1);
+    } else if (has_d) {
+      p_y = prob<EBT, false>(vty, rt);
+      q_y = prob<EBD, PROBS>(vdy, rd);
+      const uint4 r = philox4x32_10(make_uint4(0u, (uint32_t)pos, rid, 1u), k0, k1);
       u = uniform_from_bits(r.x);
       qzero = q_y == 0.0f;
       state = (u * q_y < p_y) ? SV_ROW_ACCEPTED : SV_ROW_REJECTED;
     } else {
       state = SV_ROW_BONUS;
     }
-    uint32_t* my_state = P.row_state + row_t;
-    if (rank == 0 && tid == 0) {
-      st_release(my_state, tag | (qzero ? kQZeroBit : 0u) | (uint32_t)state);
+    if (lead) {
+      st_release(P.row_state + row_t, tag | (qzero ? kQZeroBit : 0u) | (uint32_t)state);
       if (P.debug) {
         sv_row_debug d;
         d.p_y = p_y, d.q_y = q_y, d.u = u;
         d.p_kept = greedy || rt.Dstar == kNoFilter ? 1.0f : rt.Z / rt.S;
-        d.q_kept = !q.has_d || greedy || rd.Dstar == kNoFilter ? 1.0f : rd.Z / rd.S;
+        d.q_kept = !has_d || greedy || rd.Dstar == kNoFilter ? 1.0f : rd.Z / rd.S;
         d.state = state;
         d.p_thr_key = rt.Dstar == kNoFilter ? -1 : (int32_t)(rt.kmax - rt.Dstar);
-        d.q_thr_key = (!q.has_d || rd.Dstar == kNoFilter) ? -1 : (int32_t)(rd.kmax - rd.Dstar);
+        d.q_thr_key = (!has_d || rd.Dstar == kNoFilter) ? -1 : (int32_t)(rd.kmax - rd.Dstar);
         P.debug[row_t] = d;
       }
     }
 
     // -------------------------------------------------- debug: normalised rows
-    if (P.probs_p && !row_bad) {
-      float* out = P.probs_p + row_t * (size_t)P.V;
-#pragma unroll
-      for (int gi = 0; gi < NG; ++gi)
-#pragma unroll
-        for (int e = 0; e < kGroup; ++e) {
-          const int x = xt + gi * kThreads * kGroup + e;
-          if (gi < P.ng && x < x1) out[x] = prob<EBT, false>(gval<EBT>(tg[gi], e), rt);
-        }
-    }
-    if (P.probs_q && q.has_d && !row_bad) {
-      float* out = P.probs_q + row_d * (size_t)P.V;
-#pragma unroll
-      for (int gi = 0; gi < NG; ++gi)
-#pragma unroll
-        for (int e = 0; e < kGroup; ++e) {
-          const int x = xt + gi * kThreads * kGroup + e;
-          if (gi < P.ng && x < x1) out[x] = prob<EBD, PROBS>(gval<EBD>(dg[gi], e), rd);
-        }
-    }
+    if (P.probs_p && !row_bad) write_probs<EBT, false>(P.probs_p + row_t * (size_t)P.V, s_t, it, rt);
+    if (P.probs_q && has_d && !row_bad)
+      write_probs<EBD, PROBS>(P.probs_q + row_d * (size_t)P.V, s_d, it, rd);
 
     // --------------------------------------------- resolve: is this row the one?
     if (state != SV_ROW_ACCEPTED) {
-      if (rank == 0 && tid == 0) {
+      if (lead) {
         int resolver = 1;
         uint32_t st_bits = qzero ? SV_ST_Q_ZERO : 0u;
-        const uint32_t* rs = P.row_state + (size_t)q.b * (P.kmax + 1);
-        for (int j = 0; j < q.i && resolver == 1; ++j) {
+        const uint32_t* rs = P.row_state + (size_t)b * (P.kmax + 1);
+        for (int j = 0; j < i && resolver == 1; ++j) {
           uint32_t w = 0;
           int spins = 0;
           for (;;) {
             w = ld_acquire(rs + j);
             if ((w & ~0xFu) == tag && (w & kStateMask) != 0) break;
-            if (++spins > P.spin_limit) { resolver = 2; break; }
+            if (++spins > P.spin_limit) {
+              resolver = 2;
+              break;
+            }
             __nanosleep(spins < 16 ? 32 : 256);
           }
           if (resolver == 2) break;
@@ -782,11 +1294,11 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const KParams P) {
         }
         if (resolver == 2) {
           report(P.err, SV_ERR_TIMEOUT);
-          write_bad_outputs(P, q.b, SV_ST_TIMEOUT);
+          write_bad_outputs(P, b, SV_ST_TIMEOUT);
           resolver = 0;
         }
         if (resolver == 1 && state == SV_ROW_INVALID) {
-          write_bad_outputs(P, q.b, SV_ST_BAD_INPUT);
+          write_bad_outputs(P, b, SV_ST_BAD_INPUT);
           resolver = 0;
         }
         sm.decide[0] = resolver;
@@ -798,73 +1310,39 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const KParams P) {
       const uint32_t st_bits = (uint32_t)dc[1];
       if (resolver) {
         const bool residual = state == SV_ROW_REJECTED;
-        float bw = 0.0f, bE = 1.0f;
-        int bidx = 0x7FFFFFFF;
-        race_slice<EBT, EBD, PROBS, NG>(tg, dg, P.ng, xt, residual, rt, rd, (uint32_t)q.pos,
-                                        q.rid, k0, k1, bw, bE, bidx);
-        warp_race(bw, bE, bidx);
-        if (lane == 0) sm.scratch_r[warp] = {bw, bE, bidx};
-        __syncthreads();
-        if (tid == 0) {
-          RacePart a = sm.scratch_r[0];
-          for (int w = 1; w < kWarps; ++w) {
-            const RacePart o = sm.scratch_r[w];
-            if (better(o.w, o.E, o.idx, a.w, a.E, a.idx)) a = o;
-          }
-          sm.race[0] = a;
-        }
-        cluster.sync();
-        RacePart win = cluster.map_shared_rank(&sm, 0)->race[0];
-        for (int r = 1; r < C; ++r) {
-          const RacePart o = cluster.map_shared_rank(&sm, r)->race[0];
-          if (better(o.w, o.E, o.idx, win.w, win.E, win.idx)) win = o;
-        }
+        RacePart best = {0.0f, 1.0f, 0x7FFFFFFF};
+        race_slice<EBT, EBD, PROBS>(s_t, s_d, it, residual, rt, rd, (uint32_t)pos, rid, k0, k1,
+                                    sm.wbuf[warp], best);
+        RacePart win = race_reduce(cluster, sm, best, 0);
         uint32_t extra = 0u;
         if (!(win.w > 0.0f)) {
           // residual numerically empty: draw from p with the same exponentials
           extra = SV_ST_RESIDUAL_EMPTY;
-          bw = 0.0f, bE = 1.0f, bidx = 0x7FFFFFFF;
-          race_slice<EBT, EBD, PROBS, NG>(tg, dg, P.ng, xt, false, rt, rd, (uint32_t)q.pos, q.rid,
-                                          k0, k1, bw, bE, bidx);
-          warp_race(bw, bE, bidx);
-          if (lane == 0) sm.scratch_r[warp] = {bw, bE, bidx};
-          __syncthreads();
-          if (tid == 0) {
-            RacePart a = sm.scratch_r[0];
-            for (int w = 1; w < kWarps; ++w) {
-              const RacePart o = sm.scratch_r[w];
-              if (better(o.w, o.E, o.idx, a.w, a.E, a.idx)) a = o;
-            }
-            sm.race[1] = a;
-          }
-          cluster.sync();
-          win = cluster.map_shared_rank(&sm, 0)->race[1];
-          for (int r = 1; r < C; ++r) {
-            const RacePart o = cluster.map_shared_rank(&sm, r)->race[1];
-            if (better(o.w, o.E, o.idx, win.w, win.E, win.idx)) win = o;
-          }
+          best = {0.0f, 1.0f, 0x7FFFFFFF};
+          race_slice<EBT, EBD, PROBS>(s_t, s_d, it, false, rt, rd, (uint32_t)pos, rid, k0, k1,
+                                      sm.wbuf[warp], best);
+          win = race_reduce(cluster, sm, best, 1);
         }
-        if (rank == 0 && tid == 0) {
-          const int a = q.i;
-          int32_t* ot = P.out_tokens + (size_t)q.b * (P.kmax + 1);
-          for (int j = 0; j < a; ++j) ot[j] = P.tokens[(size_t)q.b * P.kmax + j];
-          ot[a] = win.idx;
-          for (int j = a + 1; j <= P.kmax; ++j) ot[j] = -1;
-          P.accepted[q.b] = a;
-          P.num_emitted[q.b] = a + 1;
-          P.status[q.b] = st_bits | extra;
+        if (lead) {
+          int32_t* ot2 = P.out_tokens + (size_t)b * (P.kmax + 1);
+          for (int j = 0; j < i; ++j) ot2[j] = P.tokens[(size_t)b * P.kmax + j];
+          ot2[i] = win.idx;
+          for (int j = i + 1; j <= P.kmax; ++j) ot2[j] = -1;
+          P.accepted[b] = i;
+          P.num_emitted[b] = i + 1;
+          P.status[b] = st_bits | extra;
         }
       }
     }
 
-    // next ticket, then the end-of-row barrier publishes it
-    grab(parity ^ 1);
+    // settle the next ticket, then the end-of-row barrier publishes it
+    if (lead) settle(next_t, parity ^ 1);
     cluster.sync();
   }
 
   // all peers must be done reading rank 0's shared memory before it exits
   cluster.sync();
-  if (rank == 0 && tid == 0) {
+  if (lead) {
     __threadfence();
     const uint32_t nclusters = gridDim.x / (uint32_t)C;
     const uint32_t d = atomicAdd(P.hdr + kHdrDone, 1u);
@@ -875,6 +1353,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const KParams P) {
       atomicAdd(P.hdr + kHdrEpoch, 1u);
     }
   }
+  (void)nblk_max;
 }
 
 using KernelFn = void (*)(KParams);
