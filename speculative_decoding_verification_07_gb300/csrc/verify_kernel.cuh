@@ -296,7 +296,10 @@ struct Smem {
   float st_raw;              // raw maximum of the draft row
   alignas(16) uint32_t hist[2][2][256];  // [buffer][row][bin]; read as uint4 over DSMEM
   RacePart race[2];          // [slot]
-  uint16_t wbuf[kWarps][256];  // per-warp compaction buffer (window bins / race candidates)
+  union {
+    uint16_t idx[kWarps][256];  // race candidates (slice element index)
+    uint8_t bin[kWarps][512];   // window bins
+  } wb;                         // per-warp compaction buffers
   float comb[5];             // cluster-combined stats (local broadcast)
   TopLvSlot lv[2];           // top-p search state (local broadcast)
   RowRes rres[2];            // top-p results (local broadcast)
@@ -388,19 +391,22 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// try_wait with a suspend-time hint: the warp is parked until the phase
+// completes (or ~0.5 ms pass) instead of spinning through issue slots.
 __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{.reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p;}"
+      "{.reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 500000; selp.u32 %0, 1, 0, p;}"
       : "=r"(ok)
       : "r"(smem_addr(bar)), "r"(parity)
       : "memory");
   return ok;
 }
 
-// Bounded wait for a TMA block; returns false (and reports) if it never lands.
+// Bounded wait for a TMA block (at most ~1 s); returns false (and reports) if
+// it never lands.
 __device__ __forceinline__ bool mbar_wait(unsigned long long* bar, uint32_t parity, int* err) {
-  for (int it = 0; it < (1 << 22); ++it)
+  for (int it = 0; it < 2000; ++it)
     if (mbar_try_wait(bar, parity)) return true;
   report(err, SV_ERR_TIMEOUT);
   return false;
@@ -530,23 +536,22 @@ __device__ __forceinline__ uint32_t group_mask_bf16(const Grp<2>& g, uint32_t th
 }
 
 __device__ __forceinline__ void put_bins_bf16(const Grp<2>& g, uint32_t msk, uint32_t kmax,
-                                              uint16_t* wb, int pos) {
+                                              uint8_t* wb, int pos) {
 #pragma unroll
   for (int e = 0; e < kGroup; ++e)  // static element index: the group stays in registers
-    if ((msk >> e) & 1u) wb[pos++] = (uint16_t)(kmax - half_key(g.w[e >> 1], e & 1));
+    if ((msk >> e) & 1u) wb[pos++] = (uint8_t)(kmax - half_key(g.w[e >> 1], e & 1));
 }
 
-__device__ __forceinline__ void flush_bins(uint32_t* hist, const uint16_t* wb, int total) {
+__device__ __forceinline__ void flush_bins(uint32_t* hist, const uint8_t* wb, int total) {
   __syncwarp();
   for (int j = threadIdx.x & 31; j < total; j += 32) {
-    const uint32_t bin = wb[j];
-    if (bin < 256u) atomicAdd(&hist[bin], 1u);  // always true for keys in the window
+    atomicAdd(&hist[wb[j]], 1u);  // a byte: always inside the 256 bins
   }
   __syncwarp();
 }
 
 __device__ __forceinline__ void window_row_bf16(const char* s, const SliceIter& it, uint32_t kmax,
-                                                uint32_t lo_key, uint32_t* hist, uint16_t* wb) {
+                                                uint32_t lo_key, uint32_t* hist, uint8_t* wb) {
   const uint32_t thr2 = bf16_pair_of(vkey_value<2>(lo_key));
   uint32_t m_lo = 0, m_hi = 0;  // 8-bit masks of groups 0-3 and 4-7
   int cnt = 0;
@@ -566,7 +571,7 @@ __device__ __forceinline__ void window_row_bf16(const char* s, const SliceIter& 
   const int incl = warp_incl_scan(cnt);
   const int total = __shfl_sync(0xffffffffu, incl, 31);
   if (total == 0) return;
-  if (total <= 256) {
+  if (total <= 512) {
     // walk the set bits only (about one per thread): each hit is re-read from
     // shared memory by index, so no lane replays the other lanes' groups
     int pos = incl - cnt;
@@ -582,7 +587,7 @@ __device__ __forceinline__ void window_row_bf16(const char* s, const SliceIter& 
         uint32_t b16 = sv[off];
         if (b16 == 0x8000u) b16 = 0u;  // -0 keys like +0
         const uint32_t key = b16 ^ ((b16 & 0x8000u) ? 0xFFFFu : 0x8000u);
-        wb[pos++] = (uint16_t)(kmax - key);
+        wb[pos++] = (uint8_t)(kmax - key);
       }
     }
     flush_bins(hist, wb, total);
@@ -769,11 +774,11 @@ __device__ __noinline__ void top_p_rows(cg::cluster_group& cluster, Smem& sm, co
     __syncthreads();
     if constexpr (EBT == 2) {
       if (!L[0].done && L[0].window)
-        window_row_bf16(st, it, rt.kmax, rt.kmax - lo_t, sm.hist[buf][0], sm.wbuf[tid >> 5]);
+        window_row_bf16(st, it, rt.kmax, rt.kmax - lo_t, sm.hist[buf][0], sm.wb.bin[tid >> 5]);
     }
     if constexpr (EBD == 2 && !PROBS) {
       if (!L[1].done && L[1].window)
-        window_row_bf16(sd, it, rd.kmax, rd.kmax - lo_d, sm.hist[buf][1], sm.wbuf[tid >> 5]);
+        window_row_bf16(sd, it, rd.kmax, rd.kmax - lo_d, sm.hist[buf][1], sm.wb.bin[tid >> 5]);
     }
     const bool gen_t = !L[0].done && !(EBT == 2 && L[0].window);
     const bool gen_d = !L[1].done && !(EBD == 2 && !PROBS && L[1].window);
@@ -922,31 +927,46 @@ __device__ __noinline__ void race_slice(const char* st, const char* sd, const Sl
       flush();
     }
   } else {
-    // dense candidates (no top-p filter yet): one group column at a time, the
-    // threshold rising after each flush
+    // dense candidates (no nucleus to filter by): every lane works through its
+    // own groups with one Philox call per 4 consecutive tokens, and the warp
+    // shares its best after every group column to raise the bound
 #pragma unroll 1
     for (int blk = 0; blk < it.nblk; ++blk) {
-      uint32_t m = ((blk < 4 ? m_lo : m_hi) >> (8 * (blk & 3))) & 0xFFu, keep = 0;
-      while (m) {
-        const int bit = __ffs(m) - 1;
-        m &= m - 1;
-        const int j = base + blk * kBlk + bit;
-        const float vp = EBT == 2 ? __uint_as_float((uint32_t)((const uint16_t*)st)[j] << 16)
-                                  : ((const float*)st)[j];
-        if (vp >= vthr) keep |= 1u << bit;
+      const int x = it.x(blk);
+      if (x < it.x1) {
+        Grp<EBT> tg;
+        Grp<EBD> dg;
+        lds_group<EBT, false>(tg, st, it.x0, x, it.x1);  // lanes past the end are neutral
+        if (residual) lds_group<EBD, PROBS>(dg, sd, it.x0, x, it.x1);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float w[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int e = h * 4 + j;
+            const float vp = gval<EBT>(tg, e);
+            w[j] = residual ? fmaxf(0.0f, prob<EBT, false>(vp, rt) - prob<EBD, PROBS>(gval<EBD>(dg, e), rd))
+                            : (kept<EBT>(vp, rt) ? weight<false>(vp, rt) : 0.0f);
+          }
+          const float wm = fmaxf(fmaxf(w[0], w[1]), fmaxf(w[2], w[3]));
+          if (!(wm * bE > bw * kEminSafe)) continue;
+          const int x4 = x + h * 4;
+          const uint4 r = philox4x32_10(make_uint4((uint32_t)x4 >> 2, pos, rid, 0u), k0, k1);
+          const uint32_t rr[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (!(w[j] > 0.0f)) continue;
+            const float U = uniform_from_bits(rr[j]);
+            const float Ef = -lg2(U) * kLn2;
+            const float Elo = Ef * (1.0f - 2e-6f) - 2e-7f;  // lower bound of the exact E
+            if (Elo <= 0.0f || w[j] * bE > bw * Elo) {
+              const float E = -logf(U);
+              if (better(w[j], E, x4 + j, bw, bE, bidx)) bw = w[j], bE = E, bidx = x4 + j;
+            }
+          }
+        }
       }
-      const int n = __popc(keep);
-      const int inc = warp_incl_scan(n);
-      const int tot = __shfl_sync(0xffffffffu, inc, 31);
-      if (tot == 0) continue;
-      int pos = inc - n;
-      while (keep) {
-        const int bit = __ffs(keep) - 1;
-        keep &= keep - 1;
-        wb[pos++] = (uint16_t)(base + blk * kBlk + bit);
-      }
-      fill = tot;
-      flush();
+      warp_race(bw, bE, bidx);
     }
   }
   best = {bw, bE, bidx};
@@ -1312,7 +1332,7 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
         const bool residual = state == SV_ROW_REJECTED;
         RacePart best = {0.0f, 1.0f, 0x7FFFFFFF};
         race_slice<EBT, EBD, PROBS>(s_t, s_d, it, residual, rt, rd, (uint32_t)pos, rid, k0, k1,
-                                    sm.wbuf[warp], best);
+                                    sm.wb.idx[warp], best);
         RacePart win = race_reduce(cluster, sm, best, 0);
         uint32_t extra = 0u;
         if (!(win.w > 0.0f)) {
@@ -1320,7 +1340,7 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
           extra = SV_ST_RESIDUAL_EMPTY;
           best = {0.0f, 1.0f, 0x7FFFFFFF};
           race_slice<EBT, EBD, PROBS>(s_t, s_d, it, false, rt, rd, (uint32_t)pos, rid, k0, k1,
-                                      sm.wbuf[warp], best);
+                                      sm.wb.idx[warp], best);
           win = race_reduce(cluster, sm, best, 1);
         }
         if (lead) {
