@@ -53,7 +53,8 @@ typedef enum {
   SV_ERR_CUDA = -3,        /* a CUDA runtime call failed */
   SV_ERR_TIMEOUT = -4,     /* a bounded device-side wait gave up (device) */
   SV_ERR_UNSUPPORTED = -5, /* valid but not provided (dtype mix, V too large) */
-  SV_ERR_STATE = -6        /* block tables / refcounts inconsistent (device) */
+  SV_ERR_STATE = -6,       /* block tables / refcounts inconsistent (device) */
+  SV_ERR_TOO_LARGE = -7    /* batch beyond spec_verify_static's fixed scratch */
 } sv_status;
 
 typedef enum { SV_BF16 = 0, SV_FP32 = 1 } sv_dtype;
@@ -182,6 +183,35 @@ sv_status sv_workspace_size(const sv_verify_args* args, size_t* bytes);
  * error word. */
 sv_status spec_verify(sv_handle* handle, const sv_verify_args* args, void* workspace,
                       size_t workspace_bytes, sv_stream_t stream);
+
+/* Most rows (B * (kmax + 1)) one spec_verify_static call accepts. */
+#define SV_STATIC_MAX_ROWS 16384
+
+/* spec_verify for callers that cannot allocate device memory.  The pages
+ * have no counterpart: this is a deployment variant of the same step.
+ * Callers inside a memory pool or allocator hook (which must not re-enter the
+ * allocator), runtimes that hand out all device memory up front and have no
+ * scratch to give, and service loops that forbid allocation after start-up
+ * cannot obtain the workspace spec_verify needs.  This entry point computes
+ * exactly what spec_verify computes, with the same arguments, but takes no
+ * handle and no workspace: its scratch (the ticket counters and one decision
+ * word per row, about 64 KB) is a fixed array in device global memory, one
+ * per device, kept for the life of the process.  It calls no cudaMalloc,
+ * cudaFree or allocating library routine.
+ *  - Limit: B * (kmax + 1) <= SV_STATIC_MAX_ROWS, else SV_ERR_TOO_LARGE and
+ *    nothing is launched.  Other argument errors as spec_verify.
+ *  - Set-up: the first call on a device (the current one) looks up the
+ *    array's address with cudaGetSymbolAddress and reads the SM count; make
+ *    that first call before any stream capture on that device.
+ *  - Sharing: every call on a device uses the same array, which keeps the
+ *    previous call's contents.  Each call clears the counters that must start
+ *    at zero with an 8-byte cudaMemsetAsync on `stream`, then launches the
+ *    kernel.  Calls whose GPU work overlaps (two streams without ordering
+ *    between them) race on the array and give wrong results; issue them on
+ *    one stream or order them with events.
+ *  - Errors: no handle, so no device error word; device-side conditions are
+ *    reported in status[] only. */
+sv_status spec_verify_static(const sv_verify_args* args, sv_stream_t stream);
 
 /* stack = [n-1, ..., 1, 0] (blocks pop as 0, 1, 2, ...), free_top = n,
  * refcount = 0. */

@@ -22,9 +22,11 @@ import torch
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libspecverify.so")
 
 SV_OK, SV_ERR_INVALID, SV_ERR_OOM, SV_ERR_CUDA = 0, -1, -2, -3
-SV_ERR_TIMEOUT, SV_ERR_UNSUPPORTED, SV_ERR_STATE = -4, -5, -6
+SV_ERR_TIMEOUT, SV_ERR_UNSUPPORTED, SV_ERR_STATE, SV_ERR_TOO_LARGE = -4, -5, -6, -7
 STATUS_NAMES = {0: "SV_OK", -1: "SV_ERR_INVALID", -2: "SV_ERR_OOM", -3: "SV_ERR_CUDA",
-                -4: "SV_ERR_TIMEOUT", -5: "SV_ERR_UNSUPPORTED", -6: "SV_ERR_STATE"}
+                -4: "SV_ERR_TIMEOUT", -5: "SV_ERR_UNSUPPORTED", -6: "SV_ERR_STATE",
+                -7: "SV_ERR_TOO_LARGE"}
+SV_STATIC_MAX_ROWS = 16384  # rows B * (kmax + 1) one spec_verify_static call accepts
 SV_BF16, SV_FP32 = 0, 1
 SV_DRAFT_LOGITS, SV_DRAFT_PROBS = 0, 1
 ST_Q_ZERO, ST_BAD_INPUT, ST_RESIDUAL_EMPTY, ST_TIMEOUT = 1, 2, 4, 8
@@ -33,7 +35,7 @@ ROW_NONE, ROW_ACCEPTED, ROW_REJECTED, ROW_SKIPPED, ROW_INVALID, ROW_BONUS = rang
 
 EXPORTS = ("sv_verify_args_size", "sv_create", "sv_destroy", "sv_workspace_size",
            "spec_verify", "bfl_init", "bfl_reserve", "bfl_fork_prefix", "bfl_release",
-           "kv_commit_rollback", "kv_rollback_contig", "sv_get_error")
+           "kv_commit_rollback", "kv_rollback_contig", "sv_get_error", "spec_verify_static")
 
 
 class SvVerifyArgs(ctypes.Structure):
@@ -74,6 +76,7 @@ def load_library(path: str = LIB_PATH):
     lib.sv_destroy.argtypes = [c_void_p]
     lib.sv_workspace_size.argtypes = [POINTER(SvVerifyArgs), POINTER(c_size_t)]
     lib.spec_verify.argtypes = [c_void_p, POINTER(SvVerifyArgs), c_void_p, c_size_t, c_void_p]
+    lib.spec_verify_static.argtypes = [POINTER(SvVerifyArgs), c_void_p]
     lib.bfl_init.argtypes = [c_void_p, POINTER(BflState), c_void_p]
     lib.bfl_reserve.argtypes = [c_void_p, POINTER(BflState), c_int32, c_void_p, c_void_p,
                                 c_void_p, c_int32, c_void_p]
@@ -94,8 +97,9 @@ def load_library(path: str = LIB_PATH):
 
 
 class SvError(RuntimeError):
-    def __init__(self, fn, code):
-        super().__init__(f"{fn} returned {STATUS_NAMES.get(code, code)}")
+    def __init__(self, fn, code, detail=None):
+        msg = f"{fn} returned {STATUS_NAMES.get(code, code)}"
+        super().__init__(msg if detail is None else f"{msg}: {detail}")
         self.code = code
 
 
@@ -176,6 +180,22 @@ def spec_verify(handle, args: SvVerifyArgs, workspace: torch.Tensor, stream=None
     _check("spec_verify", load_library().spec_verify(handle, ctypes.byref(args), _ptr(workspace),
                                                      workspace.numel() * workspace.element_size(),
                                                      _stream(stream)))
+
+
+def spec_verify_static(args: SvVerifyArgs, stream=None) -> None:
+    """spec_verify without a handle or workspace, for callers that cannot
+    allocate device memory (inside an allocator hook, or a runtime that owns
+    all memory up front): its scratch is a fixed per-device array in the
+    library, shared by every call and kept between calls, so calls must not
+    overlap on the GPU.  At most SV_STATIC_MAX_ROWS rows B * (kmax + 1), else
+    SvError(SV_ERR_TOO_LARGE).  The first call on a device does a one-time
+    set-up; make it before any stream capture."""
+    code = load_library().spec_verify_static(ctypes.byref(args), _stream(stream))
+    if code == SV_ERR_TOO_LARGE:
+        raise SvError("spec_verify_static", code,
+                      f"B * (kmax + 1) = {args.B * (args.kmax + 1)} rows exceeds the fixed "
+                      f"scratch of {SV_STATIC_MAX_ROWS} rows")
+    _check("spec_verify_static", code)
 
 
 def _state(pool) -> BflState:

@@ -23,7 +23,8 @@ LIB = os.path.join(PKG, "libspecverify.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 
-SOURCES = ["api.cu", "kv_cache.cu", "verify.cu", "verify_bf16.cu", "verify_f32.cu", "verify_mixed.cu"]
+SOURCES = ["api.cu", "kv_cache.cu", "verify.cu", "verify_bf16.cu", "verify_f32.cu", "verify_mixed.cu",
+           "verify_static.cu"]
 
 
 def nvcc() -> str:
