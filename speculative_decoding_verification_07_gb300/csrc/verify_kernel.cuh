@@ -59,6 +59,7 @@ constexpr uint32_t kNoFilter = 0xFFFFFFFFu;
 constexpr int kMaxCluster = 16;
 constexpr int kMaxK = 64;
 constexpr int kDefaultSpin = 1 << 20;
+constexpr int kWindowGuess = 4096;  // elements assumed below a top-p boundary (see top_p_rows)
 constexpr float kEminSafe = 5.9604e-8f;  // <= -ln(1 - 2^-24), the smallest E
 
 // workspace header words
@@ -279,6 +280,8 @@ struct TopLv {
   float R;      // target mass top_p * S
   int window;   // the current level is the exact bf16 count window
   int done;
+  int guess;    // the window floor is the guessed one (a miss retries with the bound)
+  int radix;    // the boundary came from the radix descent (kept mass recomputed)
 };
 
 struct RowRes {
@@ -287,30 +290,38 @@ struct RowRes {
 };
 using TopLvSlot = TopLv;
 
+// Parameters of one ticket's row, prepared by rank 0's warp 0 and read by
+// every CTA of the cluster through DSMEM.
+struct Ticket {
+  int t, kind, kb, y, pos;
+  uint32_t rid;
+  float T, top_p, vt, vd;  // vt / vd: target / draft value at the proposed token
+};
+
+// One warp's statistics partial: a = (target max, target sum, draft raw
+// maximum, TMA failure flag), d = (draft max in the weight domain, draft sum).
+struct alignas(16) StatPart {
+  float4 a, d;
+};
+
 struct Smem {
   unsigned long long bar[2][kMaxBlk];  // TMA completion: [target / draft][block]
-  int bcast[2][4];           // [iteration parity] ticket, kind (rank 0 only)
-  float vy[2];               // target / draft value at the proposed token
+  Ticket tk[2];              // [iteration parity] the row to work on (rank 0 only)
   int decide[4];             // resolver decision (rank 0 only)
-  float st_m[2], st_s[2];    // stats partials: target, draft
-  float st_raw;              // raw maximum of the draft row
+  StatPart part[kWarps];     // per-warp stats partials, read over DSMEM
   alignas(16) uint32_t hist[2][2][256];  // [buffer][row][bin]; read as uint4 over DSMEM
-  RacePart race[2];          // [slot]
+  RacePart rpart[2][kWarps]; // per-warp race partials [slot], read over DSMEM
   union {
     uint16_t idx[kWarps][256];  // race candidates (slice element index)
     uint8_t bin[kWarps][512];   // window bins
   } wb;                         // per-warp compaction buffers
-  float comb[5];             // cluster-combined stats (local broadcast)
+  float kz[2], kz_all[2];    // kept-mass partials (read over DSMEM) and totals
   TopLvSlot lv[2];           // top-p search state (local broadcast)
   RowRes rres[2];            // top-p results (local broadcast)
-  int comb_bad;              // some CTA's TMA never landed
-  int st_bad;                // this CTA's TMA never landed
-  RacePart win;              // cluster race winner (local broadcast)
   float scratch_f[kWarps][4];
-  RacePart scratch_r[kWarps];
-  int bin_pick;
 };
 static_assert(offsetof(Smem, hist) % 16 == 0, "16-byte DSMEM loads of the histograms");
+static_assert(offsetof(Smem, part) % 16 == 0, "16-byte DSMEM loads of the stats partials");
 
 enum : int { kDone = 0, kWork = 2 };
 
@@ -346,16 +357,21 @@ __device__ __forceinline__ void combine_ties(float& m, float& s, float m2, float
 
 __device__ __forceinline__ uint32_t epoch_tag(uint32_t epoch) { return (epoch & 0x0FFFFFFFu) << 4; }
 
-// Has any earlier row of b already been decided as not accepted?
-static __device__ bool earlier_not_accepted(const KParams& P, int b, int i, uint32_t epoch) {
+// Has an earlier row of request b already been decided as not accepted?
+// The warp's lanes read rows j = lane, lane + 32 in parallel (i <= 64).
+__device__ __forceinline__ bool warp_earlier_rejected(const KParams& P, int b, int i, uint32_t tag) {
   const uint32_t* rs = P.row_state + (size_t)b * (P.kmax + 1);
-  for (int j = 0; j < i; ++j) {
-    const uint32_t w = ld_acquire(rs + j);
-    if ((w & ~0xFu) == epoch_tag(epoch) && (w & kStateMask) != 0 &&
-        (w & kStateMask) != SV_ROW_ACCEPTED)
-      return true;
+  const int lane = threadIdx.x & 31;
+  bool hit = false;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int j = lane + 32 * h;
+    if (j < i) {
+      const uint32_t w = ld_relaxed(rs + j);
+      hit |= (w & ~0xFu) == tag && (w & kStateMask) != 0 && (w & kStateMask) != SV_ROW_ACCEPTED;
+    }
   }
-  return false;
+  return __any_sync(0xffffffffu, hit);
 }
 
 static __device__ void write_bad_outputs(const KParams& P, int b, uint32_t st) {
@@ -446,63 +462,96 @@ struct SliceIter {
 // ---------------------------------------------------------------------------
 // per-group passes
 // ---------------------------------------------------------------------------
-struct Online {
-  float m, raw, s;
-  float2 acc;
-};
-
-__device__ __forceinline__ void online_init(Online& o, bool probs) {
-  o.m = -INFINITY, o.raw = probs ? 0.0f : -INFINITY, o.s = 0.0f, o.acc = make_float2(0.0f, 0.0f);
-}
-
-// Online (max, sum of weights).  Logit rows: weight 2^((v - m) c).
-// Probability rows: z = lg2(v)/T first.  Greedy rows: count elements equal to
-// the running maximum.
-template <int EB, bool PROBS>
-__device__ __forceinline__ void stats_group(const Grp<EB>& g, bool greedy, float c, float invT,
-                                            Online& o) {
-  const float gm = group_max<EB>(g);
-  o.raw = fmaxf(o.raw, gm);
-  if (greedy) {
-    if (gm > o.m) o.m = gm, o.s = 0.0f;
-#pragma unroll
-    for (int e = 0; e < kGroup; ++e) o.s += gval<EB>(g, e) == o.m ? 1.0f : 0.0f;
-  } else if (!PROBS) {
-    if (gm > o.m) {
-      const float sc = o.m == -INFINITY ? 0.0f : ex2((o.m - gm) * c);
-      o.acc.x *= sc, o.acc.y *= sc;
-      o.m = gm;
-    }
-    if (o.m != -INFINITY) {
-      const float2 nm = make_float2(-o.m, -o.m), cc = make_float2(c, c);
-      const float2 d0 = f2mul(f2add(gpair<EB>(g, 0), nm), cc);
-      const float2 d1 = f2mul(f2add(gpair<EB>(g, 1), nm), cc);
-      const float2 d2 = f2mul(f2add(gpair<EB>(g, 2), nm), cc);
-      const float2 d3 = f2mul(f2add(gpair<EB>(g, 3), nm), cc);
-      const float2 e01 = f2add(make_float2(ex2(d0.x), ex2(d0.y)), make_float2(ex2(d1.x), ex2(d1.y)));
-      const float2 e23 = f2add(make_float2(ex2(d2.x), ex2(d2.y)), make_float2(ex2(d3.x), ex2(d3.y)));
-      o.acc = f2add(o.acc, f2add(e01, e23));
-    }
+// Row statistics in two sweeps over the thread's groups: the raw maximum as
+// the TMA blocks land, then the weight sum relative to the thread's own
+// maximum.  Logit rows: weight 2^((v - mz) c) with mz = max v.  Probability
+// rows: z = lg2(v)/T, weight 2^(z - mz).  T = 0: the count of elements equal
+// to the maximum.  Partials meet in warp_ms / cluster_ms, which rescale
+// each sum to the common maximum.
+template <int EB>
+__device__ __forceinline__ void max_group(const Grp<EB>& g, uint32_t& mx2, float& mx) {
+  if constexpr (EB == 2) {
+    mx2 = bmax2(mx2, bmax2(bmax2(g.w[0], g.w[1]), bmax2(g.w[2], g.w[3])));
   } else {
-    const float gz = gm > 0.0f ? lg2(gm) * invT : -INFINITY;
-    if (gz > o.m) {
-      const float sc = o.m == -INFINITY ? 0.0f : ex2(o.m - gz);
-      o.acc.x *= sc, o.acc.y *= sc;
-      o.m = gz;
-    }
-    if (o.m != -INFINITY) {
-#pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const float2 v = gpair<EB>(g, p);
-        o.acc.x += ex2(lg2(v.x) * invT - o.m);
-        o.acc.y += ex2(lg2(v.y) * invT - o.m);
-      }
-    }
+    const float a = fmaxf(fmaxf(__uint_as_float(g.w[0]), __uint_as_float(g.w[1])),
+                          fmaxf(__uint_as_float(g.w[2]), __uint_as_float(g.w[3])));
+    const float b = fmaxf(fmaxf(__uint_as_float(g.w[4]), __uint_as_float(g.w[5])),
+                          fmaxf(__uint_as_float(g.w[6]), __uint_as_float(g.w[7])));
+    mx = fmaxf(mx, fmaxf(a, b));
   }
 }
 
-__device__ __forceinline__ float online_sum(const Online& o, bool greedy) {
-  return greedy ? o.s : o.acc.x + o.acc.y;
+template <int EB>
+__device__ __forceinline__ float max_value(uint32_t mx2, float mx) {
+  if constexpr (EB == 2) return fmaxf(__uint_as_float(mx2 << 16), __uint_as_float(mx2 & 0xFFFF0000u));
+  else return mx;
+}
+
+// Sum of one group's weights.  A value no weight formula reads (NaN; for
+// probability rows also a negative value) turns the sum into NaN, which the
+// row's validity check catches.
+template <int EB, bool PROBS>
+__device__ __forceinline__ float sum_group(const Grp<EB>& g, bool greedy, float mz, float c,
+                                           float invT) {
+  const float kNaN = __int_as_float(0x7FC00000);
+  if (greedy) {
+    float n = 0.0f;
+    bool bad = false;
+#pragma unroll
+    for (int e = 0; e < kGroup; ++e) {
+      const float v = gval<EB>(g, e);
+      n += v == mz ? 1.0f : 0.0f;
+      bad |= !(v >= (PROBS ? 0.0f : -INFINITY));
+    }
+    return bad ? kNaN : n;
+  }
+  if (mz == -INFINITY) {  // the thread holds no weight: only neutral values are valid
+    bool bad = false;
+#pragma unroll
+    for (int e = 0; e < kGroup; ++e) {
+      const float v = gval<EB>(g, e);
+      bad |= PROBS ? !(v == 0.0f) : !(v == -INFINITY);
+    }
+    return bad ? kNaN : 0.0f;
+  }
+  float2 a = make_float2(0.0f, 0.0f), b = a;
+  if constexpr (!PROBS) {
+    const float2 nm = make_float2(-mz, -mz), cc = make_float2(c, c);
+    const float2 d0 = f2mul(f2add(gpair<EB>(g, 0), nm), cc);
+    const float2 d1 = f2mul(f2add(gpair<EB>(g, 1), nm), cc);
+    const float2 d2 = f2mul(f2add(gpair<EB>(g, 2), nm), cc);
+    const float2 d3 = f2mul(f2add(gpair<EB>(g, 3), nm), cc);
+    a = f2add(make_float2(ex2(d0.x), ex2(d0.y)), make_float2(ex2(d1.x), ex2(d1.y)));
+    b = f2add(make_float2(ex2(d2.x), ex2(d2.y)), make_float2(ex2(d3.x), ex2(d3.y)));
+  } else {
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const float2 v = gpair<EB>(g, p);
+      const float2 e = make_float2(ex2(lg2(v.x) * invT - mz), ex2(lg2(v.y) * invT - mz));
+      if (p < 2) a = f2add(a, e);
+      else b = f2add(b, e);
+    }
+  }
+  const float2 t = f2add(a, b);
+  return t.x + t.y;
+}
+
+// Scale a (max, sum) partial to the common maximum M.  A partial without
+// elements (sum 0) stays 0 whatever its maximum.
+__device__ __forceinline__ float rescale(float m, float s, float M, float c, bool greedy) {
+  if (greedy) return (m == M || s != s) ? s : 0.0f;  // a NaN partial must survive
+  return s == 0.0f ? 0.0f : s * ex2((m - M) * c);
+}
+
+// All lanes end with the same (M, S): butterfly max, then butterfly sum.
+__device__ __forceinline__ void warp_ms(float& m, float& s, float c, bool greedy) {
+  float M = m;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float S = rescale(m, s, M, c, greedy);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+  m = M, s = S;
 }
 
 // Warp-inclusive scan of a per-lane count.
@@ -516,32 +565,6 @@ __device__ __forceinline__ int warp_incl_scan(int v) {
   return v;
 }
 
-// bf16 order key of the low (h = 0) or high (h = 1) half of a packed word
-__device__ __forceinline__ uint32_t half_key(uint32_t w, int h) {
-  uint32_t b16 = h ? (w >> 16) : (w & 0xFFFFu);
-  if (b16 == 0x8000u) b16 = 0u;  // -0 keys like +0
-  return b16 ^ ((b16 & 0x8000u) ? 0xFFFFu : 0x8000u);
-}
-
-// Exact window histogram for bf16 rows: count elements by bf16 order-key
-// distance D = kmax - key(v) for keys in [lo_key, kmax] (one bin per bf16
-// value, at most 256).  Masks of all of the thread's groups come first, then
-// one warp scan places the in-window bins in the warp's buffer and the atomics
-// run on full warps; a window too dense for the buffer goes group by group.
-__device__ __forceinline__ uint32_t group_mask_bf16(const Grp<2>& g, uint32_t thr2) {
-  uint32_t msk = 0;
-#pragma unroll
-  for (int p = 0; p < 4; ++p) msk |= bge2(g.w[p], thr2) << (2 * p);
-  return msk;
-}
-
-__device__ __forceinline__ void put_bins_bf16(const Grp<2>& g, uint32_t msk, uint32_t kmax,
-                                              uint8_t* wb, int pos) {
-#pragma unroll
-  for (int e = 0; e < kGroup; ++e)  // static element index: the group stays in registers
-    if ((msk >> e) & 1u) wb[pos++] = (uint8_t)(kmax - half_key(g.w[e >> 1], e & 1));
-}
-
 __device__ __forceinline__ void flush_bins(uint32_t* hist, const uint8_t* wb, int total) {
   __syncwarp();
   for (int j = threadIdx.x & 31; j < total; j += 32) {
@@ -550,72 +573,87 @@ __device__ __forceinline__ void flush_bins(uint32_t* hist, const uint8_t* wb, in
   __syncwarp();
 }
 
+// One 16-byte group of a bf16 slice; a group starting at or past the slice end
+// reads the slice's first group instead (callers mask it out).
+__device__ __forceinline__ uint4 load_group_bf16(const char* s, const SliceIter& it, int blk) {
+  const int x = it.x(blk);
+  return *reinterpret_cast<const uint4*>(s + (size_t)(x < it.x1 ? x - it.x0 : 0) * 2);
+}
+
+__device__ __forceinline__ uint32_t bf16_order_key(uint32_t b16) {
+  if (b16 == 0x8000u) b16 = 0u;  // -0 keys like +0
+  return b16 ^ ((b16 & 0x8000u) ? 0xFFFFu : 0x8000u);
+}
+
+// Exact window histogram for bf16 rows: count elements by bf16 order-key
+// distance D = kmax - key(v) for keys in [lo_key, kmax] (one bin per bf16
+// value, at most 256).  The thread's 8 groups are loaded together and turned
+// into 64 candidate bits; one warp scan places the candidates in the warp's
+// buffer and the atomics run on full warps.  The candidate walk is a single
+// loop that re-reads each hit from shared memory: unrolled copies of it made
+// the code large enough that instruction fetch dominated.  A window too dense
+// for the buffer goes one group column at a time.
 __device__ __forceinline__ void window_row_bf16(const char* s, const SliceIter& it, uint32_t kmax,
                                                 uint32_t lo_key, uint32_t* hist, uint8_t* wb) {
   const uint32_t thr2 = bf16_pair_of(vkey_value<2>(lo_key));
-  uint32_t m_lo = 0, m_hi = 0;  // 8-bit masks of groups 0-3 and 4-7
+  uint4 g[kMaxBlk];  // all loads first: their latencies overlap
+#pragma unroll
+  for (int blk = 0; blk < kMaxBlk; ++blk) g[blk] = load_group_bf16(s, it, blk);
+  uint32_t mlo = 0u, mhi = 0u;
   int cnt = 0;
 #pragma unroll
   for (int blk = 0; blk < kMaxBlk; ++blk) {
-    if (blk < it.nblk) {
-      Grp<2> g;
-      const int x = it.x(blk);
-      lds_group_or_neutral<2, false>(g, s, it.x0, x, it.x1);
-      uint32_t m = group_mask_bf16(g, thr2);
-      if (x + kGroup > it.x1) m &= x < it.x1 ? (1u << (it.x1 - x)) - 1u : 0u;  // past the row end
-      cnt += __popc(m);
-      if (blk < 4) m_lo |= m << (8 * blk);
-      else m_hi |= m << (8 * (blk - 4));
-    }
+    const int x = it.x(blk);
+    uint32_t m = bge2(g[blk].x, thr2) | (bge2(g[blk].y, thr2) << 2) | (bge2(g[blk].z, thr2) << 4) |
+                 (bge2(g[blk].w, thr2) << 6);
+    if (x + kGroup > it.x1) m = x < it.x1 ? m & ((1u << (it.x1 - x)) - 1u) : 0u;  // past the end
+    cnt += __popc(m);
+    if (blk < 4) mlo |= m << (8 * blk);
+    else mhi |= m << (8 * (blk - 4));
   }
   const int incl = warp_incl_scan(cnt);
   const int total = __shfl_sync(0xffffffffu, incl, 31);
   if (total == 0) return;
+  const uint16_t* sv = reinterpret_cast<const uint16_t*>(s);
+  const int base = (int)threadIdx.x * kGroup;  // slice offset of this thread's group 0
+  unsigned long long mk = ((unsigned long long)mhi << 32) | mlo;
   if (total <= 512) {
-    // walk the set bits only (about one per thread): each hit is re-read from
-    // shared memory by index, so no lane replays the other lanes' groups
     int pos = incl - cnt;
-    const uint16_t* sv = reinterpret_cast<const uint16_t*>(s);
-    const int base = (int)threadIdx.x * kGroup;  // slice offset of this thread's group 0
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      uint32_t m = half ? m_hi : m_lo;
-      while (m) {
-        const int bit = __ffs(m) - 1;
-        m &= m - 1;
-        const int off = base + (half * 4 + (bit >> 3)) * kBlk + (bit & 7);
-        uint32_t b16 = sv[off];
-        if (b16 == 0x8000u) b16 = 0u;  // -0 keys like +0
-        const uint32_t key = b16 ^ ((b16 & 0x8000u) ? 0xFFFFu : 0x8000u);
-        wb[pos++] = (uint8_t)(kmax - key);
-      }
+    while (mk) {
+      const int bit = __ffsll((long long)mk) - 1;
+      mk &= mk - 1ull;
+      const uint32_t key = bf16_order_key(sv[base + (bit >> 3) * kBlk + (bit & 7)]);
+      wb[pos++] = (uint8_t)(kmax - key);
     }
     flush_bins(hist, wb, total);
     return;
   }
 #pragma unroll 1
-  for (int blk = 0; blk < it.nblk; ++blk) {  // dense window: one group at a time
-    const uint32_t m = ((blk < 4 ? m_lo : m_hi) >> (8 * (blk & 3))) & 0xFFu;
+  for (int blk = 0; blk < it.nblk; ++blk) {  // dense window: one group column at a time
+    uint32_t m = (uint32_t)(mk >> (8 * blk)) & 0xFFu;
     const int n = __popc(m);
     const int inc = warp_incl_scan(n);
     const int tot = __shfl_sync(0xffffffffu, inc, 31);
     if (tot == 0) continue;
-    if (m) {
-      Grp<2> g;
-      lds_group<2, false>(g, s, it.x0, it.x(blk), it.x1);
-      put_bins_bf16(g, m, kmax, wb, inc - n);
+    int pos = inc - n;
+    while (m) {
+      const int e = __ffs(m) - 1;
+      m &= m - 1;
+      const uint32_t key = bf16_order_key(sv[base + blk * kBlk + e]);
+      wb[pos++] = (uint8_t)(kmax - key);
     }
     flush_bins(hist, wb, tot);
   }
 }
 
-// Lowest key a top-p boundary can have: every element below value v_lo weighs
-// at most w(v_lo) = (1 - top_p) S / (2 V), so they hold at most half the
-// excluded mass and the boundary lies at or above v_lo.  Clamped to the
-// 256-bin window below kmax.
-__device__ __forceinline__ uint32_t window_lo_key(const RowP& r, float top_p, int V) {
+// Lowest key a top-p boundary can have when at most n elements lie below it:
+// every element below value v_lo weighs at most w(v_lo) = (1 - top_p) S / (2 n),
+// so together they hold at most half the excluded mass and the boundary lies
+// at or above v_lo.  With n = V this is a bound; clamped to the 256-bin window
+// below kmax.
+__device__ __forceinline__ uint32_t window_lo_key(const RowP& r, float top_p, int n) {
   const uint32_t floor_key = r.kmax >= 255u ? r.kmax - 255u : 0u;
-  const float wlo = (1.0f - top_p) * r.S / (2.0f * (float)V);
+  const float wlo = (1.0f - top_p) * r.S / (2.0f * (float)n);
   if (!(wlo > 0.0f)) return floor_key;
   const float vlo = r.m + lg2(wlo) / r.c - 1.0f / r.c;  // one log2 unit of slack
   if (!(vlo > -FLT_MAX)) return floor_key;
@@ -640,23 +678,6 @@ __device__ __forceinline__ void level_group(const Grp<EB>& g, const RowP& r, uin
       atomicAdd(reinterpret_cast<float*>(&hist[u >> shift]), weight<PROBS>(v, r));
   }
 }
-
-// Inclusive block scan of one float per thread (thread t holds bin t).
-__device__ __forceinline__ float block_scan(float v, Smem& sm) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float n = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += n;
-  }
-  if (lane == 31) sm.scratch_f[warp][0] = v;
-  __syncthreads();
-  float off = 0.0f;
-  for (int w = 0; w < warp; ++w) off += sm.scratch_f[w][0];
-  __syncthreads();
-  return v + off;
-}
-
 
 // One warp resolves one level of one row: gathers the C ranks' 256-bin
 // histograms (lane l owns bins 8l .. 8l+7, all remote loads in flight
@@ -721,8 +742,12 @@ __device__ __forceinline__ void resolve_level(cg::cluster_group& cluster, const 
     c = 8 * src + __shfl_sync(0xffffffffu, first, src);
     cexcl = __shfl_sync(0xffffffffu, my_excl, src);
     ch = __shfl_sync(0xffffffffu, my_h, src);
+  } else if (lv.window && lv.guess) {  // boundary below the guessed floor: retry with the bound
+    lv.guess = 0;
+    return;
   } else if (lv.window) {  // boundary beyond the exact window: full radix descent
     lv.window = 0;
+    lv.radix = 1;
     lv.lo = 0u;
     lv.above = 0.0f;
     lv.shift = EB == 2 ? 8 : 24;
@@ -762,14 +787,22 @@ __device__ __noinline__ void top_p_rows(cg::cluster_group& cluster, Smem& sm, co
   const int C = cluster.num_blocks();
   const int tid = threadIdx.x;
   TopLv L[2];
-  L[0] = {0u, EBT == 2 ? 0 : 24, 0.0f, top_p * rt.S, EBT == 2, 0};
-  L[1] = {0u, EBD == 2 ? 0 : 24, 0.0f, top_p * rd.S, EBD == 2 && !PROBS, !has_d};
+  L[0] = {0u, EBT == 2 ? 0 : 24, 0.0f, top_p * rt.S, EBT == 2, 0, EBT == 2, EBT != 2};
+  L[1] = {0u, EBD == 2 ? 0 : 24, 0.0f, top_p * rd.S, EBD == 2 && !PROBS, !has_d,
+          EBD == 2 && !PROBS, !(EBD == 2 && !PROBS)};
   // window floors as distances below the row maxima (bf16 rows only)
   uint32_t lo_t = 255u, lo_d = 255u;
-  if constexpr (EBT == 2) lo_t = rt.kmax - window_lo_key(rt, top_p, it.V);
-  if constexpr (EBD == 2 && !PROBS) lo_d = rd.kmax - window_lo_key(rd, top_p, it.V);
+  // The first floor assumes at most kWindowGuess elements below the boundary
+  // instead of V: usually true, and far fewer elements land in the window.
+  // When the boundary is not inside that window, resolve_level retries with
+  // the bound (n = V) and then falls back to the exact radix descent, so the
+  // result never depends on the guess.
+  const int nguess = min(it.V, kWindowGuess);
   int buf = 0;
   while (!(L[0].done && L[1].done)) {
+    if constexpr (EBT == 2) lo_t = rt.kmax - window_lo_key(rt, top_p, L[0].guess ? nguess : it.V);
+    if constexpr (EBD == 2 && !PROBS)
+      lo_d = rd.kmax - window_lo_key(rd, top_p, L[1].guess ? nguess : it.V);
     for (int j = tid; j < 512; j += kThreads) (&sm.hist[buf][0][0])[j] = 0u;
     __syncthreads();
     if constexpr (EBT == 2) {
@@ -823,6 +856,63 @@ __device__ __noinline__ void top_p_rows(cg::cluster_group& cluster, Smem& sm, co
     }
     __syncthreads();  // sm.lv / sm.rres are rewritten by the next level
     buf ^= 1;
+  }
+  // A boundary from the radix descent comes with a kept mass summed by float
+  // atomics, whose rounding grows with the number of elements sharing a bin
+  // (a plateau of tied values).  Recompute it as per-thread sums reduced in a
+  // fixed order across the cluster, as the row sum S is.
+  const bool fix_t = L[0].radix, fix_d = has_d && L[1].radix;
+  if (fix_t || fix_d) {
+    float zt = 0.0f, zd = 0.0f;
+#pragma unroll 1
+    for (int blk = 0; blk < it.nblk; ++blk) {
+      const int x = it.x(blk);
+      if (x >= it.x1) break;
+      if (fix_t) {
+        Grp<EBT> g;
+        lds_group<EBT, false>(g, st, it.x0, x, it.x1);
+#pragma unroll
+        for (int e = 0; e < kGroup; ++e) {
+          const float v = gval<EBT>(g, e);
+          if (kept<EBT>(v, rt)) zt += weight<false>(v, rt);
+        }
+      }
+      if (fix_d) {
+        Grp<EBD> g;
+        lds_group<EBD, PROBS>(g, sd, it.x0, x, it.x1);
+#pragma unroll
+        for (int e = 0; e < kGroup; ++e) {
+          const float v = gval<EBD>(g, e);
+          if (kept<EBD>(v, rd)) zd += weight<PROBS>(v, rd);
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      zt += __shfl_xor_sync(0xffffffffu, zt, o);
+      zd += __shfl_xor_sync(0xffffffffu, zd, o);
+    }
+    const int warp = tid >> 5;
+    if ((tid & 31) == 0) sm.scratch_f[warp][0] = zt, sm.scratch_f[warp][1] = zd;
+    __syncthreads();
+    if (tid == 0) {
+      float a = 0.0f, b = 0.0f;
+      for (int w = 0; w < kWarps; ++w) a += sm.scratch_f[w][0], b += sm.scratch_f[w][1];
+      sm.kz[0] = a, sm.kz[1] = b;
+    }
+    cluster.sync();
+    if (tid == 0) {
+      float a = 0.0f, b = 0.0f;
+      for (int r = 0; r < C; ++r) {  // rank order: the same sum in every CTA
+        const Smem* o = cluster.map_shared_rank(&sm, r);
+        a += o->kz[0], b += o->kz[1];
+      }
+      sm.kz_all[0] = a, sm.kz_all[1] = b;
+    }
+    __syncthreads();
+    if (fix_t) rt.Z = sm.kz_all[0], rt.invZ = 1.0f / rt.Z;
+    if (fix_d) rd.Z = sm.kz_all[1], rd.invZ = 1.0f / rd.Z;
+    cluster.sync();  // peers are done reading kz before it can be rewritten
   }
 }
 
@@ -972,38 +1062,27 @@ __device__ __noinline__ void race_slice(const char* st, const char* sd, const Sl
   best = {bw, bE, bidx};
 }
 
-// Block + cluster argmax of the race partials (slot `slot` of sm.race).  One
-// warp reads the C partials in parallel (lane r <- rank r); `better` is a
-// total order, so the winner does not depend on the reduction order.
+// Block + cluster argmax of the race partials in slot `slot`.  Each warp
+// posts its best; after one cluster barrier every warp reads all C x 8
+// partials (lane l: partials l, l + 32, ...) and reduces them.  `better` is a
+// total order, so every warp of every CTA gets the same winner.
 __device__ __forceinline__ RacePart race_reduce(cg::cluster_group& cluster, Smem& sm, RacePart p,
                                                 int slot) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float bw = p.w, bE = p.E;
   int bidx = p.idx;
   warp_race(bw, bE, bidx);
-  if (lane == 0) sm.scratch_r[warp] = {bw, bE, bidx};
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    RacePart a = sm.scratch_r[0];
-    for (int w = 1; w < kWarps; ++w) {
-      const RacePart o = sm.scratch_r[w];
-      if (better(o.w, o.E, o.idx, a.w, a.E, a.idx)) a = o;
-    }
-    sm.race[slot] = a;
-  }
+  if (lane == 0) sm.rpart[slot][warp] = {bw, bE, bidx};
   cluster.sync();
-  if (warp == 0) {
-    float w = 0.0f, E = 1.0f;
-    int idx = 0x7FFFFFFF;
-    if (lane < (int)cluster.num_blocks()) {
-      const RacePart o = cluster.map_shared_rank(&sm, lane)->race[slot];
-      w = o.w, E = o.E, idx = o.idx;
-    }
-    warp_race(w, E, idx);
-    if (lane == 0) sm.win = {w, E, idx};
+  const int n = (int)cluster.num_blocks() * kWarps;
+  float w = 0.0f, E = 1.0f;
+  int idx = 0x7FFFFFFF;
+  for (int q = lane; q < n; q += 32) {
+    const RacePart o = cluster.map_shared_rank(&sm, q / kWarps)->rpart[slot][q % kWarps];
+    if (better(o.w, o.E, o.idx, w, E, idx)) w = o.w, E = o.E, idx = o.idx;
   }
-  __syncthreads();
-  return sm.win;
+  warp_race(w, E, idx);
+  return {w, E, idx};
 }
 
 // Debug output: normalised probabilities of this thread's groups.
@@ -1022,6 +1101,121 @@ __device__ __noinline__ void write_probs(float* out, const char* s, const SliceI
   }
 }
 
+// ---------------------------------------------------------------------------
+// Tickets.  Rows are handed out in (position, request) order by a counter in
+// the workspace.  The control warp of a cluster (rank 0, last warp) takes the
+// next ticket while the current row's loads are in flight, checks it, and
+// loads the parameters of the row it names into sm.tk[slot]; every CTA reads
+// them from there over DSMEM.
+// ---------------------------------------------------------------------------
+template <int EBT, int EBD>
+__device__ void settle_ticket(const KParams& P, Smem& sm, int t, int slot, uint32_t tag) {
+  const int lane = threadIdx.x & 31;
+  Ticket tk = {0, kDone, 0, 0, 0, 0u, 0.0f, 1.0f, 0.0f, 0.0f};
+  t = __shfl_sync(0xffffffffu, t, 0);
+  while (t < P.n_tickets) {
+    const int i = t / P.B, b = t - i * P.B;
+    const int kb = P.k ? P.k[b] : P.kmax;
+    bool take = true;
+    if (kb < 0 || kb > P.kmax) {  // a bad k ends the request once, at its first row
+      if (i == 0 && lane == 0) write_bad_outputs(P, b, SV_ST_BAD_INPUT);
+      take = false;
+    } else if (i > kb) {
+      take = false;
+    } else if (!(P.flags & SV_FLAG_NO_SKIP) && i > 0 && warp_earlier_rejected(P, b, i, tag)) {
+      if (lane == 0) {
+        st_relaxed(P.row_state + (size_t)b * (P.kmax + 1) + i, tag | SV_ROW_SKIPPED);
+        if (P.debug) P.debug[(size_t)b * (P.kmax + 1) + i].state = SV_ROW_SKIPPED;
+      }
+      take = false;
+    }
+    if (take) {
+      const bool has_d = i < kb;
+      float T = 0.0f, tp = 1.0f;
+      int y = 0, sl = 0;
+      uint32_t rid = (uint32_t)b;
+      if (lane == 0) T = P.temperature[b];  // one parameter per lane: one round trip
+      if (lane == 1 && P.top_p) tp = P.top_p[b];
+      if (lane == 2 && has_d) y = P.tokens[(size_t)b * P.kmax + i];
+      if (lane == 3 && P.seq_len) sl = P.seq_len[b];
+      if (lane == 4 && P.request_id) rid = P.request_id[b];
+      T = __shfl_sync(0xffffffffu, T, 0);
+      tp = __shfl_sync(0xffffffffu, tp, 1);
+      y = __shfl_sync(0xffffffffu, y, 2);
+      sl = __shfl_sync(0xffffffffu, sl, 3);
+      rid = __shfl_sync(0xffffffffu, rid, 4);
+      float vt = 0.0f, vd = 0.0f;  // the accept-test operands
+      if (has_d && y >= 0 && y < P.V) {
+        const char* trow = P.target + ((size_t)b * (P.kmax + 1) + i) * P.t_ld * EBT;
+        const char* drow = P.draft + ((size_t)b * P.kmax + i) * P.d_ld * EBD;
+        if (lane == 0)
+          vt = EBT == 2 ? __uint_as_float((uint32_t)((const uint16_t*)trow)[y] << 16)
+                        : ((const float*)trow)[y];
+        if (lane == 1)
+          vd = EBD == 2 ? __uint_as_float((uint32_t)((const uint16_t*)drow)[y] << 16)
+                        : ((const float*)drow)[y];
+      }
+      vt = __shfl_sync(0xffffffffu, vt, 0);
+      vd = __shfl_sync(0xffffffffu, vd, 1);
+      tk = {t, kWork, kb, y, sl + 1 + i, rid, T, tp, vt, vd};
+      break;
+    }
+    int nt = 0;
+    if (lane == 0) nt = (int)atomicAdd(P.hdr + kHdrTicket, 1u);
+    t = __shfl_sync(0xffffffffu, nt, 0);
+  }
+  tk.t = t;
+  if (lane == 0) sm.tk[slot] = tk;
+  __syncwarp();
+}
+
+// Just before the row that holds it starts: a row whose request has meanwhile
+// seen a rejection is marked skipped and replaced by the next useful ticket.
+template <int EBT, int EBD>
+__device__ void recheck_ticket(const KParams& P, Smem& sm, int slot, uint32_t tag) {
+  const Ticket tk = sm.tk[slot];
+  if (tk.kind != kWork || (P.flags & SV_FLAG_NO_SKIP)) return;
+  const int i = tk.t / P.B, b = tk.t - i * P.B;
+  if (i == 0 || !warp_earlier_rejected(P, b, i, tag)) return;
+  int nt = 0;
+  if ((threadIdx.x & 31) == 0) {
+    st_relaxed(P.row_state + (size_t)b * (P.kmax + 1) + i, tag | SV_ROW_SKIPPED);
+    if (P.debug) P.debug[(size_t)b * (P.kmax + 1) + i].state = SV_ROW_SKIPPED;
+    nt = (int)atomicAdd(P.hdr + kHdrTicket, 1u);
+  }
+  settle_ticket<EBT, EBD>(P, sm, nt, slot, tag);
+}
+
+// Is every earlier row of request b accepted?  Returns 1 (yes: this row
+// decides the request), 0 (an earlier row was not accepted) or 2 (the wait
+// gave up).  Warp-uniform polling: lanes read rows lane and lane + 32.
+__device__ __forceinline__ int warp_wait_earlier(const KParams& P, int b, int i, uint32_t tag,
+                                                 bool& qzero_seen) {
+  const uint32_t* rs = P.row_state + (size_t)b * (P.kmax + 1);
+  const int lane = threadIdx.x & 31;
+  const uint32_t done = tag | SV_ROW_ACCEPTED;
+  for (int spins = 0;; ++spins) {
+    const uint32_t w0 = lane < i ? ld_relaxed(rs + lane) : done;
+    const uint32_t w1 = lane + 32 < i ? ld_relaxed(rs + lane + 32) : done;
+    const bool d0 = (w0 & ~0xFu) == tag && (w0 & kStateMask) != 0;
+    const bool d1 = (w1 & ~0xFu) == tag && (w1 & kStateMask) != 0;
+    const bool n0 = d0 && (w0 & kStateMask) != SV_ROW_ACCEPTED;
+    const bool n1 = d1 && (w1 & kStateMask) != SV_ROW_ACCEPTED;
+    if (__any_sync(0xffffffffu, n0 || n1)) return 0;
+    if (__all_sync(0xffffffffu, d0 && d1)) {
+      qzero_seen = __any_sync(0xffffffffu, ((w0 | w1) & kQZeroBit) != 0u);
+      return 1;
+    }
+    if (spins >= P.spin_limit) return 2;
+    __nanosleep(spins < 16 ? 32 : 256);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The kernel.  A persistent grid of clusters; each cluster works one row
+// (target row i and draft row i of request b) at a time, every CTA on its
+// slice of both rows in shared memory.
+// ---------------------------------------------------------------------------
 template <int EBT, int EBD, bool PROBS>
 __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
   cg::cluster_group cluster = cg::this_cluster();
@@ -1036,68 +1230,31 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
   const uint32_t epoch = *(volatile const uint32_t*)(P.hdr + kHdrEpoch);
   const uint32_t tag = epoch_tag(epoch);
   const uint32_t k0 = P.seed_lo, k1 = P.seed_hi;
-  const bool lead = rank == 0 && tid == 0;
-  const int nblk_max = (P.slice + kBlk - 1) / kBlk;
+  const bool lead = rank == 0 && tid == 0;                // publishes states and outputs
+  const bool ctl = rank == 0 && warp == kWarps - 1;       // takes tickets, resolves
   uint32_t phase_t = 0u, phase_d = 0u;  // mbarrier parity per block (bit blk)
 
   if (tid == 0) {
     for (int j = 0; j < kMaxBlk; ++j) mbar_init(&sm.bar[0][j]), mbar_init(&sm.bar[1][j]);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  __syncthreads();
-
-  // Rank 0 hands out tickets in (position, request) order.  `t` is a ticket
-  // already taken from the counter; rows that do not exist or whose request
-  // already has a known earlier rejection are consumed here.
-  auto settle = [&](int t, int parity) {
-    int kind = kDone;
-    for (;; t = (int)atomicAdd(P.hdr + kHdrTicket, 1u)) {
-      if (t >= P.n_tickets) break;
-      const int i = t / P.B, b = t - i * P.B;
-      const int kb = P.k ? P.k[b] : P.kmax;
-      if (kb < 0 || kb > P.kmax) {
-        if (i == 0) write_bad_outputs(P, b, SV_ST_BAD_INPUT);
-        continue;
-      }
-      if (i > kb) continue;
-      if (!(P.flags & SV_FLAG_NO_SKIP) && earlier_not_accepted(P, b, i, epoch)) {
-        st_release(P.row_state + (size_t)b * (P.kmax + 1) + i, tag | SV_ROW_SKIPPED);
-        if (P.debug) P.debug[(size_t)b * (P.kmax + 1) + i].state = SV_ROW_SKIPPED;
-        continue;
-      }
-      kind = kWork;
-      break;
-    }
-    sm.bcast[parity][0] = t;
-    sm.bcast[parity][1] = kind;
-  };
-
-  if (lead) settle((int)atomicAdd(P.hdr + kHdrTicket, 1u), 0);
+  if (ctl) {
+    int t0 = 0;
+    if (lane == 0) t0 = (int)atomicAdd(P.hdr + kHdrTicket, 1u);
+    settle_ticket<EBT, EBD>(P, sm, t0, 0, tag);
+  }
   cluster.sync();
   for (int iter = 0;; ++iter) {
     const int parity = iter & 1;
-    const int* bc = cluster.map_shared_rank(&sm.bcast[parity][0], 0);
-    const int t = bc[0], kind = bc[1];
-    if (kind == kDone) break;
-    // take the next ticket now; its checks wait until this row is done
-    int next_t = 0;
-    if (lead) next_t = (int)atomicAdd(P.hdr + kHdrTicket, 1u);
+    const Ticket tk = cluster.map_shared_rank(&sm, 0)->tk[parity];
+    if (tk.kind == kDone) break;
 
     // ---------------------------------------------------------------- row setup
+    const int t = tk.t;
     const int i = t / P.B, b = t - i * P.B;
-    const int kb = P.k ? P.k[b] : P.kmax;
-    const bool has_d = i < kb;
-    const float T = P.temperature[b];
-    const float top_p = P.top_p ? P.top_p[b] : 1.0f;
-    const bool params_ok = (T >= 0.0f) && (T <= FLT_MAX) && (top_p > 0.0f) && (top_p <= 1.0f);
-    const int y = has_d ? P.tokens[(size_t)b * P.kmax + i] : 0;
-    const int pos = (P.seq_len ? P.seq_len[b] : 0) + 1 + i;
-    const uint32_t rid = P.request_id ? P.request_id[b] : (uint32_t)b;
-    const bool y_ok = !has_d || (y >= 0 && y < P.V);
+    const bool has_d = i < tk.kb;
     const size_t row_t = (size_t)b * (P.kmax + 1) + i;
     const size_t row_d = (size_t)b * P.kmax + i;
-    const char* trow = P.target + row_t * P.t_ld * EBT;
-    const char* drow = has_d ? P.draft + row_d * P.d_ld * EBD : nullptr;
     SliceIter it;
     it.x0 = rank * P.slice;
     it.x1 = min(P.V, it.x0 + P.slice);
@@ -1106,6 +1263,8 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
 
     // ------------------------------------ TMA: this CTA's slice of both rows
     if (tid == 0) {
+      const char* trow = P.target + row_t * P.t_ld * EBT;
+      const char* drow = P.draft + row_d * P.d_ld * EBD;
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // prior reads before new writes
       for (int blk = 0; blk < it.nblk; ++blk) {
         const int e0 = it.x0 + blk * kBlk, e1 = min(it.x1, e0 + kBlk);
@@ -1118,17 +1277,19 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
           bulk_g2s(s_d + (size_t)blk * kBlk * EBD, drow + (size_t)e0 * EBD, bd, &sm.bar[1][blk]);
         }
       }
-      // the accept-test operands
-      float vt = 0.0f, vd = 0.0f;
-      if (has_d && y_ok) {
-        vt = EBT == 2 ? __uint_as_float((uint32_t)((const uint16_t*)trow)[y] << 16)
-                      : ((const float*)trow)[y];
-        vd = EBD == 2 ? __uint_as_float((uint32_t)((const uint16_t*)drow)[y] << 16)
-                      : ((const float*)drow)[y];
-      }
-      sm.vy[0] = vt, sm.vy[1] = vd;
+    }
+    // the next ticket, while this row's loads are in flight
+    if (ctl) {
+      int nt = 0;
+      if (lane == 0) nt = (int)atomicAdd(P.hdr + kHdrTicket, 1u);
+      settle_ticket<EBT, EBD>(P, sm, nt, parity ^ 1, tag);
     }
 
+    const float T = tk.T, top_p = tk.top_p;
+    const int y = tk.y, pos = tk.pos;
+    const uint32_t rid = tk.rid;
+    const bool params_ok = (T >= 0.0f) && (T <= FLT_MAX) && (top_p > 0.0f) && (top_p <= 1.0f);
+    const bool y_ok = !has_d || (y >= 0 && y < P.V);
     const bool greedy = T == 0.0f;
     RowP rt, rd;
     rt.greedy = rd.greedy = greedy;
@@ -1137,10 +1298,9 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
     rd.c = PROBS ? 1.0f : rt.c;
     rt.Dstar = rd.Dstar = kNoFilter;
 
-    // -------------------------- sweep as blocks land: max + sum (or ties)
-    Online ot, od;
-    online_init(ot, false);
-    online_init(od, PROBS);
+    // ------------------------------- sweep 1: raw maxima as the blocks land
+    uint32_t mt2 = 0xFF80FF80u, md2 = 0xFF80FF80u;
+    float rmt = -INFINITY, rmd = PROBS ? 0.0f : -INFINITY;
     bool landed = true;
 #pragma unroll 1
     for (int blk = 0; blk < it.nblk; ++blk) {
@@ -1150,105 +1310,106 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
       if (x < it.x1) {
         Grp<EBT> g;
         lds_group<EBT, false>(g, s_t, it.x0, x, it.x1);
-        stats_group<EBT, false>(g, greedy, rt.c, rt.invT, ot);
+        max_group<EBT>(g, mt2, rmt);
         if (has_d) {
           Grp<EBD> h;
           lds_group<EBD, PROBS>(h, s_d, it.x0, x, it.x1);
-          stats_group<EBD, PROBS>(h, greedy, rd.c, rd.invT, od);
+          max_group<EBD>(h, md2, rmd);
         }
       }
     }
     phase_t ^= (1u << it.nblk) - 1u;
     if (has_d) phase_d ^= (1u << it.nblk) - 1u;
-    float mt = ot.m, st = online_sum(ot, greedy), md = od.m, sd = online_sum(od, greedy);
-    float rmd = od.raw;
-    const float cc_t = rt.c, cc_d = rd.c;
+    rmt = max_value<EBT>(mt2, rmt);
+    rmd = max_value<EBD>(md2, rmd);
+    // this thread's maxima in the weight domain
+    float mt = rmt;
+    float md = (PROBS && !greedy) ? (rmd > 0.0f ? lg2(rmd) * rd.invT : -INFINITY) : rmd;
+
+    // ----------------------------------------- sweep 2: sums of the weights
+    float st = 0.0f, sd = 0.0f;
+#pragma unroll 2
+    for (int blk = 0; blk < it.nblk; ++blk) {
+      const int x = it.x(blk);
+      if (x < it.x1) {
+        Grp<EBT> g;
+        lds_group<EBT, false>(g, s_t, it.x0, x, it.x1);
+        st += sum_group<EBT, false>(g, greedy, mt, rt.c, rt.invT);
+        if (has_d) {
+          Grp<EBD> h;
+          lds_group<EBD, PROBS>(h, s_d, it.x0, x, it.x1);
+          sd += sum_group<EBD, PROBS>(h, greedy, md, rd.c, rd.invT);
+        }
+      }
+    }
+
+    // ---------------- combine: warps post partials, every warp reduces all
+    warp_ms(mt, st, rt.c, greedy);
+    warp_ms(md, sd, rd.c, greedy);
 #pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, mt, o), s2 = __shfl_xor_sync(0xffffffffu, st, o);
-      const float m3 = __shfl_xor_sync(0xffffffffu, md, o), s3 = __shfl_xor_sync(0xffffffffu, sd, o);
-      rmd = fmaxf(rmd, __shfl_xor_sync(0xffffffffu, rmd, o));
-      if (greedy) {
-        combine_ties(mt, st, m2, s2);
-        combine_ties(md, sd, m3, s3);
-      } else {
-        combine_ms(mt, st, m2, s2, cc_t);
-        combine_ms(md, sd, m3, s3, cc_d);
-      }
-    }
-    if (lane == 0) {
-      sm.scratch_f[warp][0] = mt, sm.scratch_f[warp][1] = st;
-      sm.scratch_f[warp][2] = md, sm.scratch_f[warp][3] = sd;
-      sm.scratch_r[warp].w = rmd;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      float a = sm.scratch_f[0][0], s = sm.scratch_f[0][1];
-      float c2 = sm.scratch_f[0][2], d2 = sm.scratch_f[0][3], rm = sm.scratch_r[0].w;
-      for (int w = 1; w < kWarps; ++w) {
-        rm = fmaxf(rm, sm.scratch_r[w].w);
-        if (greedy) {
-          combine_ties(a, s, sm.scratch_f[w][0], sm.scratch_f[w][1]);
-          combine_ties(c2, d2, sm.scratch_f[w][2], sm.scratch_f[w][3]);
-        } else {
-          combine_ms(a, s, sm.scratch_f[w][0], sm.scratch_f[w][1], cc_t);
-          combine_ms(c2, d2, sm.scratch_f[w][2], sm.scratch_f[w][3], cc_d);
-        }
-      }
-      sm.st_m[0] = a, sm.st_s[0] = s, sm.st_m[1] = c2, sm.st_s[1] = d2;
-      sm.st_raw = rm;
-      sm.st_bad = landed ? 0 : 1;
-    }
+    for (int o = 16; o; o >>= 1) rmd = fmaxf(rmd, __shfl_xor_sync(0xffffffffu, rmd, o));
+    const bool warp_bad = __any_sync(0xffffffffu, !landed);
+    if (lane == 0)
+      sm.part[warp] = {make_float4(mt, st, rmd, warp_bad ? 1.0f : 0.0f), make_float4(md, sd, 0.0f, 0.0f)};
     cluster.sync();  // partials visible cluster-wide
-    if (warp == 0) {
-      // lane r fetches rank r's partials (all remote loads in flight at once),
-      // lane 0 combines them in rank order so every CTA gets identical values
-      float pm0 = -INFINITY, ps0 = 0.0f, pm1 = -INFINITY, ps1 = 0.0f;
-      float praw = PROBS ? 0.0f : -INFINITY;
-      int pbad = 0;
-      if (lane < C) {
-        const Smem* o = cluster.map_shared_rank(&sm, lane);
-        pm0 = o->st_m[0], ps0 = o->st_s[0], pm1 = o->st_m[1], ps1 = o->st_s[1], praw = o->st_raw;
-        pbad = o->st_bad;
-      }
-      float a = -INFINITY, s2 = 0.0f, c2 = -INFINITY, d2 = 0.0f, rm = PROBS ? 0.0f : -INFINITY;
-      for (int r = 0; r < C; ++r) {
-        const float ma = __shfl_sync(0xffffffffu, pm0, r), sa = __shfl_sync(0xffffffffu, ps0, r);
-        const float mb = __shfl_sync(0xffffffffu, pm1, r), sb = __shfl_sync(0xffffffffu, ps1, r);
-        rm = fmaxf(rm, __shfl_sync(0xffffffffu, praw, r));
-        if (greedy) {
-          combine_ties(a, s2, ma, sa);
-          combine_ties(c2, d2, mb, sb);
+    {
+      const int n = C * kWarps;
+      float4 A[4], D[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {  // all remote loads in flight together
+        const int q = lane + 32 * r;
+        if (q < n) {
+          const StatPart* o = &cluster.map_shared_rank(&sm, q / kWarps)->part[q % kWarps];
+          A[r] = o->a, D[r] = o->d;
         } else {
-          combine_ms(a, s2, ma, sa, cc_t);
-          combine_ms(c2, d2, mb, sb, cc_d);
+          A[r] = make_float4(-INFINITY, 0.0f, PROBS ? 0.0f : -INFINITY, 0.0f);
+          D[r] = make_float4(-INFINITY, 0.0f, 0.0f, 0.0f);
         }
       }
-      const int anybad = __any_sync(0xffffffffu, pbad);
-      if (lane == 0) {
-        sm.comb[0] = a, sm.comb[1] = s2, sm.comb[2] = c2, sm.comb[3] = d2, sm.comb[4] = rm;
-        sm.comb_bad = anybad;
+      float Mt = -INFINITY, Md = -INFINITY, Rm = PROBS ? 0.0f : -INFINITY;
+      bool bad = false;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        Mt = fmaxf(Mt, A[r].x), Md = fmaxf(Md, D[r].x), Rm = fmaxf(Rm, A[r].z);
+        bad |= A[r].w != 0.0f;
       }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        Mt = fmaxf(Mt, __shfl_xor_sync(0xffffffffu, Mt, o));
+        Md = fmaxf(Md, __shfl_xor_sync(0xffffffffu, Md, o));
+        Rm = fmaxf(Rm, __shfl_xor_sync(0xffffffffu, Rm, o));
+      }
+      float St = 0.0f, Sd = 0.0f;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        St += rescale(A[r].x, A[r].y, Mt, rt.c, greedy);
+        Sd += rescale(D[r].x, D[r].y, Md, rd.c, greedy);
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        St += __shfl_xor_sync(0xffffffffu, St, o);
+        Sd += __shfl_xor_sync(0xffffffffu, Sd, o);
+      }
+      bad = __any_sync(0xffffffffu, bad);
+      rt.m = rt.mz = Mt, rt.S = St;
+      rd.m = Rm;   // raw maximum (logit or probability): defines the top-p keys
+      rd.mz = Md;  // maximum in the weight domain (== raw max except probabilities, T > 0)
+      rd.S = Sd;
+      if (bad) rt.S = __int_as_float(0x7FC00000);  // a slice never landed: the row is invalid
     }
-    __syncthreads();
-    rt.m = sm.comb[0], rt.mz = sm.comb[0], rt.S = sm.comb[1];
-    rd.S = sm.comb[3];
-    rd.m = sm.comb[4];   // raw maximum (logit or probability): defines the top-p keys
-    rd.mz = sm.comb[2];  // maximum in the weight domain (== raw max except probabilities, T > 0)
     rt.kmax = vkey<EBT>(rt.m);
     rd.kmax = vkey<EBD>(rd.m);
     rt.Z = rt.S, rd.Z = rd.S;
     rt.invZ = 1.0f / rt.Z, rd.invZ = 1.0f / rd.Z;
     rt.vstar = -INFINITY;
     rd.vstar = PROBS ? 0.0f : -INFINITY;
-    const float vty = sm.vy[0], vdy = sm.vy[1];
 
     // NaN / +inf inputs surface as a non-finite sum or maximum
     const bool bad_t = !(rt.S >= 1.0f && rt.S <= FLT_MAX) || !(rt.m <= FLT_MAX) ||
                        rt.m == -INFINITY;
     const bool bad_d = has_d && (!(rd.S >= 1.0f && rd.S <= FLT_MAX) || !(rd.m <= FLT_MAX) ||
                                  (PROBS ? !(rd.m > 0.0f) : rd.m == -INFINITY));
-    const bool row_bad = bad_t || bad_d || !params_ok || !y_ok || sm.comb_bad;
+    const bool row_bad = bad_t || bad_d || !params_ok || !y_ok;
 
     // ---------------------------------------------------------------- top-p
     if (!row_bad && !greedy && top_p < 1.0f)
@@ -1262,8 +1423,8 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
     if (row_bad) {
       state = SV_ROW_INVALID;
     } else if (has_d) {
-      p_y = prob<EBT, false>(vty, rt);
-      q_y = prob<EBD, PROBS>(vdy, rd);
+      p_y = prob<EBT, false>(tk.vt, rt);
+      q_y = prob<EBD, PROBS>(tk.vd, rd);
       const uint4 r = philox4x32_10(make_uint4(0u, (uint32_t)pos, rid, 1u), k0, k1);
       u = uniform_from_bits(r.x);
       qzero = q_y == 0.0f;
@@ -1272,7 +1433,7 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
       state = SV_ROW_BONUS;
     }
     if (lead) {
-      st_release(P.row_state + row_t, tag | (qzero ? kQZeroBit : 0u) | (uint32_t)state);
+      st_relaxed(P.row_state + row_t, tag | (qzero ? kQZeroBit : 0u) | (uint32_t)state);
       if (P.debug) {
         sv_row_debug d;
         d.p_y = p_y, d.q_y = q_y, d.u = u;
@@ -1292,37 +1453,21 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
 
     // --------------------------------------------- resolve: is this row the one?
     if (state != SV_ROW_ACCEPTED) {
-      if (lead) {
-        int resolver = 1;
-        uint32_t st_bits = qzero ? SV_ST_Q_ZERO : 0u;
-        const uint32_t* rs = P.row_state + (size_t)b * (P.kmax + 1);
-        for (int j = 0; j < i && resolver == 1; ++j) {
-          uint32_t w = 0;
-          int spins = 0;
-          for (;;) {
-            w = ld_acquire(rs + j);
-            if ((w & ~0xFu) == tag && (w & kStateMask) != 0) break;
-            if (++spins > P.spin_limit) {
-              resolver = 2;
-              break;
-            }
-            __nanosleep(spins < 16 ? 32 : 256);
+      if (ctl) {
+        bool qz = false;
+        int resolver = warp_wait_earlier(P, b, i, tag, qz);
+        if (lane == 0) {
+          if (resolver == 2) {
+            report(P.err, SV_ERR_TIMEOUT);
+            write_bad_outputs(P, b, SV_ST_TIMEOUT);
+            resolver = 0;
+          } else if (resolver == 1 && state == SV_ROW_INVALID) {
+            write_bad_outputs(P, b, SV_ST_BAD_INPUT);
+            resolver = 0;
           }
-          if (resolver == 2) break;
-          if ((w & kStateMask) != SV_ROW_ACCEPTED) resolver = 0;
-          if (w & kQZeroBit) st_bits |= SV_ST_Q_ZERO;
+          sm.decide[0] = resolver;
+          sm.decide[1] = (int)((qzero || qz) ? SV_ST_Q_ZERO : 0u);
         }
-        if (resolver == 2) {
-          report(P.err, SV_ERR_TIMEOUT);
-          write_bad_outputs(P, b, SV_ST_TIMEOUT);
-          resolver = 0;
-        }
-        if (resolver == 1 && state == SV_ROW_INVALID) {
-          write_bad_outputs(P, b, SV_ST_BAD_INPUT);
-          resolver = 0;
-        }
-        sm.decide[0] = resolver;
-        sm.decide[1] = (int)st_bits;
       }
       cluster.sync();
       const int* dc = cluster.map_shared_rank(&sm.decide[0], 0);
@@ -1355,8 +1500,9 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
       }
     }
 
-    // settle the next ticket, then the end-of-row barrier publishes it
-    if (lead) settle(next_t, parity ^ 1);
+    // the next row may have become skippable meanwhile; the end-of-row
+    // barrier then publishes its ticket
+    if (ctl) recheck_ticket<EBT, EBD>(P, sm, parity ^ 1, tag);
     cluster.sync();
   }
 
@@ -1373,7 +1519,6 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
       atomicAdd(P.hdr + kHdrEpoch, 1u);
     }
   }
-  (void)nblk_max;
 }
 
 using KernelFn = void (*)(KParams);

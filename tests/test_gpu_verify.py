@@ -82,6 +82,40 @@ def test_ragged_probs_top_p(ver):
     assert parity.compare_debug(inp, dbg) > 0
 
 
+def test_top_p_boundary_outside_the_first_window(ver):
+    """Rows whose top-p boundary sits in a plateau of up to 120000 tied logits.
+    The kernel's first window assumes few elements below the boundary, so on
+    these rows the boundary falls below it (or beyond the 256-key window) and
+    the exact radix descent must decide it; b = 1 sits just inside the window."""
+    V = 128256
+    inp = W.paged_bf16(B=4, k=2, V=V, forced=False)
+    rng = np.random.default_rng(77)
+    # (top logit, plateau size, plateau logit) per request; T = 1, top_p = 0.95
+    shapes = [(20.0, 120000, 6.0), (20.0, 100000, 8.0), (0.0, 3000, -9.0), None]
+    for b, shape in enumerate(shapes):
+        for arr, rows in (("target", 3), ("draft", 2)):
+            for i in range(rows):
+                if shape is None:
+                    x = rng.standard_normal(V).astype(np.float32) * np.float32(3.0)
+                else:
+                    top, n, lvl = shape
+                    x = np.full(V, -30.0, np.float32)
+                    idx = rng.choice(V, n + 1, replace=False)
+                    x[idx[:n]] = lvl + (0.5 if arr == "draft" and i == 1 else 0.0)
+                    x[idx[n]] = top
+                inp[arr][b, i] = W.to_bf16_bits(x)
+    inp["temperature"][:] = 1.0
+    inp["top_p"][:] = 0.95
+    W._sample_tokens(inp, np.random.default_rng(3077))
+    out, dbg, _, _ = run(ver, inp, debug=True)
+    report("top-p plateau", parity.compare(inp, out))
+    assert parity.compare_debug(inp, dbg) > 0
+    # the plateau is inside the nucleus of the target's first row (b = 0, 1, 2)
+    for b in range(3):
+        p, info = S.transform(S.decode(inp["target"][b, 0], "bf16"), "logits", 1.0, 0.95)
+        assert int(info["kept"].sum()) > 1000
+
+
 @pytest.mark.parametrize("top_p", [0.95, 1.0])
 def test_verify_b64_k4(ver, top_p):
     inp = W.verify_b64_k4(top_p=top_p)
