@@ -59,7 +59,7 @@ constexpr uint32_t kNoFilter = 0xFFFFFFFFu;
 constexpr int kMaxCluster = 16;
 constexpr int kMaxK = 64;
 constexpr int kDefaultSpin = 1 << 20;
-constexpr int kWindowGuess = 4096;  // elements assumed below a top-p boundary (see top_p_rows)
+constexpr int kWindowGuess = 2048;  // elements assumed below a top-p boundary (see top_p_rows)
 constexpr float kEminSafe = 5.9604e-8f;  // <= -ln(1 - 2^-24), the smallest E
 
 // workspace header words
@@ -288,7 +288,7 @@ struct RowRes {
   uint32_t Dstar;
   float Z, invZ, vstar;
 };
-using TopLvSlot = TopLv;
+
 
 // Parameters of one ticket's row, prepared by rank 0's warp 0 and read by
 // every CTA of the cluster through DSMEM.
@@ -308,15 +308,19 @@ struct Smem {
   unsigned long long bar[2][kMaxBlk];  // TMA completion: [target / draft][block]
   Ticket tk[2];              // [iteration parity] the row to work on (rank 0 only)
   int decide[4];             // resolver decision (rank 0 only)
-  StatPart part[kWarps];     // per-warp stats partials, read over DSMEM
+  StatPart part[kWarps];     // per-warp maxima partials
+  StatPart cpart;            // the CTA's maxima partial, read over DSMEM
+  float2 spart[kWarps];      // per-warp weight-sum partials (target, draft)
+  float2 cspart;             // the CTA's weight sums, read over DSMEM
   alignas(16) uint32_t hist[2][2][256];  // [buffer][row][bin]; read as uint4 over DSMEM
-  RacePart rpart[2][kWarps]; // per-warp race partials [slot], read over DSMEM
+  RacePart rpart[2][kWarps]; // per-warp race partials [slot]
+  RacePart crpart[2];        // the CTA's race winner [slot], read over DSMEM
   union {
     uint16_t idx[kWarps][256];  // race candidates (slice element index)
     uint8_t bin[kWarps][512];   // window bins
   } wb;                         // per-warp compaction buffers
   float kz[2], kz_all[2];    // kept-mass partials (read over DSMEM) and totals
-  TopLvSlot lv[2];           // top-p search state (local broadcast)
+  TopLv lv[2];               // top-p search state (local broadcast)
   RowRes rres[2];            // top-p results (local broadcast)
   float scratch_f[kWarps][4];
 };
@@ -554,6 +558,33 @@ __device__ __forceinline__ void warp_ms(float& m, float& s, float c, bool greedy
   m = M, s = S;
 }
 
+// Combine stats partials held one per lane (lanes without one hold the
+// neutral partial): a = (target max, target sum, draft raw maximum, failure
+// flag), d = (draft max, draft sum).  Every lane ends with the same result.
+template <bool PROBS>
+__device__ __forceinline__ StatPart neutral_part() {
+  return {make_float4(-INFINITY, 0.0f, PROBS ? 0.0f : -INFINITY, 0.0f),
+          make_float4(-INFINITY, 0.0f, 0.0f, 0.0f)};
+}
+
+__device__ __forceinline__ StatPart combine_parts(const StatPart& v, float ct, float cd, bool greedy) {
+  float Mt = v.a.x, Md = v.d.x, Rm = v.a.z, bad = v.a.w;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    Mt = fmaxf(Mt, __shfl_xor_sync(0xffffffffu, Mt, o));
+    Md = fmaxf(Md, __shfl_xor_sync(0xffffffffu, Md, o));
+    Rm = fmaxf(Rm, __shfl_xor_sync(0xffffffffu, Rm, o));
+    bad = fmaxf(bad, __shfl_xor_sync(0xffffffffu, bad, o));
+  }
+  float St = rescale(v.a.x, v.a.y, Mt, ct, greedy), Sd = rescale(v.d.x, v.d.y, Md, cd, greedy);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    St += __shfl_xor_sync(0xffffffffu, St, o);
+    Sd += __shfl_xor_sync(0xffffffffu, Sd, o);
+  }
+  return {make_float4(Mt, St, Rm, bad), make_float4(Md, Sd, 0.0f, 0.0f)};
+}
+
 // Warp-inclusive scan of a per-lane count.
 __device__ __forceinline__ int warp_incl_scan(int v) {
   const int lane = threadIdx.x & 31;
@@ -593,24 +624,24 @@ __device__ __forceinline__ uint32_t bf16_order_key(uint32_t b16) {
 // loop that re-reads each hit from shared memory: unrolled copies of it made
 // the code large enough that instruction fetch dominated.  A window too dense
 // for the buffer goes one group column at a time.
-__device__ __forceinline__ void window_row_bf16(const char* s, const SliceIter& it, uint32_t kmax,
-                                                uint32_t lo_key, uint32_t* hist, uint8_t* wb) {
-  const uint32_t thr2 = bf16_pair_of(vkey_value<2>(lo_key));
-  uint4 g[kMaxBlk];  // all loads first: their latencies overlap
-#pragma unroll
-  for (int blk = 0; blk < kMaxBlk; ++blk) g[blk] = load_group_bf16(s, it, blk);
-  uint32_t mlo = 0u, mhi = 0u;
-  int cnt = 0;
-#pragma unroll
-  for (int blk = 0; blk < kMaxBlk; ++blk) {
-    const int x = it.x(blk);
-    uint32_t m = bge2(g[blk].x, thr2) | (bge2(g[blk].y, thr2) << 2) | (bge2(g[blk].z, thr2) << 4) |
-                 (bge2(g[blk].w, thr2) << 6);
-    if (x + kGroup > it.x1) m = x < it.x1 ? m & ((1u << (it.x1 - x)) - 1u) : 0u;  // past the end
-    cnt += __popc(m);
-    if (blk < 4) mlo |= m << (8 * blk);
-    else mhi |= m << (8 * (blk - 4));
-  }
+// Candidate bits of one bf16 group: element e >= the floor pair thr2 (bit e),
+// lanes at or past the row end dropped.
+__device__ __forceinline__ uint32_t window_bits_bf16(const uint4& g, uint32_t thr2, int x, int x1) {
+  uint32_t m = bge2(g.x, thr2) | (bge2(g.y, thr2) << 2) | (bge2(g.z, thr2) << 4) |
+               (bge2(g.w, thr2) << 6);
+  if (x + kGroup > x1) m = x < x1 ? m & ((1u << (x1 - x)) - 1u) : 0u;  // past the end
+  return m;
+}
+
+// Histogram the candidates of the thread's 8 groups (bits mlo: groups 0-3,
+// mhi: groups 4-7; cnt of them).  One warp scan places the candidates in the
+// warp's buffer and the atomics run on full warps.  The candidate walk is a
+// single loop that re-reads each hit from shared memory: unrolled copies of
+// it made the code large enough that instruction fetch dominated.  A window
+// too dense for the buffer goes one group column at a time.
+__device__ __forceinline__ void window_commit_bf16(const char* s, uint32_t kmax, uint32_t mlo,
+                                                   uint32_t mhi, int cnt, const SliceIter& it,
+                                                   uint32_t* hist, uint8_t* wb) {
   const int incl = warp_incl_scan(cnt);
   const int total = __shfl_sync(0xffffffffu, incl, 31);
   if (total == 0) return;
@@ -644,6 +675,28 @@ __device__ __forceinline__ void window_row_bf16(const char* s, const SliceIter& 
     }
     flush_bins(hist, wb, tot);
   }
+}
+
+// Exact window histogram for bf16 rows: count elements by bf16 order-key
+// distance D = kmax - key(v) for keys in [lo_key, kmax] (one bin per bf16
+// value, at most 256).  The thread's 8 groups are loaded together (their
+// latencies overlap) and turned into candidate bits.
+__device__ __forceinline__ void window_row_bf16(const char* s, const SliceIter& it, uint32_t kmax,
+                                                uint32_t lo_key, uint32_t* hist, uint8_t* wb) {
+  const uint32_t thr2 = bf16_pair_of(vkey_value<2>(lo_key));
+  uint4 g[kMaxBlk];
+#pragma unroll
+  for (int blk = 0; blk < kMaxBlk; ++blk) g[blk] = load_group_bf16(s, it, blk);
+  uint32_t mlo = 0u, mhi = 0u;
+  int cnt = 0;
+#pragma unroll
+  for (int blk = 0; blk < kMaxBlk; ++blk) {
+    const uint32_t m = window_bits_bf16(g[blk], thr2, it.x(blk), it.x1);
+    cnt += __popc(m);
+    if (blk < 4) mlo |= m << (8 * blk);
+    else mhi |= m << (8 * (blk - 4));
+  }
+  window_commit_bf16(s, kmax, mlo, mhi, cnt, it, hist, wb);
 }
 
 // Lowest key a top-p boundary can have when at most n elements lie below it:
@@ -680,8 +733,8 @@ __device__ __forceinline__ void level_group(const Grp<EB>& g, const RowP& r, uin
 }
 
 // One warp resolves one level of one row: gathers the C ranks' 256-bin
-// histograms (lane l owns bins 8l .. 8l+7, all remote loads in flight
-// together), scans them in the warp, and picks the boundary bin.  Every CTA
+// histograms (lane l owns bins 8l .. 8l+7; the remote loads of four ranks
+// are in flight together), scans them in the warp, and picks the boundary bin.  Every CTA
 // runs the same arithmetic on the same data, so all reach the same result.
 template <int EB, bool PROBS>
 __device__ __forceinline__ void resolve_level(cg::cluster_group& cluster, const uint32_t* hist, int C,
@@ -691,11 +744,11 @@ __device__ __forceinline__ void resolve_level(cg::cluster_group& cluster, const 
 #pragma unroll
   for (int k = 0; k < 8; ++k) h[k] = 0.0f;
 #pragma unroll
-  for (int q0 = 0; q0 < kMaxCluster; q0 += 2) {
+  for (int q0 = 0; q0 < kMaxCluster; q0 += 4) {
     if (q0 < C) {
-      uint4 a[2], b[2];
+      uint4 a[4], b[4];
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
+      for (int q = 0; q < 4; ++q) {
         if (q0 + q < C) {
           const uint4* src = reinterpret_cast<const uint4*>(cluster.map_shared_rank(hist, q0 + q)) + 2 * lane;
           a[q] = src[0], b[q] = src[1];
@@ -704,7 +757,7 @@ __device__ __forceinline__ void resolve_level(cg::cluster_group& cluster, const 
         }
       }
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {  // rank order
+      for (int q = 0; q < 4; ++q) {  // rank order
         const uint32_t w[8] = {a[q].x, a[q].y, a[q].z, a[q].w, b[q].x, b[q].y, b[q].z, b[q].w};
 #pragma unroll
         for (int k = 0; k < 8; ++k) h[k] += lv.window ? (float)w[k] : __uint_as_float(w[k]);
@@ -783,7 +836,7 @@ __device__ __forceinline__ void resolve_level(cg::cluster_group& cluster, const 
 template <int EBT, int EBD, bool PROBS>
 __device__ __noinline__ void top_p_rows(cg::cluster_group& cluster, Smem& sm, const char* st,
                                         const char* sd, const SliceIter& it, bool has_d,
-                                        float top_p, RowP& rt, RowP& rd) {
+                                        float top_p, RowP& rt, RowP& rd, bool pre_t, bool pre_d) {
   const int C = cluster.num_blocks();
   const int tid = threadIdx.x;
   TopLv L[2];
@@ -797,24 +850,30 @@ __device__ __noinline__ void top_p_rows(cg::cluster_group& cluster, Smem& sm, co
   // When the boundary is not inside that window, resolve_level retries with
   // the bound (n = V) and then falls back to the exact radix descent, so the
   // result never depends on the guess.
+  // A row whose first window the caller already counted into sm.hist[0]
+  // (pre_t / pre_d, visible cluster-wide) goes straight to its resolve.
   const int nguess = min(it.V, kWindowGuess);
   int buf = 0;
-  while (!(L[0].done && L[1].done)) {
+  for (bool first = true; !(L[0].done && L[1].done); first = false) {
+    const bool bt = !L[0].done && !(first && pre_t);  // rows counted in this round
+    const bool bd = !L[1].done && !(first && pre_d);
+    if (bt || bd) {
     if constexpr (EBT == 2) lo_t = rt.kmax - window_lo_key(rt, top_p, L[0].guess ? nguess : it.V);
     if constexpr (EBD == 2 && !PROBS)
       lo_d = rd.kmax - window_lo_key(rd, top_p, L[1].guess ? nguess : it.V);
-    for (int j = tid; j < 512; j += kThreads) (&sm.hist[buf][0][0])[j] = 0u;
+    if (bt) for (int j = tid; j < 256; j += kThreads) sm.hist[buf][0][j] = 0u;
+    if (bd) for (int j = tid; j < 256; j += kThreads) sm.hist[buf][1][j] = 0u;
     __syncthreads();
     if constexpr (EBT == 2) {
-      if (!L[0].done && L[0].window)
+      if (bt && L[0].window)
         window_row_bf16(st, it, rt.kmax, rt.kmax - lo_t, sm.hist[buf][0], sm.wb.bin[tid >> 5]);
     }
     if constexpr (EBD == 2 && !PROBS) {
-      if (!L[1].done && L[1].window)
+      if (bd && L[1].window)
         window_row_bf16(sd, it, rd.kmax, rd.kmax - lo_d, sm.hist[buf][1], sm.wb.bin[tid >> 5]);
     }
-    const bool gen_t = !L[0].done && !(EBT == 2 && L[0].window);
-    const bool gen_d = !L[1].done && !(EBD == 2 && !PROBS && L[1].window);
+    const bool gen_t = bt && !(EBT == 2 && L[0].window);
+    const bool gen_d = bd && !(EBD == 2 && !PROBS && L[1].window);
     if (gen_t || gen_d) {
 #pragma unroll 1
       for (int blk = 0; blk < it.nblk; ++blk) {
@@ -834,6 +893,7 @@ __device__ __noinline__ void top_p_rows(cg::cluster_group& cluster, Smem& sm, co
     }
     __syncthreads();
     cluster.sync();
+    }
     // warp 0 resolves the target row, warp 1 the draft row; one barrier
     // publishes both results to the whole CTA
     const int warp = tid >> 5;
@@ -1062,10 +1122,10 @@ __device__ __noinline__ void race_slice(const char* st, const char* sd, const Sl
   best = {bw, bE, bidx};
 }
 
-// Block + cluster argmax of the race partials in slot `slot`.  Each warp
-// posts its best; after one cluster barrier every warp reads all C x 8
-// partials (lane l: partials l, l + 32, ...) and reduces them.  `better` is a
-// total order, so every warp of every CTA gets the same winner.
+// Block + cluster argmax of the race partials in slot `slot`: warp winners
+// meet in warp 0, which posts the CTA's winner; after one cluster barrier
+// every warp reduces the C CTA winners.  `better` is a total order, so every
+// warp of every CTA gets the same winner.
 __device__ __forceinline__ RacePart race_reduce(cg::cluster_group& cluster, Smem& sm, RacePart p,
                                                 int slot) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -1073,16 +1133,17 @@ __device__ __forceinline__ RacePart race_reduce(cg::cluster_group& cluster, Smem
   int bidx = p.idx;
   warp_race(bw, bE, bidx);
   if (lane == 0) sm.rpart[slot][warp] = {bw, bE, bidx};
-  cluster.sync();
-  const int n = (int)cluster.num_blocks() * kWarps;
-  float w = 0.0f, E = 1.0f;
-  int idx = 0x7FFFFFFF;
-  for (int q = lane; q < n; q += 32) {
-    const RacePart o = cluster.map_shared_rank(&sm, q / kWarps)->rpart[slot][q % kWarps];
-    if (better(o.w, o.E, o.idx, w, E, idx)) w = o.w, E = o.E, idx = o.idx;
+  __syncthreads();
+  if (warp == 0) {
+    RacePart o = lane < kWarps ? sm.rpart[slot][lane] : RacePart{0.0f, 1.0f, 0x7FFFFFFF};
+    warp_race(o.w, o.E, o.idx);
+    if (lane == 0) sm.crpart[slot] = o;
   }
-  warp_race(w, E, idx);
-  return {w, E, idx};
+  cluster.sync();
+  RacePart o = lane < (int)cluster.num_blocks() ? cluster.map_shared_rank(&sm, lane)->crpart[slot]
+                                                : RacePart{0.0f, 1.0f, 0x7FFFFFFF};
+  warp_race(o.w, o.E, o.idx);
+  return o;
 }
 
 // Debug output: normalised probabilities of this thread's groups.
@@ -1323,82 +1384,135 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
     rmt = max_value<EBT>(mt2, rmt);
     rmd = max_value<EBD>(md2, rmd);
     // this thread's maxima in the weight domain
-    float mt = rmt;
-    float md = (PROBS && !greedy) ? (rmd > 0.0f ? lg2(rmd) * rd.invT : -INFINITY) : rmd;
+    const float mt = rmt;
+    const float md = (PROBS && !greedy) ? (rmd > 0.0f ? lg2(rmd) * rd.invT : -INFINITY) : rmd;
+    // bf16 logit rows with top_p < 1 count their top-p window during sweep 2
+    const bool topp = !greedy && top_p < 1.0f && params_ok;
+    const bool win_t = EBT == 2 && topp;
+    const bool win_d = EBD == 2 && !PROBS && topp && has_d;
+    if (win_t || win_d)
+      for (int j = tid; j < 512; j += kThreads) (&sm.hist[0][0][0])[j] = 0u;
 
-    // ----------------------------------------- sweep 2: sums of the weights
+    // ------ exchange 1: row maxima, and a lower bound of the weight sums
+    // Every thread's own maximum weighs 1 relative to itself, so the sum over
+    // threads of 2^((m_thread - M) c) is at most the row's weight sum S.
+    {
+      float Mw = mt, Lw = mt == -INFINITY ? 0.0f : 1.0f;
+      float Nw = md, Kw = md == -INFINITY ? 0.0f : 1.0f;
+      warp_ms(Mw, Lw, rt.c, greedy);
+      warp_ms(Nw, Kw, rd.c, greedy);
+      float Rw = rmd;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) Rw = fmaxf(Rw, __shfl_xor_sync(0xffffffffu, Rw, o));
+      const bool warp_bad = __any_sync(0xffffffffu, !landed);
+      if (lane == 0)
+        sm.part[warp] = {make_float4(Mw, Lw, Rw, warp_bad ? 1.0f : 0.0f), make_float4(Nw, Kw, 0.0f, 0.0f)};
+    }
+    __syncthreads();
+    if (warp == 0) {  // the CTA's partial
+      const StatPart c = combine_parts(lane < kWarps ? sm.part[lane] : neutral_part<PROBS>(), rt.c,
+                                       rd.c, greedy);
+      if (lane == 0) sm.cpart = c;
+    }
+    cluster.sync();  // partials visible cluster-wide
+    float St_lb, Sd_lb;
+    bool slice_bad;
+    {
+      const StatPart c = combine_parts(
+          lane < C ? cluster.map_shared_rank(&sm, lane)->cpart : neutral_part<PROBS>(), rt.c, rd.c, greedy);
+      rt.m = rt.mz = c.a.x;
+      rd.m = c.a.z;   // raw maximum (logit or probability): defines the top-p keys
+      rd.mz = c.d.x;  // maximum in the weight domain (== raw max except probabilities, T > 0)
+      St_lb = c.a.y, Sd_lb = c.d.y;
+      slice_bad = c.a.w != 0.0f;
+    }
+    rt.kmax = vkey<EBT>(rt.m);
+    rd.kmax = vkey<EBD>(rd.m);
+
+    // window floors from the lower bound of S (a lower floor than S gives)
+    uint32_t thr2_t = 0x7FFF7FFFu, thr2_d = 0x7FFF7FFFu;  // NaN pairs: nothing passes
+    const int nguess = min(P.V, kWindowGuess);
+    if (win_t) {
+      RowP q = rt;
+      q.S = St_lb;
+      thr2_t = bf16_pair_of(vkey_value<2>(window_lo_key(q, top_p, nguess)));
+    }
+    if (win_d) {
+      RowP q = rd;
+      q.S = Sd_lb;
+      thr2_d = bf16_pair_of(vkey_value<2>(window_lo_key(q, top_p, nguess)));
+    }
+
+    // ------------- sweep 2: weight sums to the row maxima, window candidates
     float st = 0.0f, sd = 0.0f;
+    uint32_t wt_lo = 0u, wt_hi = 0u, wd_lo = 0u, wd_hi = 0u;
+    int wt_n = 0, wd_n = 0;
 #pragma unroll 2
     for (int blk = 0; blk < it.nblk; ++blk) {
       const int x = it.x(blk);
       if (x < it.x1) {
         Grp<EBT> g;
         lds_group<EBT, false>(g, s_t, it.x0, x, it.x1);
-        st += sum_group<EBT, false>(g, greedy, mt, rt.c, rt.invT);
+        st += sum_group<EBT, false>(g, greedy, rt.mz, rt.c, rt.invT);
+        if constexpr (EBT == 2) {
+          if (win_t) {
+            const uint32_t m = window_bits_bf16(make_uint4(g.w[0], g.w[1], g.w[2], g.w[3]), thr2_t, x, it.x1);
+            wt_n += __popc(m);
+            if (blk < 4) wt_lo |= m << (8 * blk);
+            else wt_hi |= m << (8 * (blk - 4));
+          }
+        }
         if (has_d) {
           Grp<EBD> h;
           lds_group<EBD, PROBS>(h, s_d, it.x0, x, it.x1);
-          sd += sum_group<EBD, PROBS>(h, greedy, md, rd.c, rd.invT);
+          sd += sum_group<EBD, PROBS>(h, greedy, rd.mz, rd.c, rd.invT);
+          if constexpr (EBD == 2 && !PROBS) {
+            if (win_d) {
+              const uint32_t m = window_bits_bf16(make_uint4(h.w[0], h.w[1], h.w[2], h.w[3]), thr2_d, x, it.x1);
+              wd_n += __popc(m);
+              if (blk < 4) wd_lo |= m << (8 * blk);
+              else wd_hi |= m << (8 * (blk - 4));
+            }
+          }
         }
       }
+    }
+    if constexpr (EBT == 2) {
+      if (win_t) window_commit_bf16(s_t, rt.kmax, wt_lo, wt_hi, wt_n, it, sm.hist[0][0], sm.wb.bin[warp]);
+    }
+    if constexpr (EBD == 2 && !PROBS) {
+      if (win_d) window_commit_bf16(s_d, rd.kmax, wd_lo, wd_hi, wd_n, it, sm.hist[0][1], sm.wb.bin[warp]);
     }
 
-    // ---------------- combine: warps post partials, every warp reduces all
-    warp_ms(mt, st, rt.c, greedy);
-    warp_ms(md, sd, rd.c, greedy);
+    // ------ exchange 2: the weight sums (and the window histograms with them)
 #pragma unroll
-    for (int o = 16; o; o >>= 1) rmd = fmaxf(rmd, __shfl_xor_sync(0xffffffffu, rmd, o));
-    const bool warp_bad = __any_sync(0xffffffffu, !landed);
-    if (lane == 0)
-      sm.part[warp] = {make_float4(mt, st, rmd, warp_bad ? 1.0f : 0.0f), make_float4(md, sd, 0.0f, 0.0f)};
-    cluster.sync();  // partials visible cluster-wide
-    {
-      const int n = C * kWarps;
-      float4 A[4], D[4];
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {  // all remote loads in flight together
-        const int q = lane + 32 * r;
-        if (q < n) {
-          const StatPart* o = &cluster.map_shared_rank(&sm, q / kWarps)->part[q % kWarps];
-          A[r] = o->a, D[r] = o->d;
-        } else {
-          A[r] = make_float4(-INFINITY, 0.0f, PROBS ? 0.0f : -INFINITY, 0.0f);
-          D[r] = make_float4(-INFINITY, 0.0f, 0.0f, 0.0f);
-        }
-      }
-      float Mt = -INFINITY, Md = -INFINITY, Rm = PROBS ? 0.0f : -INFINITY;
-      bool bad = false;
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        Mt = fmaxf(Mt, A[r].x), Md = fmaxf(Md, D[r].x), Rm = fmaxf(Rm, A[r].z);
-        bad |= A[r].w != 0.0f;
-      }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        Mt = fmaxf(Mt, __shfl_xor_sync(0xffffffffu, Mt, o));
-        Md = fmaxf(Md, __shfl_xor_sync(0xffffffffu, Md, o));
-        Rm = fmaxf(Rm, __shfl_xor_sync(0xffffffffu, Rm, o));
-      }
-      float St = 0.0f, Sd = 0.0f;
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        St += rescale(A[r].x, A[r].y, Mt, rt.c, greedy);
-        Sd += rescale(D[r].x, D[r].y, Md, rd.c, greedy);
-      }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        St += __shfl_xor_sync(0xffffffffu, St, o);
-        Sd += __shfl_xor_sync(0xffffffffu, Sd, o);
-      }
-      bad = __any_sync(0xffffffffu, bad);
-      rt.m = rt.mz = Mt, rt.S = St;
-      rd.m = Rm;   // raw maximum (logit or probability): defines the top-p keys
-      rd.mz = Md;  // maximum in the weight domain (== raw max except probabilities, T > 0)
-      rd.S = Sd;
-      if (bad) rt.S = __int_as_float(0x7FC00000);  // a slice never landed: the row is invalid
+    for (int o = 16; o; o >>= 1) {
+      st += __shfl_xor_sync(0xffffffffu, st, o);
+      sd += __shfl_xor_sync(0xffffffffu, sd, o);
     }
-    rt.kmax = vkey<EBT>(rt.m);
-    rd.kmax = vkey<EBD>(rd.m);
+    if (lane == 0) sm.spart[warp] = make_float2(st, sd);
+    __syncthreads();
+    if (warp == 0) {  // the CTA's sums, warps in order
+      float2 v = lane < kWarps ? sm.spart[lane] : make_float2(0.0f, 0.0f);
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+        v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+      }
+      if (lane == 0) sm.cspart = v;
+    }
+    cluster.sync();
+    {
+      float2 v = lane < C ? cluster.map_shared_rank(&sm, lane)->cspart : make_float2(0.0f, 0.0f);
+      float a = v.x, c2 = v.y;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        a += __shfl_xor_sync(0xffffffffu, a, o);
+        c2 += __shfl_xor_sync(0xffffffffu, c2, o);
+      }
+      rt.S = a, rd.S = c2;
+      if (slice_bad) rt.S = __int_as_float(0x7FC00000);  // a slice never landed: the row is invalid
+    }
     rt.Z = rt.S, rd.Z = rd.S;
     rt.invZ = 1.0f / rt.Z, rd.invZ = 1.0f / rd.Z;
     rt.vstar = -INFINITY;
@@ -1413,7 +1527,7 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
 
     // ---------------------------------------------------------------- top-p
     if (!row_bad && !greedy && top_p < 1.0f)
-      top_p_rows<EBT, EBD, PROBS>(cluster, sm, s_t, s_d, it, has_d, top_p, rt, rd);
+      top_p_rows<EBT, EBD, PROBS>(cluster, sm, s_t, s_d, it, has_d, top_p, rt, rd, win_t, win_d);
 
     // ---------------------------------------------------------- accept test
     // Every CTA evaluates the test identically from the same values.
