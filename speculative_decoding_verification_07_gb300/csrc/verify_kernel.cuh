@@ -305,7 +305,7 @@ struct alignas(16) StatPart {
 };
 
 struct Smem {
-  unsigned long long bar[2][kMaxBlk];  // TMA completion: [target / draft][block]
+  unsigned long long bar[2];  // TMA completion: target / draft slice
   Ticket tk[2];              // [iteration parity] the row to work on (rank 0 only)
   int decide[4];             // resolver decision (rank 0 only)
   StatPart part[kWarps];     // per-warp maxima partials
@@ -409,6 +409,11 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
           smem_addr(dst)),
       "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
+}
+
+// Pull [src, src + bytes) into L2 without waiting (bytes a multiple of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // try_wait with a suspend-time hint: the warp is parked until the phase
@@ -1293,10 +1298,10 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
   const uint32_t k0 = P.seed_lo, k1 = P.seed_hi;
   const bool lead = rank == 0 && tid == 0;                // publishes states and outputs
   const bool ctl = rank == 0 && warp == kWarps - 1;       // takes tickets, resolves
-  uint32_t phase_t = 0u, phase_d = 0u;  // mbarrier parity per block (bit blk)
+  uint32_t phase_t = 0u, phase_d = 0u;  // mbarrier parities
 
   if (tid == 0) {
-    for (int j = 0; j < kMaxBlk; ++j) mbar_init(&sm.bar[0][j]), mbar_init(&sm.bar[1][j]);
+    mbar_init(&sm.bar[0]), mbar_init(&sm.bar[1]);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (ctl) {
@@ -1327,15 +1332,16 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
       const char* trow = P.target + row_t * P.t_ld * EBT;
       const char* drow = P.draft + row_d * P.d_ld * EBD;
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // prior reads before new writes
-      for (int blk = 0; blk < it.nblk; ++blk) {
-        const int e0 = it.x0 + blk * kBlk, e1 = min(it.x1, e0 + kBlk);
-        const uint32_t bt = (uint32_t)(((e1 - e0) * EBT + 15) & ~15);
-        mbar_expect_tx(&sm.bar[0][blk], bt);
-        bulk_g2s(s_t + (size_t)blk * kBlk * EBT, trow + (size_t)e0 * EBT, bt, &sm.bar[0][blk]);
+      // one copy per row: the TMA unit's cost grows with the number of
+      // copies far more than with their size
+      if (it.nblk > 0) {
+        const uint32_t bt = (uint32_t)(((it.x1 - it.x0) * EBT + 15) & ~15);
+        mbar_expect_tx(&sm.bar[0], bt);
+        bulk_g2s(s_t, trow + (size_t)it.x0 * EBT, bt, &sm.bar[0]);
         if (has_d) {
-          const uint32_t bd = (uint32_t)(((e1 - e0) * EBD + 15) & ~15);
-          mbar_expect_tx(&sm.bar[1][blk], bd);
-          bulk_g2s(s_d + (size_t)blk * kBlk * EBD, drow + (size_t)e0 * EBD, bd, &sm.bar[1][blk]);
+          const uint32_t bd = (uint32_t)(((it.x1 - it.x0) * EBD + 15) & ~15);
+          mbar_expect_tx(&sm.bar[1], bd);
+          bulk_g2s(s_d, drow + (size_t)it.x0 * EBD, bd, &sm.bar[1]);
         }
       }
     }
@@ -1359,16 +1365,20 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
     rd.c = PROBS ? 1.0f : rt.c;
     rt.Dstar = rd.Dstar = kNoFilter;
 
-    // ------------------------------- sweep 1: raw maxima as the blocks land
+    // --------------------------------------------- sweep 1: raw maxima
     uint32_t mt2 = 0xFF80FF80u, md2 = 0xFF80FF80u;
     float rmt = -INFINITY, rmd = PROBS ? 0.0f : -INFINITY;
     bool landed = true;
-#pragma unroll 1
-    for (int blk = 0; blk < it.nblk; ++blk) {
-      landed &= mbar_wait(&sm.bar[0][blk], (phase_t >> blk) & 1u, P.err);
-      if (has_d) landed &= mbar_wait(&sm.bar[1][blk], (phase_d >> blk) & 1u, P.err);
+    if (it.nblk > 0) {
+      landed &= mbar_wait(&sm.bar[0], phase_t, P.err);
+      if (has_d) landed &= mbar_wait(&sm.bar[1], phase_d, P.err);
+      phase_t ^= 1u;
+      if (has_d) phase_d ^= 1u;
+    }
+#pragma unroll
+    for (int blk = 0; blk < kMaxBlk; ++blk) {
       const int x = it.x(blk);
-      if (x < it.x1) {
+      if (blk < it.nblk && x < it.x1) {
         Grp<EBT> g;
         lds_group<EBT, false>(g, s_t, it.x0, x, it.x1);
         max_group<EBT>(g, mt2, rmt);
@@ -1379,8 +1389,6 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
         }
       }
     }
-    phase_t ^= (1u << it.nblk) - 1u;
-    if (has_d) phase_d ^= (1u << it.nblk) - 1u;
     rmt = max_value<EBT>(mt2, rmt);
     rmd = max_value<EBD>(md2, rmd);
     // this thread's maxima in the weight domain
@@ -1425,6 +1433,23 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
       rd.mz = c.d.x;  // maximum in the weight domain (== raw max except probabilities, T > 0)
       St_lb = c.a.y, Sd_lb = c.d.y;
       slice_bad = c.a.w != 0.0f;
+    }
+    // This row's slices have landed.  Pull this CTA's slices of the next
+    // row's ticket (final here until the end-of-row re-check, which runs after
+    // exchange 2) toward L2, so that its loads hit L2 when that row starts.
+    if (tid == 0) {
+      const Ticket nt = cluster.map_shared_rank(&sm, 0)->tk[parity ^ 1];
+      if (nt.kind == kWork && nt.t >= 0 && nt.t < P.n_tickets) {
+        const int ni = nt.t / P.B, nb = nt.t - ni * P.B;
+        const char* trow = P.target + ((size_t)nb * (P.kmax + 1) + ni) * P.t_ld * EBT;
+        const char* drow = P.draft + ((size_t)nb * P.kmax + ni) * P.d_ld * EBD;
+        for (int blk = 0; blk < it.nblk; ++blk) {
+          const int e0 = it.x0 + blk * kBlk, e1 = min(it.x1, e0 + kBlk);
+          bulk_prefetch_l2(trow + (size_t)e0 * EBT, (uint32_t)(((e1 - e0) * EBT + 15) & ~15));
+          if (ni < nt.kb)
+            bulk_prefetch_l2(drow + (size_t)e0 * EBD, (uint32_t)(((e1 - e0) * EBD + 15) & ~15));
+        }
+      }
     }
     rt.kmax = vkey<EBT>(rt.m);
     rd.kmax = vkey<EBD>(rd.m);
