@@ -1345,12 +1345,6 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
         }
       }
     }
-    // the next ticket, while this row's loads are in flight
-    if (ctl) {
-      int nt = 0;
-      if (lane == 0) nt = (int)atomicAdd(P.hdr + kHdrTicket, 1u);
-      settle_ticket<EBT, EBD>(P, sm, nt, parity ^ 1, tag);
-    }
 
     const float T = tk.T, top_p = tk.top_p;
     const int y = tk.y, pos = tk.pos;
@@ -1433,23 +1427,6 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
       rd.mz = c.d.x;  // maximum in the weight domain (== raw max except probabilities, T > 0)
       St_lb = c.a.y, Sd_lb = c.d.y;
       slice_bad = c.a.w != 0.0f;
-    }
-    // This row's slices have landed.  Pull this CTA's slices of the next
-    // row's ticket (final here until the end-of-row re-check, which runs after
-    // exchange 2) toward L2, so that its loads hit L2 when that row starts.
-    if (tid == 0) {
-      const Ticket nt = cluster.map_shared_rank(&sm, 0)->tk[parity ^ 1];
-      if (nt.kind == kWork && nt.t >= 0 && nt.t < P.n_tickets) {
-        const int ni = nt.t / P.B, nb = nt.t - ni * P.B;
-        const char* trow = P.target + ((size_t)nb * (P.kmax + 1) + ni) * P.t_ld * EBT;
-        const char* drow = P.draft + ((size_t)nb * P.kmax + ni) * P.d_ld * EBD;
-        for (int blk = 0; blk < it.nblk; ++blk) {
-          const int e0 = it.x0 + blk * kBlk, e1 = min(it.x1, e0 + kBlk);
-          bulk_prefetch_l2(trow + (size_t)e0 * EBT, (uint32_t)(((e1 - e0) * EBT + 15) & ~15));
-          if (ni < nt.kb)
-            bulk_prefetch_l2(drow + (size_t)e0 * EBD, (uint32_t)(((e1 - e0) * EBD + 15) & ~15));
-        }
-      }
     }
     rt.kmax = vkey<EBT>(rt.m);
     rd.kmax = vkey<EBD>(rd.m);
@@ -1549,6 +1526,14 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
     const bool bad_d = has_d && (!(rd.S >= 1.0f && rd.S <= FLT_MAX) || !(rd.m <= FLT_MAX) ||
                                  (PROBS ? !(rd.m > 0.0f) : rd.m == -INFINITY));
     const bool row_bad = bad_t || bad_d || !params_ok || !y_ok;
+
+    // The next ticket: taken by the control warp while warps 0 and 1 resolve
+    // the top-p boundary (the CTA's other warps wait for them anyway).
+    if (ctl) {
+      int nt = 0;
+      if (lane == 0) nt = (int)atomicAdd(P.hdr + kHdrTicket, 1u);
+      settle_ticket<EBT, EBD>(P, sm, nt, parity ^ 1, tag);
+    }
 
     // ---------------------------------------------------------------- top-p
     if (!row_bad && !greedy && top_p < 1.0f)
