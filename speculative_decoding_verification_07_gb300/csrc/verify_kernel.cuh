@@ -1349,6 +1349,9 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
     const float T = tk.T, top_p = tk.top_p;
     const int y = tk.y, pos = tk.pos;
     const uint32_t rid = tk.rid;
+    // the accept uniform depends only on (seed, position, request): draw it
+    // while the slices load
+    const float u_row = uniform_from_bits(philox4x32_10(make_uint4(0u, (uint32_t)pos, rid, 1u), k0, k1).x);
     const bool params_ok = (T >= 0.0f) && (T <= FLT_MAX) && (top_p > 0.0f) && (top_p <= 1.0f);
     const bool y_ok = !has_d || (y >= 0 && y < P.V);
     const bool greedy = T == 0.0f;
@@ -1549,8 +1552,7 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
     } else if (has_d) {
       p_y = prob<EBT, false>(tk.vt, rt);
       q_y = prob<EBD, PROBS>(tk.vd, rd);
-      const uint4 r = philox4x32_10(make_uint4(0u, (uint32_t)pos, rid, 1u), k0, k1);
-      u = uniform_from_bits(r.x);
+      u = u_row;
       qzero = q_y == 0.0f;
       state = (u * q_y < p_y) ? SV_ROW_ACCEPTED : SV_ROW_REJECTED;
     } else {
@@ -1576,6 +1578,7 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
       write_probs<EBD, PROBS>(P.probs_q + row_d * (size_t)P.V, s_d, it, rd);
 
     // --------------------------------------------- resolve: is this row the one?
+    bool ended = false;  // a barrier after the re-check has published the next ticket
     if (state != SV_ROW_ACCEPTED) {
       if (ctl) {
         bool qz = false;
@@ -1592,8 +1595,12 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
           sm.decide[0] = resolver;
           sm.decide[1] = (int)((qzero || qz) ? SV_ST_Q_ZERO : 0u);
         }
+        // the next row may have become skippable meanwhile; the barrier
+        // below publishes both the decision and the next ticket
+        recheck_ticket<EBT, EBD>(P, sm, parity ^ 1, tag);
       }
       cluster.sync();
+      ended = true;
       const int* dc = cluster.map_shared_rank(&sm.decide[0], 0);
       const int resolver = dc[0];
       const uint32_t st_bits = (uint32_t)dc[1];
@@ -1624,10 +1631,12 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
       }
     }
 
-    // the next row may have become skippable meanwhile; the end-of-row
-    // barrier then publishes its ticket
-    if (ctl) recheck_ticket<EBT, EBD>(P, sm, parity ^ 1, tag);
-    cluster.sync();
+    if (!ended) {
+      // the next row may have become skippable meanwhile; the end-of-row
+      // barrier then publishes its ticket
+      if (ctl) recheck_ticket<EBT, EBD>(P, sm, parity ^ 1, tag);
+      cluster.sync();
+    }
   }
 
   // all peers must be done reading rank 0's shared memory before it exits
