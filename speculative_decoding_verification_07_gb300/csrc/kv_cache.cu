@@ -24,6 +24,13 @@ namespace sv {
 
 constexpr int kKvThreads = 1024;
 
+// Threads of the one-block kernels: one per item up to 1024, whole warps.
+// Fewer idle warps make every block barrier and scan cheaper.
+static int kv_threads(int n) {
+  const int t = ((n > 0 ? n : 1) + 31) / 32 * 32;
+  return t < kKvThreads ? t : kKvThreads;
+}
+
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // Exclusive block-wide scan of one int per thread; returns the exclusive
@@ -398,7 +405,7 @@ extern "C" sv_status bfl_reserve(sv_handle* h, const bfl_state* st, int32_t B,
   if (!h || bad_state(st) || B < 0 || max_blocks < 1) return SV_ERR_INVALID;
   if (B == 0) return SV_OK;
   if (!seq_len || !table) return SV_ERR_INVALID;
-  bfl_reserve_kernel<<<1, kKvThreads, 0, (cudaStream_t)stream>>>(*st, B, seq_len, k, table,
+  bfl_reserve_kernel<<<1, kv_threads(B), 0, (cudaStream_t)stream>>>(*st, B, seq_len, k, table,
                                                                  max_blocks, h->d_err);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
@@ -410,7 +417,7 @@ extern "C" sv_status bfl_fork_prefix(sv_handle* h, const bfl_state* st, int32_t 
   if (!h || bad_state(st) || n_pairs < 0 || n_rows < 0 || max_blocks < 1) return SV_ERR_INVALID;
   if (n_pairs == 0) return SV_OK;
   if (!src || !dst || !n_blocks || !table) return SV_ERR_INVALID;
-  bfl_fork_kernel<<<1, kKvThreads, 0, (cudaStream_t)stream>>>(*st, n_pairs, src, dst, n_blocks,
+  bfl_fork_kernel<<<1, kv_threads(n_pairs), 0, (cudaStream_t)stream>>>(*st, n_pairs, src, dst, n_blocks,
                                                               table, n_rows, max_blocks, h->d_err);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
@@ -422,7 +429,7 @@ extern "C" sv_status bfl_release(sv_handle* h, const bfl_state* st, int32_t n,
   if (!h || bad_state(st) || n < 0 || n_rows < 0 || max_blocks < 1) return SV_ERR_INVALID;
   if (n == 0) return SV_OK;
   if (!req_ids || !seq_len || !table) return SV_ERR_INVALID;
-  bfl_release_kernel<<<1, kKvThreads, 0, (cudaStream_t)stream>>>(*st, n, req_ids, seq_len, table,
+  bfl_release_kernel<<<1, kv_threads(n), 0, (cudaStream_t)stream>>>(*st, n, req_ids, seq_len, table,
                                                                  n_rows, max_blocks, n_freed,
                                                                  h->d_err);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
@@ -435,7 +442,7 @@ extern "C" sv_status kv_commit_rollback(sv_handle* h, const bfl_state* st, int32
   if (!h || bad_state(st) || B < 0 || max_blocks < 1) return SV_ERR_INVALID;
   if (B == 0) return SV_OK;
   if (!accepted || !seq_len || !table) return SV_ERR_INVALID;
-  kv_commit_kernel<<<1, kKvThreads, 0, (cudaStream_t)stream>>>(*st, B, k, accepted, seq_len, table,
+  kv_commit_kernel<<<1, kv_threads(B), 0, (cudaStream_t)stream>>>(*st, B, k, accepted, seq_len, table,
                                                                max_blocks, n_freed, h->d_err);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
