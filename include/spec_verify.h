@@ -262,6 +262,25 @@ sv_status kv_commit_rollback(sv_handle* handle, const bfl_state* st, int32_t B, 
                              const int32_t* accepted, int32_t* seq_len, int32_t* block_table,
                              int32_t max_blocks, int32_t* n_freed, sv_stream_t stream);
 
+/* Draft-cache realignment ([SD] section 4, "update cache state": the draft
+ * cache is reconciled with the corrected token; [CV] paragraph 4: the draft
+ * follows its own processed-state convention and is never filled from target
+ * K/V).  The draft's own pool and table: draft_len_b (in: D_b, the positions
+ * the draft processed, however far its proposal loop went) becomes
+ * min(D_b, S_b + 1 + a_b), or min(D_b, S_b) when a_b = -1, i.e. only
+ * committed tokens stay; a shorter draft catches up on them next round.
+ * Blocks j in [ceil(new/BS), ceil(D_b/BS)) leave the table; each loses a
+ * reference and is pushed on the free stack when that reaches 0, in
+ * (request, j) order.  seq_len [B]: the TARGET length before the pass (S_b;
+ * call this before kv_commit_rollback updates it), accepted [B], draft_len [B]
+ * in/out, draft_table [B][max_blocks] in/out, n_freed optional [B].
+ * A table row not covering its length or accepted < -1: SV_ERR_STATE,
+ * nothing changes. */
+sv_status kv_commit_draft(sv_handle* handle, const bfl_state* st, int32_t B,
+                          const int32_t* seq_len, const int32_t* accepted, int32_t* draft_len,
+                          int32_t* draft_table, int32_t max_blocks, int32_t* n_freed,
+                          sv_stream_t stream);
+
 /* Contiguous cache ([KV]: rewind the write pointer): write_ptr_b (in: S_b)
  * becomes S_b + 1 + a_b, or stays S_b when a_b = -1.  [B] each. */
 sv_status kv_rollback_contig(sv_handle* handle, int32_t B, const int32_t* accepted,

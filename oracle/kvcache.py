@@ -36,6 +36,8 @@ Readings (listed in DESIGN.md):
     free stack starts as [n-1, ..., 1, 0] so that blocks pop as 0, 1, 2, ...
   * a fork shares whole blocks only; appending into a partially filled block
     whose refcount is above 1 is refused (copy-on-write is not provided).
+  * a draft model's cache keeps min(D_b, committed length) of its own
+    processed positions (see commit_draft).
 """
 
 from __future__ import annotations
@@ -135,6 +137,37 @@ class BlockPool:
                 block_table[b, j] = -1
                 n_freed[b] += self._drop(blk)
             seq_len[b] = new
+        return n_freed
+
+    def commit_draft(self, seq_len, accepted, draft_len, block_table):
+        """Realign a draft model's cache with the committed history ([SD]
+        section 4, "update cache state": the draft cache is reconciled with the
+        corrected token; [CV] paragraph 4: the draft follows its own processed-
+        state convention and is never filled from target K/V).
+
+        Reading: the draft's cache holds draft_len[b] = D_b processed positions
+        (however far its own proposal loop went).  After the pass the committed
+        history has S_b + 1 + a_b processed tokens (S_b when a_b = -1), so the
+        draft keeps min(D_b, that) positions; a shorter draft catches up on the
+        committed tokens next round.  Blocks j in [ceil(keep/BS), ceil(D_b/BS))
+        are dropped in (request, j) order.  seq_len is the TARGET length before
+        the pass (S_b).  Returns n_freed [B].
+        """
+        BS = self.block_size
+        B = len(draft_len)
+        n_freed = np.zeros(B, np.int32)
+        for b in range(B):
+            S, a, D = int(seq_len[b]), int(accepted[b]), int(draft_len[b])
+            if S < 0 or D < 0 or a < -1 or ceil_div(D, BS) > block_table.shape[1]:
+                raise CacheError(f"request {b}: bad sizes")
+            if (block_table[b, :ceil_div(D, BS)] < 0).any():
+                raise CacheError(f"request {b}: draft table does not cover its length")
+            keep = min(D, S if a < 0 else S + 1 + a)
+            for j in range(ceil_div(keep, BS), ceil_div(D, BS)):
+                blk = int(block_table[b, j])
+                block_table[b, j] = -1
+                n_freed[b] += self._drop(blk)
+            draft_len[b] = keep
         return n_freed
 
     def fork_prefix(self, src, dst, n_blocks, block_table) -> None:

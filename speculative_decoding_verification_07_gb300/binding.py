@@ -7,7 +7,7 @@ and there is no fallback: if the library is missing the import fails loudly.
 
 Functions carry the C names: sv_create, sv_destroy, sv_workspace_size,
 spec_verify, bfl_init, bfl_reserve, bfl_fork_prefix, bfl_release,
-kv_commit_rollback, kv_rollback_contig, sv_get_error.  ``Verifier`` and
+kv_commit_rollback, kv_commit_draft, kv_rollback_contig, sv_get_error.  ``Verifier`` and
 ``BlockPool`` are thin owners of a handle / workspace and of the pool arrays.
 """
 
@@ -35,7 +35,8 @@ ROW_NONE, ROW_ACCEPTED, ROW_REJECTED, ROW_SKIPPED, ROW_INVALID, ROW_BONUS = rang
 
 EXPORTS = ("sv_verify_args_size", "sv_create", "sv_destroy", "sv_workspace_size",
            "spec_verify", "bfl_init", "bfl_reserve", "bfl_fork_prefix", "bfl_release",
-           "kv_commit_rollback", "kv_rollback_contig", "sv_get_error", "spec_verify_static")
+           "kv_commit_rollback", "kv_rollback_contig", "sv_get_error", "spec_verify_static",
+           "kv_commit_draft")
 
 
 class SvVerifyArgs(ctypes.Structure):
@@ -84,6 +85,8 @@ def load_library(path: str = LIB_PATH):
                                     c_void_p, c_void_p, c_int32, c_int32, c_void_p]
     lib.bfl_release.argtypes = [c_void_p, POINTER(BflState), c_int32, c_void_p, c_void_p,
                                 c_void_p, c_int32, c_int32, c_void_p, c_void_p]
+    lib.kv_commit_draft.argtypes = [c_void_p, POINTER(BflState), c_int32, c_void_p, c_void_p,
+                                    c_void_p, c_void_p, c_int32, c_void_p, c_void_p]
     lib.kv_commit_rollback.argtypes = [c_void_p, POINTER(BflState), c_int32, c_void_p, c_void_p,
                                        c_void_p, c_void_p, c_int32, c_void_p, c_void_p]
     lib.kv_rollback_contig.argtypes = [c_void_p, c_int32, c_void_p, c_void_p, c_void_p]
@@ -229,6 +232,13 @@ def bfl_release(handle, pool, req_ids, seq_len, block_table, n_freed=None, strea
         _stream(stream)))
 
 
+def kv_commit_draft(handle, pool, seq_len, accepted, draft_len, draft_table, n_freed=None,
+                    stream=None) -> None:
+    _check("kv_commit_draft", load_library().kv_commit_draft(
+        handle, ctypes.byref(_state(pool)), draft_len.numel(), _ptr(seq_len), _ptr(accepted),
+        _ptr(draft_len), _ptr(draft_table), draft_table.shape[1], _ptr(n_freed), _stream(stream)))
+
+
 def kv_commit_rollback(handle, pool, k, accepted, seq_len, block_table, n_freed=None,
                        stream=None) -> None:
     _check("kv_commit_rollback", load_library().kv_commit_rollback(
@@ -266,6 +276,9 @@ class BlockPool:
 
     def commit_rollback(self, k, accepted, seq_len, block_table, n_freed=None, stream=None):
         kv_commit_rollback(self.handle, self, k, accepted, seq_len, block_table, n_freed, stream)
+
+    def commit_draft(self, seq_len, accepted, draft_len, draft_table, n_freed=None, stream=None):
+        kv_commit_draft(self.handle, self, seq_len, accepted, draft_len, draft_table, n_freed, stream)
 
     def fork_prefix(self, src, dst, n_blocks, block_table, stream=None):
         bfl_fork_prefix(self.handle, self, src, dst, n_blocks, block_table, stream)

@@ -302,6 +302,50 @@ __global__ void __launch_bounds__(kKvThreads) kv_commit_kernel(bfl_state st, int
 }
 
 // ---------------------------------------------------------------------------
+// Draft-cache realignment: the draft keeps min(D_b, committed length) of its
+// own processed positions and drops the blocks past them.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kKvThreads) kv_commit_draft_kernel(bfl_state st, int B,
+                                                                     const int32_t* seq_len,
+                                                                     const int32_t* accepted,
+                                                                     int32_t* draft_len,
+                                                                     int32_t* table, int max_blocks,
+                                                                     int32_t* n_freed, int* err) {
+  const int BS = st.block_size, nb = st.num_blocks;
+  __shared__ int s_bad;
+  if (threadIdx.x == 0) s_bad = 0;
+  __syncthreads();
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    const int S = seq_len[b], a = accepted[b], D = draft_len[b];
+    bool bad = S < 0 || D < 0 || a < -1 || ceil_div(D, BS) > max_blocks;
+    const int32_t* row = table + (size_t)b * max_blocks;
+    for (int j = 0; !bad && j < ceil_div(D, BS); ++j) bad = row[j] < 0 || row[j] >= nb;
+    if (bad) atomicExch(&s_bad, 1);
+  }
+  __syncthreads();
+  if (s_bad) {
+    if (threadIdx.x == 0) report(err, SV_ERR_STATE);
+    return;
+  }
+  auto keep_of = [&](int b) {
+    const int S = seq_len[b], a = accepted[b], D = draft_len[b];
+    const int c = a < 0 ? S : S + 1 + a;
+    return c < D ? c : D;
+  };
+  auto range = [&](int b) {
+    return DropRange{table + (size_t)b * max_blocks, ceil_div(keep_of(b), BS),
+                     ceil_div(draft_len[b], BS)};
+  };
+  auto done = [&](int b, int pushes) {
+    if (n_freed) n_freed[b] = pushes;
+  };
+  const bool ok = drop_blocks(st, B, max_blocks, range, done, err);
+  __syncthreads();  // range() reads draft_len: update it only after every drop
+  if (!ok) return;
+  for (int b = threadIdx.x; b < B; b += blockDim.x) draft_len[b] = keep_of(b);
+}
+
+// ---------------------------------------------------------------------------
 // Release finished requests: drop every block they hold.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kKvThreads) bfl_release_kernel(bfl_state st, int n,
@@ -444,6 +488,18 @@ extern "C" sv_status kv_commit_rollback(sv_handle* h, const bfl_state* st, int32
   if (!accepted || !seq_len || !table) return SV_ERR_INVALID;
   kv_commit_kernel<<<1, kv_threads(B), 0, (cudaStream_t)stream>>>(*st, B, k, accepted, seq_len, table,
                                                                max_blocks, n_freed, h->d_err);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+extern "C" sv_status kv_commit_draft(sv_handle* h, const bfl_state* st, int32_t B,
+                                     const int32_t* seq_len, const int32_t* accepted,
+                                     int32_t* draft_len, int32_t* draft_table, int32_t max_blocks,
+                                     int32_t* n_freed, sv_stream_t stream) {
+  if (!h || bad_state(st) || B < 0 || max_blocks < 1) return SV_ERR_INVALID;
+  if (B == 0) return SV_OK;
+  if (!seq_len || !accepted || !draft_len || !draft_table) return SV_ERR_INVALID;
+  kv_commit_draft_kernel<<<1, kv_threads(B), 0, (cudaStream_t)stream>>>(
+      *st, B, seq_len, accepted, draft_len, draft_table, max_blocks, n_freed, h->d_err);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 

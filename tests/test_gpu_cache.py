@@ -233,3 +233,44 @@ def test_verify_then_commit_matches_no_speculation_recompute(ver):
             model.next_distribution(recompute, hist[b][-1], len(hist[b]) - 1))
         assert (tbl[b] >= 0).sum() == -(-int(seq_h[b]) // BS)
     assert (seq_h[4] % BS) == 0 and (seq_h[5] % BS) == 1   # block-edge scenarios
+
+
+def test_draft_cache_realignment_bit_exact(ver):
+    """Target and draft pools side by side: each round the draft catches up and
+    proposes (its cache covers [0, S + k)), then kv_commit_draft realigns it
+    with the committed history; GPU and reference agree bit for bit."""
+    rng = np.random.default_rng(21)
+    B, BS, mb = 48, 16, 700
+    tgt = Pair(ver, B * mb, BS, B, mb)
+    drf = Pair(ver, B * mb, BS, B, mb)
+    S0 = rng.integers(1, 4000, B)
+    tgt.prefill(S0)
+    drf.prefill(S0)                                     # the draft saw the same prefix
+    for step in range(20):
+        k = rng.integers(1, 9, B)
+        tgt.reserve(k)
+        S = tgt.rs.copy()
+        D = drf.rs.copy()
+        extra = S + k - D                               # the draft processes D .. S + k - 1
+        drf.reserve(extra - 1)
+        drf.gs.copy_(drf.t(S + k))
+        drf.rs[:] = S + k
+        acc = np.array([rng.integers(-1, kb + 1) for kb in k])
+        nf = torch.full((B,), -7, dtype=torch.int32, device=DEV)
+        drf.g.commit_draft(tgt.gs, drf.t(acc), drf.gs, drf.gt, nf)
+        want = drf.r.commit_draft(tgt.rs, acc, drf.rs, drf.rt)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(nf.cpu().numpy(), want)
+        drf.check()
+        tgt.commit(k, acc)
+        tgt.check()
+        assert (drf.rs <= tgt.rs).all()
+    # a bad accepted value changes nothing
+    snap = (drf.gt.clone(), drf.gs.clone(), drf.g.refcount.clone(), drf.g.free_top.clone())
+    bad = np.zeros(B, np.int64)
+    bad[3] = -2
+    drf.g.commit_draft(tgt.gs, drf.t(bad), drf.gs, drf.gt)
+    torch.cuda.synchronize()
+    assert ver.error() == binding.SV_ERR_STATE
+    for a, b in zip(snap, (drf.gt, drf.gs, drf.g.refcount, drf.g.free_top)):
+        assert torch.equal(a, b)

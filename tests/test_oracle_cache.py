@@ -215,3 +215,77 @@ def test_contiguous_write_pointer_rollback():
             history = history + drafts[:a] + [int(rng.integers(0, 1000))]
         assert wp[0] == len(history) - 1
         np.testing.assert_array_equal(buf[:wp[0]], m.kv(history[:-1], list(range(wp[0]))))
+
+
+# --------------------------------------------------------------------------- #
+# draft-cache realignment
+# --------------------------------------------------------------------------- #
+def test_draft_commit_hand_scenario():
+    """BS = 4, target length S = 5, k = 4 proposals; the draft processed the
+    pending token and y_0..y_2 while proposing (D = S + k = 9, blocks 0-2)."""
+    for a, keep, freed in [(1, 7, 1), (4, 9, 0), (-1, 5, 1), (3, 9, 0), (0, 6, 1)]:
+        pool = BlockPool(6, 4)
+        table = np.full((1, 4), -1, np.int32)
+        pool.reserve(np.array([0]), [8], table)          # covers [0, 9)
+        np.testing.assert_array_equal(table[0], [0, 1, 2, -1])
+        D = np.array([9], np.int32)
+        n = pool.commit_draft(np.array([5]), np.array([a]), D, table)
+        assert D[0] == keep and n[0] == freed, (a, D, n)
+        assert (table[0] >= 0).sum() == ceil_div(keep, 4)
+        _check_invariants(pool, table)
+    # a draft that processed everything (D = S + k + 1 = 10) keeps S + 1 + a
+    pool = BlockPool(6, 4)
+    table = np.full((1, 4), -1, np.int32)
+    pool.reserve(np.array([0]), [9], table)
+    D = np.array([10], np.int32)
+    pool.commit_draft(np.array([5]), np.array([4]), D, table)
+    assert D[0] == 10 and (table[0] >= 0).sum() == 3
+    with pytest.raises(CacheError):                      # accepted below -1
+        pool.copy().commit_draft(np.array([5]), np.array([-2]), D.copy(), table.copy())
+    with pytest.raises(CacheError):                      # table shorter than the length
+        pool.copy().commit_draft(np.array([5]), np.array([1]), np.array([13]), table.copy())
+
+
+@pytest.mark.parametrize("reject_at", [0, 2, 4, None])
+def test_draft_cache_matches_recompute_after_realignment(reject_at):
+    """A toy draft proposes k tokens autoregressively into its own paged cache;
+    after the draft commit its valid cache equals a recompute of the committed
+    history, and after catching up on the committed tokens it has not processed
+    its next-step distribution equals the recompute's."""
+    BS, k = 8, 5
+    draft = ToyAttention(seed=11)
+    rng = np.random.default_rng(12)
+    pool = BlockPool(64, BS)
+    payload = PagedPayload(draft, 64, BS)
+    table = np.full((1, 16), -1, np.int32)
+    S = 21
+    history = list(rng.integers(0, 1000, S + 1))          # S processed + 1 pending
+    D = np.array([0], np.int32)
+    pool.reserve(D, [S - 1], table)
+    payload.write(table[0], history[:S], list(range(S)))
+    D[0] = S
+    for rnd in range(3):
+        S0 = len(history) - 1                              # target length before the pass
+        need = S0 + k - int(D[0])                           # the draft catches up, then proposes
+        pool.reserve(D, [need - 1], table)
+        todo = history[int(D[0]):] + []                    # committed tokens not yet processed
+        drafts = list(rng.integers(0, 1000, k))
+        seq_in = todo + drafts[:-1]                        # the draft processes up to y_{k-2}
+        payload.write(table[0], seq_in, list(range(int(D[0]), int(D[0]) + len(seq_in))))
+        D[0] = S0 + k
+        a = (reject_at if reject_at is not None else k) if rnd == 0 else int(rng.integers(-1, k + 1))
+        corr = int(rng.integers(0, 1000))
+        pool.commit_draft(np.array([S0]), np.array([a]), D, table)
+        history = history + (drafts[:a] + [corr] if a >= 0 else [])
+        committed = S0 if a < 0 else S0 + 1 + a
+        assert D[0] == min(S0 + k, committed)
+        valid = payload.gather(table[0], int(D[0]))
+        recompute = draft.kv(history[:int(D[0])], list(range(int(D[0]))))
+        np.testing.assert_array_equal(valid, recompute)
+        # catch up on committed-but-unprocessed tokens, then compare the next step
+        n_proc = len(history) - 1
+        cache = np.concatenate([valid, draft.kv(history[int(D[0]):n_proc], list(range(int(D[0]), n_proc)))])
+        got = draft.next_distribution(cache, history[-1], n_proc)
+        want = draft.next_distribution(draft.kv(history[:n_proc], list(range(n_proc))), history[-1], n_proc)
+        np.testing.assert_array_equal(got, want)
+        _check_invariants(pool, table)
