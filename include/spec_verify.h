@@ -153,6 +153,16 @@ typedef struct {
   int32_t* refcount;   /* [num_blocks]; 0 = free                    */
 } bfl_state;
 
+/* K/V payload of a paged cache (used only by the copy entry points):
+ * data [num_blocks][layers][2][heads][block_size][head_dim] (2 = K, V), every
+ * block's payload contiguous; 16-byte aligned, head_dim * elem_bytes a
+ * multiple of 16.  elem_bytes 2 (bf16 / fp16) or 4; values are moved, never
+ * interpreted. */
+typedef struct {
+  void* data;
+  int32_t layers, heads, head_dim, elem_bytes;
+} kv_payload;
+
 /* sizeof(sv_verify_args) as compiled, for bindings to check their layout. */
 size_t sv_verify_args_size(void);
 
@@ -261,6 +271,36 @@ sv_status bfl_release(sv_handle* handle, const bfl_state* st, int32_t n, const i
 sv_status kv_commit_rollback(sv_handle* handle, const bfl_state* st, int32_t B, const int32_t* k,
                              const int32_t* accepted, int32_t* seq_len, int32_t* block_table,
                              int32_t max_blocks, int32_t* n_freed, sv_stream_t stream);
+
+/* Lookahead allocation with copy-on-write ([CV] paragraph 4: copy-on-write
+ * addresses physical sharing while the decoder keeps the token and position
+ * mapping).  As bfl_reserve, but a request whose last held block is partially
+ * filled (r = S_b % BS > 0) and shared (refcount > 1 when the call starts)
+ * first gets a fresh block holding a copy of that block's valid slots [0, r)
+ * (every layer, K/V and head of kv); the table entry points at the copy and
+ * the shared block loses one reference per copy, unchanged for its other
+ * owners.  Pops run in (request, j) order, the copy taking j = have - 1; a
+ * shared block left without references is pushed on the free stack after
+ * every pop, in request order.  cow_scratch [B][3] is caller-owned device
+ * memory the call uses between its two kernels.  All or nothing: an exhausted
+ * pool (SV_ERR_OOM) or an inconsistent table (SV_ERR_STATE) changes nothing. */
+sv_status bfl_reserve_cow(sv_handle* handle, const bfl_state* st, int32_t B, const int32_t* seq_len,
+                          const int32_t* k, int32_t* block_table, int32_t max_blocks,
+                          const kv_payload* kv, int32_t* cow_scratch, sv_stream_t stream);
+
+/* Commit by copy ([KV]: candidate K/V is appended provisionally, only the
+ * accepted part is kept; [RJ] paragraph 1: allocation is not acceptance).
+ * The verify pass wrote the K/V of positions S_b .. S_b + k_b (the pending
+ * token and the drafts) to stage [B][kmax + 1][layers][2][heads][head_dim];
+ * entries i = 0 .. a_b go to their paged slots (block_table[b][p / BS], slot
+ * p % BS, p = S_b + i); a_b = -1 copies nothing and rejected entries are never
+ * written.  seq_len [B]: S_b, the length BEFORE kv_commit_rollback updates it;
+ * accepted [B].  A position without a block in [0, num_blocks): SV_ERR_STATE
+ * in the error word, that entry skipped. */
+sv_status kv_commit_copy(sv_handle* handle, int32_t B, int32_t kmax, const int32_t* accepted,
+                         const int32_t* seq_len, const int32_t* block_table, int32_t max_blocks,
+                         int32_t block_size, int32_t num_blocks, const void* stage,
+                         const kv_payload* kv, sv_stream_t stream);
 
 /* Draft-cache realignment ([SD] section 4, "update cache state": the draft
  * cache is reconciled with the corrected token; [CV] paragraph 4: the draft

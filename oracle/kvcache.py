@@ -34,8 +34,9 @@ Readings (listed in DESIGN.md):
     reaches 0.  A block with at least one valid slot is kept.
   * order: requests ascending, j ascending, for pops and pushes alike; the
     free stack starts as [n-1, ..., 1, 0] so that blocks pop as 0, 1, 2, ...
-  * a fork shares whole blocks only; appending into a partially filled block
-    whose refcount is above 1 is refused (copy-on-write is not provided).
+  * a fork shares whole blocks (a partially filled last block included);
+    reserve refuses to append into a partially filled block whose refcount is
+    above 1, reserve_cow copies it first (copy-on-write).
   * a draft model's cache keeps min(D_b, committed length) of its own
     processed positions (see commit_draft).
 """
@@ -119,6 +120,52 @@ class BlockPool:
             for t in range(need[b]):
                 block_table[b, have + t] = self._pop()
 
+    def reserve_cow(self, seq_len, k, block_table, kv) -> None:
+        """Lookahead allocation with copy-on-write of a shared partial block
+        ([CV] paragraph 4: copy-on-write addresses physical sharing while the
+        decoder keeps the token and position mapping).
+
+        Like reserve, but a request whose last held block is partially filled
+        (r = S_b % BS > 0) and shared (refcount > 1 when the call starts) first
+        gets a fresh block holding a copy of that block's valid slots [0, r)
+        for every layer, K/V and head; the table entry points at the copy and
+        the shared block loses one reference per copy, staying unchanged with
+        its other owners.  Pops run in (request, j) order, the copy taking
+        index j = have - 1; a shared block left without references (all its
+        owners copied) is pushed on the free stack after every pop, in request
+        order.  All or nothing.  kv: payload [num_blocks, L, 2, H, BS, D].
+        """
+        BS = self.block_size
+        B = len(seq_len)
+        need, cow = [], []
+        for b in range(B):
+            S, kb = int(seq_len[b]), int(k[b])
+            have, want = ceil_div(S, BS), ceil_div(S + kb + 1, BS)
+            if S < 0 or kb < 0 or want > block_table.shape[1]:
+                raise CacheError(f"request {b}: bad sizes")
+            row = block_table[b]
+            if (row[:have] < 0).any() or (row[have:want] >= 0).any():
+                raise CacheError(f"request {b}: table does not match seq_len")
+            c = bool(S % BS) and self.refcount[row[have - 1]] > 1
+            need.append(want - have + int(c))
+            cow.append(c)
+        if sum(need) > self.free_top:
+            raise OutOfBlocks(f"need {sum(need)} blocks, {self.free_top} free")
+        dropped = []
+        for b in range(B):
+            S = int(seq_len[b])
+            have = ceil_div(S, BS)
+            row = block_table[b]
+            if cow[b]:
+                old, new, r = int(row[have - 1]), self._pop(), S % BS
+                kv[new, :, :, :, :r, :] = kv[old, :, :, :, :r, :]
+                dropped.append(old)
+                row[have - 1] = new
+            for t in range(need[b] - int(cow[b])):
+                row[have + t] = self._pop()
+        for old in dropped:  # after every pop: a freed block is not reused in this call
+            self._drop(old)
+
     def commit_rollback(self, k, accepted, seq_len, block_table):
         """Commit the accepted prefix, roll back the rejected tail ([KV], [CV] 2-3).
 
@@ -193,6 +240,27 @@ class BlockPool:
                 n_freed[i] += self._drop(blk)
             seq_len[b] = 0
         return n_freed
+
+
+def commit_copy(stage, accepted, seq_len, block_table, kv, block_size) -> None:
+    """Commit by copy ([KV]: candidate K/V is written provisionally and only the
+    accepted part is kept; [RJ] paragraph 1: allocation is not acceptance).
+
+    The verify pass wrote the K/V of positions S_b .. S_b + k_b (the pending
+    token and the drafts) into stage [B, kmax + 1, L, 2, H, D]; this copies
+    entries i = 0 .. a_b (positions S_b .. S_b + a_b) into their paged slots
+    kv[table[b, p // BS], :, :, :, p % BS, :]; a_b = -1 copies nothing, and
+    rejected entries are never written.  seq_len: S_b, the length before
+    commit_rollback updates it.
+    """
+    for b in range(len(accepted)):
+        S, a = int(seq_len[b]), int(accepted[b])
+        for i in range(a + 1):
+            p = S + i
+            blk = int(block_table[b, p // block_size])
+            if blk < 0:
+                raise CacheError(f"request {b}: position {p} has no block")
+            kv[blk, :, :, :, p % block_size, :] = stage[b, i]
 
 
 def rollback_contiguous(accepted, write_ptr) -> None:

@@ -7,7 +7,8 @@ and there is no fallback: if the library is missing the import fails loudly.
 
 Functions carry the C names: sv_create, sv_destroy, sv_workspace_size,
 spec_verify, bfl_init, bfl_reserve, bfl_fork_prefix, bfl_release,
-kv_commit_rollback, kv_commit_draft, kv_rollback_contig, sv_get_error.  ``Verifier`` and
+kv_commit_rollback, kv_commit_draft, bfl_reserve_cow, kv_commit_copy,
+kv_rollback_contig, sv_get_error.  ``Verifier`` and
 ``BlockPool`` are thin owners of a handle / workspace and of the pool arrays.
 """
 
@@ -36,7 +37,22 @@ ROW_NONE, ROW_ACCEPTED, ROW_REJECTED, ROW_SKIPPED, ROW_INVALID, ROW_BONUS = rang
 EXPORTS = ("sv_verify_args_size", "sv_create", "sv_destroy", "sv_workspace_size",
            "spec_verify", "bfl_init", "bfl_reserve", "bfl_fork_prefix", "bfl_release",
            "kv_commit_rollback", "kv_rollback_contig", "sv_get_error", "spec_verify_static",
-           "kv_commit_draft")
+           "kv_commit_draft", "bfl_reserve_cow", "kv_commit_copy")
+
+
+class KvPayload(ctypes.Structure):
+    _fields_ = [("data", c_void_p), ("layers", c_int32), ("heads", c_int32),
+                ("head_dim", c_int32), ("elem_bytes", c_int32)]
+
+
+def _payload(kv: torch.Tensor) -> KvPayload:
+    """kv: [num_blocks, layers, 2, heads, block_size, head_dim], contiguous."""
+    if kv.dim() != 6 or kv.shape[2] != 2 or not kv.is_contiguous():
+        raise ValueError("kv must be a contiguous [num_blocks, layers, 2, heads, BS, head_dim] tensor")
+    p = KvPayload()
+    p.data, p.layers, p.heads, p.head_dim = _ptr(kv), kv.shape[1], kv.shape[3], kv.shape[5]
+    p.elem_bytes = kv.element_size()
+    return p
 
 
 class SvVerifyArgs(ctypes.Structure):
@@ -85,6 +101,10 @@ def load_library(path: str = LIB_PATH):
                                     c_void_p, c_void_p, c_int32, c_int32, c_void_p]
     lib.bfl_release.argtypes = [c_void_p, POINTER(BflState), c_int32, c_void_p, c_void_p,
                                 c_void_p, c_int32, c_int32, c_void_p, c_void_p]
+    lib.bfl_reserve_cow.argtypes = [c_void_p, POINTER(BflState), c_int32, c_void_p, c_void_p,
+                                    c_void_p, c_int32, POINTER(KvPayload), c_void_p, c_void_p]
+    lib.kv_commit_copy.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
+                                   c_int32, c_int32, c_int32, c_void_p, POINTER(KvPayload), c_void_p]
     lib.kv_commit_draft.argtypes = [c_void_p, POINTER(BflState), c_int32, c_void_p, c_void_p,
                                     c_void_p, c_void_p, c_int32, c_void_p, c_void_p]
     lib.kv_commit_rollback.argtypes = [c_void_p, POINTER(BflState), c_int32, c_void_p, c_void_p,
@@ -232,6 +252,27 @@ def bfl_release(handle, pool, req_ids, seq_len, block_table, n_freed=None, strea
         _stream(stream)))
 
 
+def bfl_reserve_cow(handle, pool, seq_len, k, block_table, kv, cow_scratch, stream=None) -> None:
+    """cow_scratch: int32 device tensor of at least 3 * B elements (caller-owned)."""
+    if cow_scratch.numel() < 3 * seq_len.numel():
+        raise ValueError("cow_scratch needs 3 * B int32 elements")
+    _check("bfl_reserve_cow", load_library().bfl_reserve_cow(
+        handle, ctypes.byref(_state(pool)), seq_len.numel(), _ptr(seq_len), _ptr(k),
+        _ptr(block_table), block_table.shape[1], ctypes.byref(_payload(kv)), _ptr(cow_scratch),
+        _stream(stream)))
+
+
+def kv_commit_copy(handle, accepted, seq_len, block_table, block_size, num_blocks, stage, kv,
+                   stream=None) -> None:
+    """stage: [B, kmax + 1, layers, 2, heads, head_dim] contiguous, kv's dtype."""
+    if stage.dim() != 6 or not stage.is_contiguous() or stage.dtype != kv.dtype:
+        raise ValueError("stage must be a contiguous [B, kmax+1, layers, 2, heads, head_dim] tensor")
+    _check("kv_commit_copy", load_library().kv_commit_copy(
+        handle, accepted.numel(), stage.shape[1] - 1, _ptr(accepted), _ptr(seq_len),
+        _ptr(block_table), block_table.shape[1], block_size, num_blocks, _ptr(stage),
+        ctypes.byref(_payload(kv)), _stream(stream)))
+
+
 def kv_commit_draft(handle, pool, seq_len, accepted, draft_len, draft_table, n_freed=None,
                     stream=None) -> None:
     _check("kv_commit_draft", load_library().kv_commit_draft(
@@ -276,6 +317,9 @@ class BlockPool:
 
     def commit_rollback(self, k, accepted, seq_len, block_table, n_freed=None, stream=None):
         kv_commit_rollback(self.handle, self, k, accepted, seq_len, block_table, n_freed, stream)
+
+    def reserve_cow(self, seq_len, k, block_table, kv, cow_scratch, stream=None):
+        bfl_reserve_cow(self.handle, self, seq_len, k, block_table, kv, cow_scratch, stream)
 
     def commit_draft(self, seq_len, accepted, draft_len, draft_table, n_freed=None, stream=None):
         kv_commit_draft(self.handle, self, seq_len, accepted, draft_len, draft_table, n_freed, stream)

@@ -302,6 +302,150 @@ __global__ void __launch_bounds__(kKvThreads) kv_commit_kernel(bfl_state st, int
 }
 
 // ---------------------------------------------------------------------------
+// Lookahead reserve with copy-on-write of a shared partial last block.
+// Bookkeeping (one block): pops in (request, j) order with the copy first, the
+// copy list to cow[b] = (old, new, r), then the old blocks dropped in request
+// order and the copies installed.  kv_cow_copy_kernel moves the payload.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kKvThreads) bfl_reserve_cow_kernel(bfl_state st, int B,
+                                                                     const int32_t* seq_len,
+                                                                     const int32_t* k, int32_t* table,
+                                                                     int max_blocks, int32_t* cow,
+                                                                     int* err) {
+  __shared__ int scratch[32];
+  __shared__ int s_err;
+  const int BS = st.block_size, nb = st.num_blocks;
+  if (threadIdx.x == 0) s_err = 0;
+  __syncthreads();
+  int total = 0;
+  for (int base = 0; base < B; base += blockDim.x) {
+    const int b = base + threadIdx.x;
+    int need = 0;
+    if (b < B) {
+      const int S = seq_len[b], kb = k ? k[b] : 0;
+      const int have = ceil_div(S, BS), want = ceil_div(S + kb + 1, BS);
+      const int32_t* row = table + (size_t)b * max_blocks;
+      bool bad = S < 0 || kb < 0 || want > max_blocks;
+      for (int j = 0; !bad && j < have; ++j) bad = row[j] < 0 || row[j] >= nb;
+      for (int j = have; !bad && j < want; ++j) bad = row[j] >= 0;
+      if (bad) atomicExch(&s_err, 1);
+      const bool c = !bad && (S % BS) != 0 && st.refcount[row[have - 1]] > 1;
+      need = bad ? 0 : want - have + (c ? 1 : 0);
+      cow[3 * b] = c ? row[have - 1] : -1;
+      cow[3 * b + 1] = -1;
+      cow[3 * b + 2] = c ? S % BS : 0;
+    }
+    int t;
+    block_excl_scan(need, scratch, &t);
+    total += t;
+  }
+  __syncthreads();
+  const int top = *st.free_top;
+  if (s_err || total > top) {  // refused: no copy may run either
+    for (int b = threadIdx.x; b < B; b += blockDim.x) cow[3 * b] = -1;
+    if (threadIdx.x == 0) report(err, s_err ? SV_ERR_STATE : SV_ERR_OOM);
+    return;
+  }
+  int running = 0;
+  for (int base = 0; base < B; base += blockDim.x) {
+    const int b = base + threadIdx.x;
+    int need = 0, have = 0, c = 0;
+    if (b < B) {
+      const int S = seq_len[b], kb = k ? k[b] : 0;
+      have = ceil_div(S, BS);
+      c = cow[3 * b] >= 0 ? 1 : 0;
+      need = ceil_div(S + kb + 1, BS) - have + c;
+    }
+    int t;
+    const int excl = block_excl_scan(need, scratch, &t) + running;
+    if (b < B) {
+      int32_t* row = table + (size_t)b * max_blocks;
+      for (int j = 0; j < need; ++j) {
+        const int blk = st.free_stack[top - 1 - (excl + j)];
+        st.refcount[blk] = 1;
+        if (c && j == 0) cow[3 * b + 1] = blk;  // the copy: installed after the drops
+        else row[have + j - c] = blk;
+      }
+      if (!c) cow[3 * b + 1] = -1;
+    }
+    running += t;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) *st.free_top = top - total;
+  __syncthreads();
+  // the shared blocks lose one reference per copy (pushed if none is left)
+  auto range = [&](int b) {
+    const int S = seq_len[b];
+    const int have = ceil_div(S, BS);
+    return cow[3 * b] >= 0 ? DropRange{table + (size_t)b * max_blocks, have - 1, have}
+                           : DropRange{table + (size_t)b * max_blocks, 0, 0};
+  };
+  auto done = [&](int, int) {};
+  drop_blocks(st, B, max_blocks, range, done, err);
+  __syncthreads();
+  for (int b = threadIdx.x; b < B; b += blockDim.x)
+    if (cow[3 * b] >= 0) table[(size_t)b * max_blocks + ceil_div(seq_len[b], BS) - 1] = cow[3 * b + 1];
+}
+
+// Payload of the copy-on-write blocks: slots [0, r) of every (layer, K/V,
+// head) run, old -> new.  Grid: B x kCowSplit CTAs, 16-byte vectors.
+constexpr int kCowSplit = 8;
+
+__global__ void kv_cow_copy_kernel(int B, const int32_t* cow, kv_payload kv, int block_size) {
+  const int b = blockIdx.x / kCowSplit, part = blockIdx.x % kCowSplit;
+  if (b >= B) return;
+  const int old = cow[3 * b], nw = cow[3 * b + 1], r = cow[3 * b + 2];
+  if (old < 0 || nw < 0 || r <= 0) return;
+  const int runs = kv.layers * 2 * kv.heads;
+  const size_t run = (size_t)block_size * kv.head_dim * kv.elem_bytes;  // bytes of one (l, kv, h) run
+  const int vec = (int)((size_t)r * kv.head_dim * kv.elem_bytes / 16);  // 16-byte vectors to copy per run
+  const char* src = static_cast<const char*>(kv.data) + (size_t)old * runs * run;
+  char* dst = static_cast<char*>(kv.data) + (size_t)nw * runs * run;
+  for (int q = part; q < runs; q += kCowSplit) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src + (size_t)q * run);
+    uint4* d4 = reinterpret_cast<uint4*>(dst + (size_t)q * run);
+    for (int v = threadIdx.x; v < vec; v += blockDim.x) d4[v] = s4[v];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Commit by copy: staged K/V of positions S_b .. S_b + a_b into paged slots.
+// One CTA per (request, entry); each moves layers x 2 x heads runs of
+// head_dim elements with 16-byte vectors.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) kv_commit_copy_kernel(int B, int kmax, const int32_t* accepted,
+                                                             const int32_t* seq_len,
+                                                             const int32_t* table, int max_blocks,
+                                                             int block_size, int num_blocks,
+                                                             const char* stage, kv_payload kv,
+                                                             int* err) {
+  const int b = blockIdx.x / (kmax + 1), i = blockIdx.x % (kmax + 1);
+  if (b >= B) return;
+  const int a = accepted[b];
+  if (i > a) return;
+  const int p = seq_len[b] + i;
+  const int j = p / block_size;
+  const int blk = (p >= 0 && j < max_blocks) ? table[(size_t)b * max_blocks + j] : -1;
+  if (blk < 0 || blk >= num_blocks) {
+    if (threadIdx.x == 0) report(err, SV_ERR_STATE);
+    return;
+  }
+  const int runs = kv.layers * 2 * kv.heads;
+  const int vrun = kv.head_dim * kv.elem_bytes / 16;  // 16-byte vectors per run
+  const size_t run = (size_t)block_size * kv.head_dim * kv.elem_bytes;
+  const uint4* src = reinterpret_cast<const uint4*>(
+      stage + ((size_t)b * (kmax + 1) + i) * runs * kv.head_dim * kv.elem_bytes);
+  char* dst = static_cast<char*>(kv.data) + (size_t)blk * runs * run +
+              (size_t)(p % block_size) * kv.head_dim * kv.elem_bytes;
+  const int n = runs * vrun;
+#pragma unroll 4
+  for (int v = threadIdx.x; v < n; v += blockDim.x) {
+    const int q = v / vrun, w = v - q * vrun;
+    reinterpret_cast<uint4*>(dst + (size_t)q * run)[w] = src[v];
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Draft-cache realignment: the draft keeps min(D_b, committed length) of its
 // own processed positions and drops the blocks past them.
 // ---------------------------------------------------------------------------
@@ -488,6 +632,42 @@ extern "C" sv_status kv_commit_rollback(sv_handle* h, const bfl_state* st, int32
   if (!accepted || !seq_len || !table) return SV_ERR_INVALID;
   kv_commit_kernel<<<1, kv_threads(B), 0, (cudaStream_t)stream>>>(*st, B, k, accepted, seq_len, table,
                                                                max_blocks, n_freed, h->d_err);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+static bool bad_payload(const kv_payload* kv) {
+  return !kv || !kv->data || ((uintptr_t)kv->data & 15u) || kv->layers < 1 || kv->heads < 1 ||
+         kv->head_dim < 1 || (kv->elem_bytes != 2 && kv->elem_bytes != 4) ||
+         ((size_t)kv->head_dim * kv->elem_bytes) % 16;
+}
+
+extern "C" sv_status bfl_reserve_cow(sv_handle* h, const bfl_state* st, int32_t B,
+                                     const int32_t* seq_len, const int32_t* k, int32_t* table,
+                                     int32_t max_blocks, const kv_payload* kv, int32_t* cow_scratch,
+                                     sv_stream_t stream) {
+  if (!h || bad_state(st) || B < 0 || max_blocks < 1 || bad_payload(kv)) return SV_ERR_INVALID;
+  if (B == 0) return SV_OK;
+  if (!seq_len || !table || !cow_scratch) return SV_ERR_INVALID;
+  bfl_reserve_cow_kernel<<<1, kv_threads(B), 0, (cudaStream_t)stream>>>(*st, B, seq_len, k, table,
+                                                                       max_blocks, cow_scratch,
+                                                                       h->d_err);
+  kv_cow_copy_kernel<<<B * kCowSplit, 256, 0, (cudaStream_t)stream>>>(B, cow_scratch, *kv,
+                                                                      st->block_size);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+extern "C" sv_status kv_commit_copy(sv_handle* h, int32_t B, int32_t kmax, const int32_t* accepted,
+                                    const int32_t* seq_len, const int32_t* table, int32_t max_blocks,
+                                    int32_t block_size, int32_t num_blocks, const void* stage,
+                                    const kv_payload* kv, sv_stream_t stream) {
+  if (!h || B < 0 || kmax < 0 || max_blocks < 1 || block_size < 1 || num_blocks < 0 ||
+      bad_payload(kv) || ((uintptr_t)stage & 15u))
+    return SV_ERR_INVALID;
+  if (B == 0) return SV_OK;
+  if (!accepted || !seq_len || !table || !stage) return SV_ERR_INVALID;
+  kv_commit_copy_kernel<<<B * (kmax + 1), 256, 0, (cudaStream_t)stream>>>(
+      B, kmax, accepted, seq_len, table, max_blocks, block_size, num_blocks,
+      static_cast<const char*>(stage), *kv, h->d_err);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 

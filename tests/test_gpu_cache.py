@@ -274,3 +274,44 @@ def test_draft_cache_realignment_bit_exact(ver):
     assert ver.error() == binding.SV_ERR_STATE
     for a, b in zip(snap, (drf.gt, drf.gs, drf.g.refcount, drf.g.free_top)):
         assert torch.equal(a, b)
+
+
+def test_copy_on_write_and_commit_by_copy_bit_exact(ver):
+    """Paged payload [blocks, L, 2, H, BS, D] on both sides: requests fork
+    prefixes whose last block is partial, reserve with copy-on-write, stage
+    candidate K/V and commit the accepted entries by copy.  Pools, tables and
+    the whole payload match the reference bit for bit every round."""
+    rng = np.random.default_rng(31)
+    B, BS, mb, L, H, D = 24, 16, 64, 2, 2, 8
+    nblk = B * mb
+    pr = Pair(ver, nblk, BS, B, mb)
+    kv_r = rng.standard_normal((nblk, L, 2, H, BS, D)).astype(np.float32)
+    kv_g = torch.tensor(kv_r, device=DEV)
+    scratch = torch.empty(3 * B, dtype=torch.int32, device=DEV)
+    # requests 0..7 get prefixes; 8..23 fork them (the last forked block is partial)
+    pr.admit(np.arange(8), rng.integers(20, 300, 8))
+    src = np.arange(8).repeat(2)
+    dst = np.arange(8, 24)
+    nblocks = np.array([kvcache.ceil_div(int(pr.rs[s]), BS) for s in src])
+    pr.g.fork_prefix(pr.t(src), pr.t(dst), pr.t(nblocks), pr.gt)
+    pr.r.fork_prefix(src, dst, nblocks, pr.rt)
+    pr.gs[torch.tensor(dst, device=DEV)] = pr.t(pr.rs[src])
+    pr.rs[dst] = pr.rs[src]
+    pr.check()
+    kmax = 6
+    for step in range(8):
+        k = rng.integers(0, kmax + 1, B)
+        pr.g.reserve_cow(pr.gs, pr.t(k), pr.gt, kv_g, scratch)
+        pr.r.reserve_cow(pr.rs, k, pr.rt, kv_r)
+        pr.check()
+        np.testing.assert_array_equal(kv_g.cpu().numpy(), kv_r)
+        stage = rng.standard_normal((B, kmax + 1, L, 2, H, D)).astype(np.float32)
+        acc = np.array([rng.integers(-1, kb + 1) for kb in k])
+        binding.kv_commit_copy(ver.handle, pr.t(acc), pr.gs, pr.gt, BS, nblk,
+                               torch.tensor(stage, device=DEV), kv_g)
+        kvcache.commit_copy(stage, acc, pr.rs, pr.rt, kv_r, BS)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(kv_g.cpu().numpy(), kv_r)
+        pr.commit(k, acc)
+        pr.check()
+    assert ver.error() == 0

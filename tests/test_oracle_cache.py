@@ -5,7 +5,8 @@ model against a no-speculation recompute, and shared-prefix isolation."""
 import numpy as np
 import pytest
 
-from oracle.kvcache import BlockPool, CacheError, OutOfBlocks, ceil_div, rollback_contiguous
+from oracle.kvcache import (BlockPool, CacheError, OutOfBlocks, ceil_div, commit_copy,
+                            rollback_contiguous)
 from tests.toy_model import PagedPayload, ToyAttention
 
 
@@ -289,3 +290,111 @@ def test_draft_cache_matches_recompute_after_realignment(reject_at):
         want = draft.next_distribution(draft.kv(history[:n_proc], list(range(n_proc))), history[-1], n_proc)
         np.testing.assert_array_equal(got, want)
         _check_invariants(pool, table)
+
+
+# --------------------------------------------------------------------------- #
+# commit by copy and copy-on-write
+# --------------------------------------------------------------------------- #
+def _gather(kv, row, n, BS):
+    return np.stack([kv[row[j // BS], :, :, :, j % BS, :] for j in range(n)]) if n else \
+        np.zeros((0,) + kv.shape[1:4] + kv.shape[5:], kv.dtype)
+
+
+@pytest.mark.parametrize("reject_at", [0, 2, 4, None])
+def test_commit_by_copy_matches_recompute(reject_at):
+    """The verify pass writes candidate K/V to a staging buffer only; commit by
+    copy moves the accepted entries into the paged cache, which then equals a
+    recompute of the committed history (rejected entries never reach it)."""
+    BS, k = 16, 5
+    m = ToyAttention(seed=5)
+    rng = np.random.default_rng(6)
+    pool = BlockPool(32, BS)
+    kv = np.full((32, m.L, 2, m.H, BS, m.d), np.nan, np.float32)   # unwritten slots are NaN
+    table = np.full((1, 16), -1, np.int32)
+    S = 30
+    history = list(rng.integers(0, 1000, S + 1))
+    seq = np.array([0], np.int32)
+    pool.reserve(seq, [S - 1], table)
+    stage0 = m.kv(history[:S], list(range(S)))
+    for j in range(S):
+        kv[table[0, j // BS], :, :, :, j % BS, :] = stage0[j]
+    seq[0] = S
+    for rnd in range(3):
+        drafts = list(rng.integers(0, 1000, k))
+        pool.reserve(seq, [k], table)
+        S0 = int(seq[0])
+        stage = m.kv([history[-1]] + drafts, list(range(S0, S0 + k + 1)))[None]
+        a = (k if reject_at is None else reject_at) if rnd == 0 else int(rng.integers(0, k + 1))
+        commit_copy(stage, [a], seq.copy(), table, kv, BS)
+        pool.commit_rollback([k], [a], seq, table)
+        history = history + drafts[:a] + [int(rng.integers(0, 1000))]
+        n = int(seq[0])
+        np.testing.assert_array_equal(_gather(kv, table[0], n, BS),
+                                      m.kv(history[:-1], list(range(n))))
+        _check_invariants(pool, table, seq)
+
+
+def test_copy_on_write_keeps_forked_prefixes_isolated():
+    """Three requests share a 37-token prefix (its third block is partial).
+    Each appends its own drafts through reserve_cow; the shared partial block
+    is copied before any write, every request's cache equals a recompute of its
+    own history, and the blocks still shared are never written."""
+    BS, k, S = 16, 4, 37
+    m = ToyAttention(seed=7)
+    rng = np.random.default_rng(8)
+    pool = BlockPool(64, BS)
+    kv = np.full((64, m.L, 2, m.H, BS, m.d), np.nan, np.float32)
+    table = np.full((3, 16), -1, np.int32)
+    prefix = list(rng.integers(0, 1000, S + 1))
+    seq = np.array([0, 0, 0], np.int32)
+    pool.reserve(seq[:1], [S - 1], table[:1])
+    rows = m.kv(prefix[:S], list(range(S)))
+    for j in range(S):
+        kv[table[0, j // BS], :, :, :, j % BS, :] = rows[j]
+    pool.fork_prefix([0, 0], [1, 2], [3, 3], table)
+    seq[:] = S
+    full_blocks = table[0, :2].copy()
+    shared_full = kv[full_blocks].copy()
+    partial = int(table[0, 2])
+    partial_before = kv[partial].copy()
+    hist = [list(prefix), list(prefix), list(prefix)]
+    with pytest.raises(CacheError):                       # plain reserve refuses the append
+        pool.copy().reserve(seq, [k, k, k], table.copy())
+    for rnd in range(3):
+        pool.reserve_cow(seq, [k, k, k], table, kv)
+        if rnd == 0:
+            # all three owners append in this call: each gets a copy (popped in
+            # request order) and the original partial block returns to the free list
+            assert partial not in {int(table[b, 2]) for b in range(3)}
+            assert len({int(table[b, 2]) for b in range(3)}) == 3
+            assert pool.refcount[partial] == 0 and partial in pool.free_stack[:pool.free_top]
+            for b in range(3):
+                np.testing.assert_array_equal(kv[table[b, 2], :, :, :, :S % BS],
+                                              partial_before[:, :, :, :S % BS])
+        drafts = [list(rng.integers(0, 1000, k)) for _ in range(3)]
+        stage = np.stack([m.kv([hist[b][-1]] + drafts[b], list(range(int(seq[b]), int(seq[b]) + k + 1)))
+                          for b in range(3)])
+        acc = [int(rng.integers(0, k + 1)) for _ in range(3)]
+        commit_copy(stage, acc, seq.copy(), table, kv, BS)
+        pool.commit_rollback([k, k, k], acc, seq, table)
+        for b in range(3):
+            hist[b] = hist[b] + drafts[b][:acc[b]] + [int(rng.integers(0, 1000))]
+            n = int(seq[b])
+            assert n == len(hist[b]) - 1
+            np.testing.assert_array_equal(_gather(kv, table[b], n, BS),
+                                          m.kv(hist[b][:-1], list(range(n))))
+        _check_invariants(pool, table, seq)
+    np.testing.assert_array_equal(kv[full_blocks], shared_full)   # whole shared blocks untouched
+    # an owner outside the call keeps the original block; the caller that appends copies it
+    pool2 = BlockPool(16, BS)
+    kv2 = np.zeros((16, 1, 2, 1, BS, 2), np.float32)
+    t2 = np.full((2, 4), -1, np.int32)
+    s2 = np.array([0, 0], np.int32)
+    pool2.reserve(s2[:1], [S - 1], t2[:1])
+    kv2[t2[0, 2], :, :, :, :S % BS] = 7.0
+    pool2.fork_prefix([0], [1], [3], t2)
+    s2[:] = S
+    pool2.reserve_cow(s2[1:], [k], t2[1:], kv2)
+    assert t2[0, 2] == 2 and t2[1, 2] != 2 and pool2.refcount[2] == 1
+    np.testing.assert_array_equal(kv2[t2[1, 2], :, :, :, :S % BS], 7.0)
+    _check_invariants(pool2, t2)
