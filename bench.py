@@ -335,6 +335,7 @@ def run_ours(args):
 
     # end to end through the public API with host buffers (pinned)
     e2e = e2e_run(ver, sets, dev, args, pool, table, seq, kk, B, k)
+    copy_line = commit_copy_run(ver, sets, outs, dev, peak)
 
     line = {"metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": ws, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
@@ -354,7 +355,8 @@ def run_ours(args):
                          "peak_source": peak_src,
                          "frac_of_8tbs": achieved / 8000.0},
             "clocks": clk.summary(),
-            "e2e": e2e}
+            "e2e": e2e,
+            "kv_commit_copy": copy_line}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(sets[0])
     if rank == 0:
@@ -405,6 +407,51 @@ def e2e_run(ver, sets, dev, args, pool, table, seq, kk, B, k):
     rows = rows_per_step(sets[0])
     return {"value": rows * n / (ms / 1e3), "unit": "rows/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": n}
+
+
+def commit_copy_run(ver, sets, outs, dev, peak):
+    """The commit-by-copy kernel at the workload's KV shape (32 layers x 8 KV
+    heads x d128 bf16, block 16): entries 0..a_b of every request move from a
+    staging buffer into their paged slots.  Four staging sets (> L2) rotate.
+    Bytes per launch: sum_b (a_b + 1) x layers x 2 x heads x d x 2 B, read + written."""
+    import torch
+
+    from speculative_decoding_verification_07_gb300 import binding
+    L, H, D, BS = 32, 8, 128, 16
+    B, kmax = 64, 4
+    # every request's positions S .. S + k lie in at most 2 blocks: give each its own two
+    S = [torch.tensor(s["seq_len"], dtype=torch.int32, device=dev) for s in sets]
+    max_blocks = (8192 + 2 * BS) // BS + 2
+    tables = []
+    for s_dev in S:
+        t = torch.full((B, max_blocks), -1, dtype=torch.int32)
+        for b, s0 in enumerate(s_dev.cpu().tolist()):
+            t[b, s0 // BS] = 2 * b
+            t[b, (s0 + kmax) // BS] = 2 * b + 1
+        tables.append(t.to(dev))
+    kv = torch.zeros(2 * B, L, 2, H, BS, D, dtype=torch.bfloat16, device=dev)
+    stages = [torch.randn(B, kmax + 1, L, 2, H, D, device=dev).to(torch.bfloat16) for _ in sets]
+    acc = [o["accepted"].clone() for o in outs]
+    run = lambda i: binding.kv_commit_copy(ver.handle, acc[i % len(sets)], S[i % len(sets)],
+                                           tables[i % len(sets)], BS, 2 * B,
+                                           stages[i % len(sets)], kv)
+    for i in range(8):
+        run(i)
+    torch.cuda.synchronize()
+    n = 64
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(n):
+        run(i)
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) / n * 1e3
+    per_tok = L * 2 * H * D * 2
+    nbytes = float(np.mean([2 * ((a.cpu().numpy().astype(np.int64) + 1).clip(min=0).sum()) * per_tok
+                            for a in acc]))
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"us": us, "bytes_per_launch": nbytes, "GB/s": gbs, "peak": peak, "frac": gbs / peak,
+            "shape": "32 layers x 8 KV heads x d128 bf16, block 16, staged entries 0..a_b"}
 
 
 def kernel_source_sha():

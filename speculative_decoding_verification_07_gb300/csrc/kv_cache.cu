@@ -410,16 +410,19 @@ __global__ void kv_cow_copy_kernel(int B, const int32_t* cow, kv_payload kv, int
 
 // ---------------------------------------------------------------------------
 // Commit by copy: staged K/V of positions S_b .. S_b + a_b into paged slots.
-// One CTA per (request, entry); each moves layers x 2 x heads runs of
-// head_dim elements with 16-byte vectors.
+// kCopySplit CTAs per (request, entry) share its layers x 2 x heads runs of
+// head_dim elements; every thread keeps 8 16-byte loads in flight.
 // ---------------------------------------------------------------------------
+constexpr int kCopySplit = 8;
+
 __global__ void __launch_bounds__(256) kv_commit_copy_kernel(int B, int kmax, const int32_t* accepted,
                                                              const int32_t* seq_len,
                                                              const int32_t* table, int max_blocks,
                                                              int block_size, int num_blocks,
                                                              const char* stage, kv_payload kv,
                                                              int* err) {
-  const int b = blockIdx.x / (kmax + 1), i = blockIdx.x % (kmax + 1);
+  const int e = blockIdx.x / kCopySplit, part = blockIdx.x % kCopySplit;
+  const int b = e / (kmax + 1), i = e % (kmax + 1);
   if (b >= B) return;
   const int a = accepted[b];
   if (i > a) return;
@@ -427,7 +430,7 @@ __global__ void __launch_bounds__(256) kv_commit_copy_kernel(int B, int kmax, co
   const int j = p / block_size;
   const int blk = (p >= 0 && j < max_blocks) ? table[(size_t)b * max_blocks + j] : -1;
   if (blk < 0 || blk >= num_blocks) {
-    if (threadIdx.x == 0) report(err, SV_ERR_STATE);
+    if (threadIdx.x == 0 && part == 0) report(err, SV_ERR_STATE);
     return;
   }
   const int runs = kv.layers * 2 * kv.heads;
@@ -438,10 +441,23 @@ __global__ void __launch_bounds__(256) kv_commit_copy_kernel(int B, int kmax, co
   char* dst = static_cast<char*>(kv.data) + (size_t)blk * runs * run +
               (size_t)(p % block_size) * kv.head_dim * kv.elem_bytes;
   const int n = runs * vrun;
-#pragma unroll 4
-  for (int v = threadIdx.x; v < n; v += blockDim.x) {
-    const int q = v / vrun, w = v - q * vrun;
-    reinterpret_cast<uint4*>(dst + (size_t)q * run)[w] = src[v];
+  const int v0 = (int)((long long)n * part / kCopySplit), v1 = (int)((long long)n * (part + 1) / kCopySplit);
+  constexpr int kU = 8;
+  for (int base = v0 + threadIdx.x; base < v1; base += kU * blockDim.x) {
+    uint4 r[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int v = base + u * blockDim.x;
+      if (v < v1) r[u] = src[v];
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int v = base + u * blockDim.x;
+      if (v < v1) {
+        const int q = v / vrun, w = v - q * vrun;
+        reinterpret_cast<uint4*>(dst + (size_t)q * run)[w] = r[u];
+      }
+    }
   }
 }
 
@@ -665,7 +681,7 @@ extern "C" sv_status kv_commit_copy(sv_handle* h, int32_t B, int32_t kmax, const
     return SV_ERR_INVALID;
   if (B == 0) return SV_OK;
   if (!accepted || !seq_len || !table || !stage) return SV_ERR_INVALID;
-  kv_commit_copy_kernel<<<B * (kmax + 1), 256, 0, (cudaStream_t)stream>>>(
+  kv_commit_copy_kernel<<<B * (kmax + 1) * kCopySplit, 256, 0, (cudaStream_t)stream>>>(
       B, kmax, accepted, seq_len, table, max_blocks, block_size, num_blocks,
       static_cast<const char*>(stage), *kv, h->d_err);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
