@@ -65,6 +65,8 @@ typedef enum { SV_DRAFT_LOGITS = 0, SV_DRAFT_PROBS = 1 } sv_draft_kind;
 #define SV_ST_BAD_INPUT 2u      /* NaN/+inf/empty row, bad T, top_p, k or token id */
 #define SV_ST_RESIDUAL_EMPTY 4u /* rejected but max(0, p - q) == 0 numerically: drew from p */
 #define SV_ST_TIMEOUT 8u        /* the request's outcome was not resolved in time */
+#define SV_ST_EOS 16u           /* an accepted draft was the request's EOS id: it ended there */
+#define SV_ST_CAPPED 32u        /* the output cap stopped the walk after accepted drafts */
 
 /* sv_verify_args.flags */
 #define SV_FLAG_NO_SKIP 1u /* also process rows after a known rejection (debug) */
@@ -76,6 +78,7 @@ typedef enum { SV_DRAFT_LOGITS = 0, SV_DRAFT_PROBS = 1 } sv_draft_kind;
 #define SV_ROW_SKIPPED 3 /* not processed: an earlier row was already rejected */
 #define SV_ROW_INVALID 4
 #define SV_ROW_BONUS 5
+#define SV_ROW_TERMINAL 6 /* accepted, and the request ends here (EOS id or output cap) */
 
 /* Optional per-row record, [B][kmax+1], written for every processed row. */
 typedef struct {
@@ -109,9 +112,18 @@ typedef struct {
  * request_id   [B] uint32 Philox stream id; NULL = b.
  * seq_len      [B] int32 S_b (read only here); NULL = 0.
  * seed         Philox4x32-10 key (lo, hi words).
+ * eos_id       [B] int32 end-of-sequence token per request (< 0: none); NULL =
+ *              none.  An ACCEPTED draft equal to it ends the request: it is
+ *              emitted and no correction or bonus follows (SV_ST_EOS).
+ * max_new      [B] int32 most tokens to emit in this call (>= 1); NULL = no
+ *              cap.  Once max_new_b accepted drafts are emitted the walk stops
+ *              (SV_ST_CAPPED); a correction or bonus is drawn only while the
+ *              cap allows it.  A cap below 1 is bad input.  ([CV] paragraph 5
+ *              lists EOS and output caps among the cases to test.)
  * Outputs: accepted [B] (a_b in [0, k_b], or -1 when the request's input is
  *   bad), out_tokens [B][kmax+1] (the a_b accepted drafts, then the correction
- *   or bonus token, then -1), num_emitted [B] (a_b + 1, or 0), status [B].
+ *   or bonus token unless EOS or the cap ended the walk, then -1), num_emitted
+ *   [B] (a_b + 1, or a_b after EOS / cap, or 0), status [B].
  * debug  optional [B][kmax+1] sv_row_debug.  probs_p / probs_q optional
  *   [B][kmax+1][V] / [B][kmax][V] fp32 normalised transformed rows (debug
  *   only: the kernel then writes 4 bytes per element of every processed row).
@@ -141,6 +153,8 @@ typedef struct {
   sv_row_debug* debug;
   float* probs_p;
   float* probs_q;
+  const int32_t* eos_id;
+  const int32_t* max_new;
 } sv_verify_args;
 
 /* Paged block pool: a LIFO free stack plus per-block reference counts

@@ -36,6 +36,12 @@ Readings taken where the pages leave a step open (each also listed in the design doc)
     ends the request: accepted = -1, nothing emitted, ST_BAD_INPUT.
   * absolute position of the token decided by row i: pos = S_b + 1 + i, where
     S_b is the cache length before the pass and the pending token sits at S_b.
+  * end of sequence and output caps ([CV] paragraph 5 lists both among the
+    cases to test): an ACCEPTED draft equal to the request's EOS id ends the
+    request there (it is emitted, no correction or bonus follows; ST_EOS); a
+    cap of c tokens per call stops the walk once c accepted drafts are emitted
+    (ST_CAPPED); a correction or bonus is emitted only while the cap allows.
+    A cap below 1 is bad input.
 """
 
 from __future__ import annotations
@@ -48,6 +54,8 @@ ST_Q_ZERO = 1
 ST_BAD_INPUT = 2
 ST_RESIDUAL_EMPTY = 4
 ST_TIMEOUT = 8
+ST_EOS = 16
+ST_CAPPED = 32
 
 
 # --------------------------------------------------------------------------- #
@@ -170,12 +178,14 @@ def exponential_race(w: np.ndarray, E: np.ndarray) -> int:
 # one request, left to right  ([SD] section 2, [KV])
 # --------------------------------------------------------------------------- #
 def verify_request(target_rows, draft_rows, tokens, k, T, top_p, draft_kind,
-                   seed, request_id, seq_len, force=None, keep_rows=False):
+                   seed, request_id, seq_len, force=None, keep_rows=False, eos=-1, cap=None):
     """Run the walk for one request on decoded fp64 rows.
 
     target_rows [>= k+1][V], draft_rows [>= k][V], tokens [>= k] (ints).
     force: optional {row: bool} that overrides the accept decision of a row
     (the parity harness uses it to follow a counted near-tie flip).
+    eos: end-of-sequence token id (< 0: none); cap: most tokens to emit (None:
+    no cap).
     Returns a dict: accepted (-1 on bad input), tokens (emitted list), status,
     rows (per-row record: p_y, q_y, u, accept, kept masses, and p/q if keep_rows).
     """
@@ -190,7 +200,12 @@ def verify_request(target_rows, draft_rows, tokens, k, T, top_p, draft_kind,
         return bad
     if not (T >= 0.0) or not (0.0 < top_p <= 1.0):
         return bad
+    if cap is not None and cap < 1:
+        return bad
     for i in range(k + 1):
+        if cap is not None and i == cap:           # c accepted drafts emitted: stop
+            return dict(accepted=i, tokens=[int(t) for t in tokens[:i]],
+                        status=status | ST_CAPPED, rows=rows)
         pos = int(seq_len) + 1 + i
         trow = target_rows[i]
         if not row_is_valid(trow, "logits"):
@@ -224,6 +239,9 @@ def verify_request(target_rows, draft_rows, tokens, k, T, top_p, draft_kind,
             ok = bool(force[i])
         rec["accept"] = ok
         if ok:
+            if eos >= 0 and y == eos:                 # an accepted end of sequence
+                return dict(accepted=i + 1, tokens=[int(t) for t in tokens[:i + 1]],
+                            status=status | ST_EOS, rows=rows)
             continue
         # first rejection: correction from normalize(max(0, p - q))
         w = residual(p, q)
@@ -244,7 +262,7 @@ def verify_batch(inp: dict, force=None, keep_rows=False):
     inp keys: target [B][kmax+1][V] (bf16 bits or fp32), target_dtype,
     draft [B][kmax][V], draft_dtype, draft_kind ('logits' | 'probs'),
     tokens [B][kmax], k [B], temperature [B], top_p [B], seed, request_id [B],
-    seq_len [B].  force: optional {b: {row: bool}}.
+    seq_len [B]; optional eos [B] and max_new [B].  force: optional {b: {row: bool}}.
     Returns accepted [B], out_tokens [B][kmax+1] (-1 padded), num_emitted [B],
     status [B] and the per-request records.
     """
@@ -267,7 +285,9 @@ def verify_batch(inp: dict, force=None, keep_rows=False):
                                inp["temperature"][b], inp["top_p"][b],
                                inp["draft_kind"], inp["seed"],
                                int(inp["request_id"][b]), int(inp["seq_len"][b]),
-                               force=(force or {}).get(b), keep_rows=keep_rows)
+                               force=(force or {}).get(b), keep_rows=keep_rows,
+                               eos=int(inp["eos"][b]) if inp.get("eos") is not None else -1,
+                               cap=int(inp["max_new"][b]) if inp.get("max_new") is not None else None)
         accepted[b] = r["accepted"]
         status[b] = r["status"]
         nemit[b] = len(r["tokens"])

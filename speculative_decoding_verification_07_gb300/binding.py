@@ -31,8 +31,9 @@ SV_STATIC_MAX_ROWS = 16384  # rows B * (kmax + 1) one spec_verify_static call ac
 SV_BF16, SV_FP32 = 0, 1
 SV_DRAFT_LOGITS, SV_DRAFT_PROBS = 0, 1
 ST_Q_ZERO, ST_BAD_INPUT, ST_RESIDUAL_EMPTY, ST_TIMEOUT = 1, 2, 4, 8
+ST_EOS, ST_CAPPED = 16, 32
 FLAG_NO_SKIP = 1
-ROW_NONE, ROW_ACCEPTED, ROW_REJECTED, ROW_SKIPPED, ROW_INVALID, ROW_BONUS = range(6)
+ROW_NONE, ROW_ACCEPTED, ROW_REJECTED, ROW_SKIPPED, ROW_INVALID, ROW_BONUS, ROW_TERMINAL = range(7)
 
 EXPORTS = ("sv_verify_args_size", "sv_create", "sv_destroy", "sv_workspace_size",
            "spec_verify", "bfl_init", "bfl_reserve", "bfl_fork_prefix", "bfl_release",
@@ -66,7 +67,7 @@ class SvVerifyArgs(ctypes.Structure):
                 ("seed", c_uint64),
                 ("accepted", c_void_p), ("out_tokens", c_void_p), ("num_emitted", c_void_p),
                 ("status", c_void_p), ("debug", c_void_p), ("probs_p", c_void_p),
-                ("probs_q", c_void_p)]
+                ("probs_q", c_void_p), ("eos_id", c_void_p), ("max_new", c_void_p)]
 
 
 class BflState(ctypes.Structure):
@@ -173,7 +174,8 @@ def sv_destroy(handle) -> None:
 
 def make_args(*, target, draft, draft_tokens, temperature, accepted, out_tokens, num_emitted,
               status, V=None, k=None, top_p=None, seed=0, request_id=None, seq_len=None,
-              draft_kind="logits", flags=0, debug=None, probs_p=None, probs_q=None):
+              draft_kind="logits", flags=0, debug=None, probs_p=None, probs_q=None,
+              eos=None, max_new=None):
     B, rows, _ = target.shape
     kmax = rows - 1
     a = SvVerifyArgs()
@@ -190,6 +192,7 @@ def make_args(*, target, draft, draft_tokens, temperature, accepted, out_tokens,
     a.accepted, a.out_tokens = _ptr(accepted), _ptr(out_tokens)
     a.num_emitted, a.status = _ptr(num_emitted), _ptr(status)
     a.debug, a.probs_p, a.probs_q = _ptr(debug), _ptr(probs_p), _ptr(probs_q)
+    a.eos_id, a.max_new = _ptr(eos), _ptr(max_new)
     return a
 
 

@@ -102,6 +102,7 @@ extern "C" sv_status spec_verify(sv_handle* h, const sv_verify_args* a, void* ws
   P.err = h->d_err;
   P.slice = slice, P.d_off = d_off, P.n_tickets = (int)n_tickets;
   P.spin_limit = kDefaultSpin;
+  P.eos = a->eos_id, P.max_new = a->max_new;
 
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];

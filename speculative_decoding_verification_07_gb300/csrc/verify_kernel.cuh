@@ -97,6 +97,8 @@ struct KParams {
   int d_off;      // byte offset of the draft slice in dynamic shared memory
   int n_tickets;  // (kmax + 1) * B
   int spin_limit;
+  const int32_t* eos;      // [B] or null
+  const int32_t* max_new;  // [B] or null
 };
 
 // ---------------------------------------------------------------------------
@@ -296,6 +298,8 @@ struct Ticket {
   int t, kind, kb, y, pos;
   uint32_t rid;
   float T, top_p, vt, vd;  // vt / vd: target / draft value at the proposed token
+  int eos;                 // the request's end-of-sequence id, or -1
+  int cap_row;             // 1: accepting this row reaches the output cap
 };
 
 // One warp's statistics partial: a = (target max, target sum, draft raw
@@ -1177,16 +1181,19 @@ __device__ __noinline__ void write_probs(float* out, const char* s, const SliceI
 template <int EBT, int EBD>
 __device__ void settle_ticket(const KParams& P, Smem& sm, int t, int slot, uint32_t tag) {
   const int lane = threadIdx.x & 31;
-  Ticket tk = {0, kDone, 0, 0, 0, 0u, 0.0f, 1.0f, 0.0f, 0.0f};
+  Ticket tk = {0, kDone, 0, 0, 0, 0u, 0.0f, 1.0f, 0.0f, 0.0f, -1, 0};
   t = __shfl_sync(0xffffffffu, t, 0);
   while (t < P.n_tickets) {
     const int i = t / P.B, b = t - i * P.B;
     const int kb = P.k ? P.k[b] : P.kmax;
+    const int cap = P.max_new ? P.max_new[b] : 0x7FFFFFFF;
+    // with a cap c <= k only rows 0 .. c-1 matter (accepting row c-1 ends the walk)
+    const int last = cap <= kb ? cap - 1 : kb;
     bool take = true;
-    if (kb < 0 || kb > P.kmax) {  // a bad k ends the request once, at its first row
+    if (kb < 0 || kb > P.kmax || cap < 1) {  // bad k or cap end the request once, at row 0
       if (i == 0 && lane == 0) write_bad_outputs(P, b, SV_ST_BAD_INPUT);
       take = false;
-    } else if (i > kb) {
+    } else if (i > last) {
       take = false;
     } else if (!(P.flags & SV_FLAG_NO_SKIP) && i > 0 && warp_earlier_rejected(P, b, i, tag)) {
       if (lane == 0) {
@@ -1223,7 +1230,8 @@ __device__ void settle_ticket(const KParams& P, Smem& sm, int t, int slot, uint3
       }
       vt = __shfl_sync(0xffffffffu, vt, 0);
       vd = __shfl_sync(0xffffffffu, vd, 1);
-      tk = {t, kWork, kb, y, sl + 1 + i, rid, T, tp, vt, vd};
+      const int eos = P.eos ? P.eos[b] : -1;
+      tk = {t, kWork, kb, y, sl + 1 + i, rid, T, tp, vt, vd, eos < 0 ? -1 : eos, cap <= kb && i == cap - 1};
       break;
     }
     int nt = 0;
@@ -1555,6 +1563,9 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
       u = u_row;
       qzero = q_y == 0.0f;
       state = (u * q_y < p_y) ? SV_ROW_ACCEPTED : SV_ROW_REJECTED;
+      // an accepted EOS id, or the last row the output cap allows, ends the request
+      if (state == SV_ROW_ACCEPTED && ((tk.eos >= 0 && y == tk.eos) || tk.cap_row))
+        state = SV_ROW_TERMINAL;
     } else {
       state = SV_ROW_BONUS;
     }
@@ -1604,7 +1615,17 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
       const int* dc = cluster.map_shared_rank(&sm.decide[0], 0);
       const int resolver = dc[0];
       const uint32_t st_bits = (uint32_t)dc[1];
-      if (resolver) {
+      if (resolver && state == SV_ROW_TERMINAL) {
+        // the accepted drafts 0 .. i are the whole output: no correction or bonus
+        if (lead) {
+          int32_t* ot2 = P.out_tokens + (size_t)b * (P.kmax + 1);
+          for (int j = 0; j <= i; ++j) ot2[j] = P.tokens[(size_t)b * P.kmax + j];
+          for (int j = i + 1; j <= P.kmax; ++j) ot2[j] = -1;
+          P.accepted[b] = i + 1;
+          P.num_emitted[b] = i + 1;
+          P.status[b] = st_bits | ((tk.eos >= 0 && y == tk.eos) ? SV_ST_EOS : SV_ST_CAPPED);
+        }
+      } else if (resolver) {
         const bool residual = state == SV_ROW_REJECTED;
         RacePart best = {0.0f, 1.0f, 0x7FFFFFFF};
         race_slice<EBT, EBD, PROBS>(s_t, s_d, it, residual, rt, rd, (uint32_t)pos, rid, k0, k1,

@@ -152,6 +152,7 @@ extern "C" sv_status spec_verify_static(const sv_verify_args* a, sv_stream_t str
   P.err = nullptr;  // no handle: device conditions go to the status bits only
   P.slice = slice, P.d_off = d_off, P.n_tickets = (int)rows;
   P.spin_limit = kDefaultSpin;
+  P.eos = a->eos_id, P.max_new = a->max_new;
 
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];

@@ -35,7 +35,13 @@ def to_device(inp: dict, device="cuda", pin=False) -> dict:
             x = x.pin_memory()
         return x if dev is None else x.to(dev)
 
+    extra = {}
+    if inp.get("eos") is not None:
+        extra["eos"] = t(inp["eos"], np.int32)
+    if inp.get("max_new") is not None:
+        extra["max_new"] = t(inp["max_new"], np.int32)
     return dict(
+        **extra,
         target=rows_to_device(inp["target"], inp["target_dtype"], dev, pin=pin),
         draft=rows_to_device(inp["draft"], inp["draft_dtype"], dev, pin=pin)
         if inp["draft"].shape[1] > 0 else None,

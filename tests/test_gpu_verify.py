@@ -116,6 +116,34 @@ def test_top_p_boundary_outside_the_first_window(ver):
         assert int(info["kept"].sum()) > 1000
 
 
+@pytest.mark.parametrize("V", [4093, 128256])
+def test_eos_and_output_caps(ver, V):
+    """EOS ids drawn from the requests' own proposals and random output caps
+    (some below k, some above, one invalid): outputs match the oracle's walk."""
+    inp = W.verify_b64_k4(B=64, V=V)
+    rng = np.random.default_rng(V)
+    B, k = inp["tokens"].shape
+    eos = np.full(B, -1, np.int32)
+    pick = rng.random(B) < 0.6
+    eos[pick] = inp["tokens"][pick, rng.integers(0, k, pick.sum())]
+    cap = rng.integers(1, k + 3, B).astype(np.int32)
+    cap[::5] = 1_000_000                            # effectively no cap
+    cap[7] = 0                                      # invalid
+    inp["eos"], inp["max_new"] = eos, cap
+    out, dbg, _, _ = run(ver, inp, debug=True)
+    rep = parity.compare(inp, out)
+    report(f"eos/caps V={V}", rep)
+    st = out["status"].cpu().numpy()
+    acc = out["accepted"].cpu().numpy()
+    assert acc[7] == -1 and st[7] == binding.ST_BAD_INPUT
+    assert (st & binding.ST_EOS).any() and (st & binding.ST_CAPPED).any()
+    nem = out["num_emitted"].cpu().numpy()
+    assert (nem <= np.maximum(cap, 0)).all()
+    # requests stopped by EOS or the cap emit exactly their accepted drafts
+    stopped = (st & (binding.ST_EOS | binding.ST_CAPPED)) != 0
+    assert (nem[stopped] == acc[stopped]).all()
+
+
 @pytest.mark.parametrize("top_p", [0.95, 1.0])
 def test_verify_b64_k4(ver, top_p):
     inp = W.verify_b64_k4(top_p=top_p)

@@ -374,3 +374,40 @@ def test_bad_input_and_q_zero_flags():
     inp["draft"][0, 0, y] = 0.0
     r = S.verify_batch(inp)
     assert r["status"][0] & S.ST_Q_ZERO
+
+
+def test_eos_and_output_cap():
+    """End of sequence and output caps ([CV] paragraph 5 lists both as cases to
+    test): q = p makes every proposal accepted, so the walk's stopping point
+    is fixed by the EOS id and the cap alone."""
+    rng = np.random.default_rng(40)
+    V, k = 8, 4
+    rows = rng.standard_normal((k + 1, V))
+    y = np.array([3, 5, 2, 6])
+
+    def run(**kw):
+        return S.verify_request(rows, rows[:k], y, k, 1.0, 1.0, "logits", 9, 1, 100, **kw)
+
+    r = run(eos=2)
+    assert r["accepted"] == 3 and r["tokens"] == [3, 5, 2] and r["status"] == S.ST_EOS
+    r = run(cap=2)
+    assert r["accepted"] == 2 and r["tokens"] == [3, 5] and r["status"] == S.ST_CAPPED
+    r = run(cap=4)                                   # the cap equals k: no bonus
+    assert r["accepted"] == 4 and r["tokens"] == [3, 5, 2, 6] and r["status"] == S.ST_CAPPED
+    full = run()
+    r = run(cap=5)                                   # above k: the bonus fits
+    assert r["accepted"] == 4 and r["tokens"] == full["tokens"] and len(r["tokens"]) == 5
+    assert r["status"] == 0
+    r = run(eos=5, cap=2)                            # EOS at the cap's last token
+    assert r["accepted"] == 2 and r["tokens"] == [3, 5] and r["status"] == S.ST_EOS
+    assert run(cap=0)["accepted"] == -1 and run(cap=0)["status"] == S.ST_BAD_INPUT
+    # an EOS id that is proposed but rejected changes nothing: the correction follows
+    t2 = rows.copy()
+    t2[0, 3] = -np.inf                               # p(y_0) = 0: row 0 rejects
+    r = S.verify_request(t2, rows[:k], y, k, 1.0, 1.0, "logits", 9, 1, 100, eos=3)
+    r0 = S.verify_request(t2, rows[:k], y, k, 1.0, 1.0, "logits", 9, 1, 100)
+    assert r["accepted"] == 0 and r["tokens"] == r0["tokens"] and r["status"] == 0
+    # a bonus that happens to be the EOS id is emitted as usual
+    r = run(eos=full["tokens"][-1])
+    if full["tokens"][-1] not in y.tolist():
+        assert r["tokens"] == full["tokens"] and r["status"] == 0
