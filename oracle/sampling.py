@@ -42,6 +42,11 @@ Readings taken where the pages leave a step open (each also listed in the design doc)
     cap of c tokens per call stops the walk once c accepted drafts are emitted
     (ST_CAPPED); a correction or bonus is emitted only while the cap allows.
     A cap below 1 is bad input.
+  * repetition penalty ([SD] sections 4 and 6 name it, give no formula): the
+    CTRL rule on the logits of the request's history ids plus the drafts before
+    row i, in fp32, rounded back to bf16 for bf16 rows; target and draft logit
+    rows alike; probability drafts are taken as given.  theta must be a finite
+    number > 0 (1: no penalty), else bad input.
 """
 
 from __future__ import annotations
@@ -65,6 +70,38 @@ def decode_bf16(bits) -> np.ndarray:
     """bfloat16 bit patterns (uint16) -> fp64 values (bf16 is the top half of fp32)."""
     bits = np.asarray(bits, dtype=np.uint16)
     return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def round_bf16(x) -> np.ndarray:
+    """fp32 values -> the nearest bfloat16 (ties to even), returned as fp64.
+    bfloat16 is the upper half of an fp32 word; infinities and NaN keep their
+    class."""
+    f = np.atleast_1d(np.asarray(x, dtype=np.float32))
+    u = f.view(np.uint32).astype(np.uint64)
+    r = (u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
+    r = np.where(np.isinf(f), u >> np.uint64(16), r)
+    r = np.where(np.isnan(f), np.uint64(0x7FC0), r)
+    return decode_bf16(r.astype(np.uint16))
+
+
+def repetition_penalty(row: np.ndarray, ids, theta: float, dtype: str) -> np.ndarray:
+    """Repetition penalty on the logits of the tokens in `ids` (a set; ids
+    outside [0, V) are ignored).  [SD] section 4 ("When it wins") counts
+    repetition penalties among the transforms that p and q are taken after,
+    and section 6 requires draft and target to apply the same ones; the pages
+    give no formula, so this takes the usual one (Keskar et al., "CTRL",
+    2019): a logit l > 0 becomes l / theta, any other l becomes l * theta.
+    Readings: applied to target and draft logit rows alike, before the
+    temperature, in fp32 (the rows' arithmetic), and a bf16 row keeps the
+    result rounded back to bf16 (ties to even)."""
+    out = np.array(row, dtype=np.float64, copy=True)
+    th = np.float32(theta)
+    V = out.shape[-1]
+    for t in sorted({int(i) for i in ids if 0 <= int(i) < V}):
+        l = np.float32(out[t])
+        v = np.float32(l / th) if l > 0 else np.float32(l * th)
+        out[t] = float(round_bf16(v)[0]) if dtype == "bf16" else float(v)
+    return out
 
 
 def decode(values, dtype: str) -> np.ndarray:
@@ -178,14 +215,17 @@ def exponential_race(w: np.ndarray, E: np.ndarray) -> int:
 # one request, left to right  ([SD] section 2, [KV])
 # --------------------------------------------------------------------------- #
 def verify_request(target_rows, draft_rows, tokens, k, T, top_p, draft_kind,
-                   seed, request_id, seq_len, force=None, keep_rows=False, eos=-1, cap=None):
+                   seed, request_id, seq_len, force=None, keep_rows=False, eos=-1, cap=None,
+                   rep=None):
     """Run the walk for one request on decoded fp64 rows.
 
     target_rows [>= k+1][V], draft_rows [>= k][V], tokens [>= k] (ints).
     force: optional {row: bool} that overrides the accept decision of a row
     (the parity harness uses it to follow a counted near-tie flip).
     eos: end-of-sequence token id (< 0: none); cap: most tokens to emit (None:
-    no cap).
+    no cap).  rep: optional (theta, history ids, target dtype, draft dtype):
+    row i's logits get the repetition penalty for history + tokens[:i]
+    (probability drafts are taken as given).
     Returns a dict: accepted (-1 on bad input), tokens (emitted list), status,
     rows (per-row record: p_y, q_y, u, accept, kept masses, and p/q if keep_rows).
     """
@@ -202,12 +242,16 @@ def verify_request(target_rows, draft_rows, tokens, k, T, top_p, draft_kind,
         return bad
     if cap is not None and cap < 1:
         return bad
+    if rep is not None and not (0.0 < float(np.float32(rep[0])) < np.inf):
+        return bad
     for i in range(k + 1):
         if cap is not None and i == cap:           # c accepted drafts emitted: stop
             return dict(accepted=i, tokens=[int(t) for t in tokens[:i]],
                         status=status | ST_CAPPED, rows=rows)
         pos = int(seq_len) + 1 + i
         trow = target_rows[i]
+        if rep is not None:
+            trow = repetition_penalty(trow, list(rep[1]) + [int(t) for t in tokens[:i]], rep[0], rep[2])
         if not row_is_valid(trow, "logits"):
             return bad
         p, pinfo = transform(trow, "logits", T, top_p)
@@ -222,6 +266,8 @@ def verify_request(target_rows, draft_rows, tokens, k, T, top_p, draft_kind,
             return dict(accepted=k, tokens=[int(t) for t in tokens[:k]] + [tok],
                         status=status, rows=rows)
         drow = draft_rows[i]
+        if rep is not None and draft_kind == "logits":
+            drow = repetition_penalty(drow, list(rep[1]) + [int(t) for t in tokens[:i]], rep[0], rep[3])
         y = int(tokens[i])
         if not row_is_valid(drow, draft_kind) or not (0 <= y < V):
             return bad
@@ -262,7 +308,8 @@ def verify_batch(inp: dict, force=None, keep_rows=False):
     inp keys: target [B][kmax+1][V] (bf16 bits or fp32), target_dtype,
     draft [B][kmax][V], draft_dtype, draft_kind ('logits' | 'probs'),
     tokens [B][kmax], k [B], temperature [B], top_p [B], seed, request_id [B],
-    seq_len [B]; optional eos [B] and max_new [B].  force: optional {b: {row: bool}}.
+    seq_len [B]; optional eos [B], max_new [B], and rep_penalty [B] with
+    rep_tokens [B][H] (-1 padded).  force: optional {b: {row: bool}}.
     Returns accepted [B], out_tokens [B][kmax+1] (-1 padded), num_emitted [B],
     status [B] and the per-request records.
     """
@@ -287,7 +334,11 @@ def verify_batch(inp: dict, force=None, keep_rows=False):
                                int(inp["request_id"][b]), int(inp["seq_len"][b]),
                                force=(force or {}).get(b), keep_rows=keep_rows,
                                eos=int(inp["eos"][b]) if inp.get("eos") is not None else -1,
-                               cap=int(inp["max_new"][b]) if inp.get("max_new") is not None else None)
+                               cap=int(inp["max_new"][b]) if inp.get("max_new") is not None else None,
+                               rep=None if inp.get("rep_penalty") is None else
+                               (float(inp["rep_penalty"][b]),
+                                [int(t) for t in inp["rep_tokens"][b] if t >= 0],
+                                inp["target_dtype"], inp["draft_dtype"]))
         accepted[b] = r["accepted"]
         status[b] = r["status"]
         nemit[b] = len(r["tokens"])

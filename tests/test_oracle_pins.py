@@ -411,3 +411,54 @@ def test_eos_and_output_cap():
     r = run(eos=full["tokens"][-1])
     if full["tokens"][-1] not in y.tolist():
         assert r["tokens"] == full["tokens"] and r["status"] == 0
+
+
+def test_repetition_penalty_closed_forms():
+    """Repetition penalty ([SD] sections 4 and 6 name it; the rule is CTRL's):
+    a positive logit is divided by theta, a negative one multiplied.  V = 2
+    rows whose softmax after the penalty has a closed form: logits (ln 3, 0)
+    with theta = 2 give p_0 = sqrt(3) / (1 + sqrt(3)); logits (-ln 2, 0) with
+    theta = 3 give p_0 = (1/8) / (1 + 1/8) = 1/9 (the wrong sign rule gives
+    2^(-1/3) / (1 + 2^(-1/3)) instead)."""
+    def p_row(logits, theta, hist, i=0, dtype="f32"):
+        rows = np.array([logits] * 3, dtype=np.float64)
+        rows = np.asarray(np.float32(rows), np.float64)   # the rows' own fp32 values
+        r = S.verify_request(rows, rows[:2], np.array([1, 1]), 2, 1.0, 1.0, "logits", 5, 0, 10,
+                             keep_rows=True, rep=(theta, hist, dtype, dtype))
+        return r["rows"][i]["p"], r
+
+    p, r = p_row([np.log(3.0), 0.0], 2.0, [0])
+    assert abs(p[0] - np.sqrt(3.0) / (1.0 + np.sqrt(3.0))) < 1e-6
+    p, _ = p_row([-np.log(2.0), 0.0], 3.0, [0])
+    assert abs(p[0] - 1.0 / 9.0) < 1e-6
+    # history ids outside [0, V) and repeats change nothing; theta = 1 is no penalty
+    p1, _ = p_row([np.log(3.0), 0.0], 2.0, [0, 0, 7, -3])
+    assert abs(p1[0] - np.sqrt(3.0) / (1.0 + np.sqrt(3.0))) < 1e-6
+    p, _ = p_row([np.log(3.0), 0.0], 1.0, [0, 1])
+    assert abs(p[0] - 0.75) < 1e-6
+    # the drafts before row i join the penalised set: with no history and
+    # y_0 = 1, row 1 sees logit 0 of token 1 (unchanged by either rule) and
+    # token 0 untouched, so p_0 = 3/4; proposing token 0 first penalises it
+    rows = np.asarray(np.float32([[np.log(3.0), 0.0]] * 3), np.float64)
+    r = S.verify_request(rows, rows[:2], np.array([0, 1]), 2, 1.0, 1.0, "logits", 5, 0, 10,
+                         keep_rows=True, rep=(2.0, [], "f32", "f32"))
+    assert abs(r["rows"][0]["p"][0] - 0.75) < 1e-6
+    assert r["accepted"] == 2                       # q = p on every row
+    assert abs(r["rows"][1]["p"][0] - np.sqrt(3.0) / (1.0 + np.sqrt(3.0))) < 1e-6
+    # the same penalty on both sides keeps q = p: every proposal is accepted
+    rng = np.random.default_rng(41)
+    rows = rng.standard_normal((5, 16)) * 2
+    y = np.array([3, 3, 9, 4])
+    r = S.verify_request(rows, rows[:4], y, 4, 0.8, 1.0, "logits", 5, 2, 10,
+                         rep=(1.7, [3, 4, 11], "f32", "f32"))
+    assert r["accepted"] == 4 and r["tokens"][:4] == y.tolist()
+    # bf16 rows keep the penalised value rounded to bf16 (ties to even):
+    # 2 / 1.3 = 1.53846.. lies between 1.53125 and 1.5390625 (step 2^-7);
+    # -2 * 1.3 = -2.6 between -2.59375 and -2.609375 (step 2^-6)
+    out = S.repetition_penalty(np.array([2.0, -2.0, 0.5]), [0, 1], 1.3, "bf16")
+    assert out.tolist() == [1.5390625, -2.59375, 0.5]
+    # theta must be finite and > 0
+    for bad in (0.0, -1.0, np.inf, np.nan):
+        r = S.verify_request(rows, rows[:4], y, 4, 1.0, 1.0, "logits", 5, 2, 10,
+                             rep=(bad, [], "f32", "f32"))
+        assert r["accepted"] == -1 and r["status"] == S.ST_BAD_INPUT
