@@ -120,6 +120,25 @@ typedef struct {
  *              (SV_ST_CAPPED); a correction or bonus is drawn only while the
  *              cap allows it.  A cap below 1 is bad input.  ([CV] paragraph 5
  *              lists EOS and output caps among the cases to test.)
+ * rep_penalty  [B] fp32 repetition penalty theta_b per request, finite > 0
+ *              (1 = none; anything else makes the request bad input); NULL =
+ *              none.  [SD] s4 ("When it wins") counts repetition penalties
+ *              among the transforms p and q are taken after and s6 requires
+ *              target and draft to apply the same ones; the rule is CTRL's
+ *              (Keskar et al. 2019): the logit l of a penalised token becomes
+ *              l / theta if l > 0, else l * theta, in fp32 (round to nearest),
+ *              rounded back to bf16 (ties to even) in a bf16 row.  Row i's
+ *              penalised set is rep_tokens[b] together with draft_tokens[b][0
+ *              .. i-1]; each token counts once however often it occurs.  Target
+ *              rows and draft LOGIT rows are penalised alike; probability
+ *              drafts are taken as given.
+ * rep_tokens   [B][rep_ld] int32 the request's generated history (or any
+ *              token set to penalise); entries outside [0, V) (e.g. -1
+ *              padding) are ignored.  May be NULL when rep_ld == 0.
+ * rep_ld       row stride of rep_tokens, 0 .. 2^24 (else SV_ERR_INVALID); read
+ *              only when rep_penalty is set.  The inputs are read, never
+ *              written; the penalty costs each CTA one pass over rep_ld + i ids
+ *              per row.
  * Outputs: accepted [B] (a_b in [0, k_b], or -1 when the request's input is
  *   bad), out_tokens [B][kmax+1] (the a_b accepted drafts, then the correction
  *   or bonus token unless EOS or the cap ended the walk, then -1), num_emitted
@@ -155,6 +174,9 @@ typedef struct {
   float* probs_q;
   const int32_t* eos_id;
   const int32_t* max_new;
+  const float* rep_penalty;
+  const int32_t* rep_tokens;
+  int64_t rep_ld;
 } sv_verify_args;
 
 /* Paged block pool: a LIFO free stack plus per-block reference counts

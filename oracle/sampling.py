@@ -302,6 +302,17 @@ def verify_request(target_rows, draft_rows, tokens, k, T, top_p, draft_kind,
     raise AssertionError("unreachable")
 
 
+def request_options(inp: dict, b: int) -> dict:
+    """The optional per-request inputs of request b (EOS id, output cap,
+    repetition penalty) as verify_request keywords."""
+    return dict(
+        eos=int(inp["eos"][b]) if inp.get("eos") is not None else -1,
+        cap=int(inp["max_new"][b]) if inp.get("max_new") is not None else None,
+        rep=None if inp.get("rep_penalty") is None else
+        (float(inp["rep_penalty"][b]), [int(t) for t in inp["rep_tokens"][b]],
+         inp["target_dtype"], inp["draft_dtype"]))
+
+
 def verify_batch(inp: dict, force=None, keep_rows=False):
     """The batched verification step over every request of a workload dict.
 
@@ -333,12 +344,7 @@ def verify_batch(inp: dict, force=None, keep_rows=False):
                                inp["draft_kind"], inp["seed"],
                                int(inp["request_id"][b]), int(inp["seq_len"][b]),
                                force=(force or {}).get(b), keep_rows=keep_rows,
-                               eos=int(inp["eos"][b]) if inp.get("eos") is not None else -1,
-                               cap=int(inp["max_new"][b]) if inp.get("max_new") is not None else None,
-                               rep=None if inp.get("rep_penalty") is None else
-                               (float(inp["rep_penalty"][b]),
-                                [int(t) for t in inp["rep_tokens"][b] if t >= 0],
-                                inp["target_dtype"], inp["draft_dtype"]))
+                               **request_options(inp, b))
         accepted[b] = r["accepted"]
         status[b] = r["status"]
         nemit[b] = len(r["tokens"])

@@ -55,6 +55,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kGroup = 8;  // elements per group (one 16-byte bf16 vector)
 constexpr int kBlk = kThreads * kGroup;  // elements per TMA block (one group per thread)
 constexpr int kMaxBlk = 8;               // blocks per slice: slices hold <= 16384 elements
+constexpr int64_t kMaxRepLd = 1 << 24;  // longest repetition-penalty history per request
 constexpr uint32_t kNoFilter = 0xFFFFFFFFu;
 constexpr int kMaxCluster = 16;
 constexpr int kMaxK = 64;
@@ -99,6 +100,10 @@ struct KParams {
   int spin_limit;
   const int32_t* eos;      // [B] or null
   const int32_t* max_new;  // [B] or null
+  const float* rep_penalty;   // [B] or null
+  const int32_t* rep_tokens;  // [B][rep_ld]
+  int rep_ld;
+  int rep_draft;  // 1: draft rows are logits and take the penalty too
 };
 
 // ---------------------------------------------------------------------------
@@ -300,6 +305,7 @@ struct Ticket {
   float T, top_p, vt, vd;  // vt / vd: target / draft value at the proposed token
   int eos;                 // the request's end-of-sequence id, or -1
   int cap_row;             // 1: accepting this row reaches the output cap
+  float theta;             // repetition penalty (1: none)
 };
 
 // One warp's statistics partial: a = (target max, target sum, draft raw
@@ -330,6 +336,7 @@ struct Smem {
 };
 static_assert(offsetof(Smem, hist) % 16 == 0, "16-byte DSMEM loads of the histograms");
 static_assert(offsetof(Smem, part) % 16 == 0, "16-byte DSMEM loads of the stats partials");
+static_assert(sizeof(Smem::wb) * 8 >= kMaxBlk * kBlk, "the penalty bitmap covers a slice");
 
 enum : int { kDone = 0, kWork = 2 };
 
@@ -1172,6 +1179,35 @@ __device__ __noinline__ void write_probs(float* out, const char* s, const SliceI
 }
 
 // ---------------------------------------------------------------------------
+// Repetition penalty (CTRL's rule): a positive logit is divided by theta, any
+// other multiplied, in fp32 round-to-nearest; a bf16 row keeps the result
+// rounded to bf16, ties to even.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ bool theta_valid(float th) { return th > 0.0f && th <= FLT_MAX; }
+
+template <int EB>
+__device__ __forceinline__ float penalised(float l, float th) {
+  float v = l > 0.0f ? __fdiv_rn(l, th) : __fmul_rn(l, th);
+  if constexpr (EB == 2) {
+    uint16_t h;
+    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(v));
+    v = __uint_as_float((uint32_t)h << 16);
+  }
+  return v;
+}
+
+template <int EB>
+__device__ __forceinline__ void penalise_elem(char* s, int e, float th) {
+  if constexpr (EB == 2) {
+    uint16_t* p = reinterpret_cast<uint16_t*>(s) + e;
+    *p = (uint16_t)(__float_as_uint(penalised<2>(__uint_as_float((uint32_t)*p << 16), th)) >> 16);
+  } else {
+    float* p = reinterpret_cast<float*>(s) + e;
+    *p = penalised<4>(*p, th);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Tickets.  Rows are handed out in (position, request) order by a counter in
 // the workspace.  The control warp of a cluster (rank 0, last warp) takes the
 // next ticket while the current row's loads are in flight, checks it, and
@@ -1181,7 +1217,7 @@ __device__ __noinline__ void write_probs(float* out, const char* s, const SliceI
 template <int EBT, int EBD>
 __device__ void settle_ticket(const KParams& P, Smem& sm, int t, int slot, uint32_t tag) {
   const int lane = threadIdx.x & 31;
-  Ticket tk = {0, kDone, 0, 0, 0, 0u, 0.0f, 1.0f, 0.0f, 0.0f, -1, 0};
+  Ticket tk = {0, kDone, 0, 0, 0, 0u, 0.0f, 1.0f, 0.0f, 0.0f, -1, 0, 1.0f};
   t = __shfl_sync(0xffffffffu, t, 0);
   while (t < P.n_tickets) {
     const int i = t / P.B, b = t - i * P.B;
@@ -1212,6 +1248,9 @@ __device__ void settle_ticket(const KParams& P, Smem& sm, int t, int slot, uint3
       if (lane == 2 && has_d) y = P.tokens[(size_t)b * P.kmax + i];
       if (lane == 3 && P.seq_len) sl = P.seq_len[b];
       if (lane == 4 && P.request_id) rid = P.request_id[b];
+      float th = 1.0f;
+      if (lane == 5 && P.rep_penalty) th = P.rep_penalty[b];
+      th = __shfl_sync(0xffffffffu, th, 5);
       T = __shfl_sync(0xffffffffu, T, 0);
       tp = __shfl_sync(0xffffffffu, tp, 1);
       y = __shfl_sync(0xffffffffu, y, 2);
@@ -1230,8 +1269,20 @@ __device__ void settle_ticket(const KParams& P, Smem& sm, int t, int slot, uint3
       }
       vt = __shfl_sync(0xffffffffu, vt, 0);
       vd = __shfl_sync(0xffffffffu, vd, 1);
+      if (th != 1.0f && theta_valid(th) && has_d && y >= 0 && y < P.V) {
+        // is y in row i's penalised set (the history and the drafts before i)?
+        bool hit = false;
+        const int32_t* h = P.rep_tokens + (size_t)b * P.rep_ld;
+        for (int j = lane; j < P.rep_ld; j += 32) hit |= h[j] == y;
+        for (int j = lane; j < i; j += 32) hit |= P.tokens[(size_t)b * P.kmax + j] == y;
+        if (__any_sync(0xffffffffu, hit)) {
+          vt = penalised<EBT>(vt, th);
+          if (P.rep_draft) vd = penalised<EBD>(vd, th);
+        }
+      }
       const int eos = P.eos ? P.eos[b] : -1;
-      tk = {t, kWork, kb, y, sl + 1 + i, rid, T, tp, vt, vd, eos < 0 ? -1 : eos, cap <= kb && i == cap - 1};
+      tk = {t, kWork, kb, y, sl + 1 + i, rid, T, tp, vt, vd, eos < 0 ? -1 : eos, cap <= kb && i == cap - 1,
+            th};
       break;
     }
     int nt = 0;
@@ -1354,13 +1405,32 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
       }
     }
 
+    // repetition penalty: mark this slice's penalised elements in a bitmap
+    // (one bit per element, so that a token listed twice counts once) while
+    // the slices load; they are rewritten once the loads have landed
+    const float theta = tk.theta;
+    const bool rep = theta != 1.0f && theta_valid(theta) && it.nblk > 0;
+    uint32_t* rmask = reinterpret_cast<uint32_t*>(&sm.wb);
+    if (rep) {
+      for (int j = tid; j < kMaxBlk * kBlk / 32; j += kThreads) rmask[j] = 0u;
+      __syncthreads();
+      const int32_t* h = P.rep_tokens + (size_t)b * P.rep_ld;
+      const int32_t* dt = P.tokens + (size_t)b * P.kmax;
+      for (int j = tid; j < P.rep_ld + i; j += kThreads) {
+        const int x = j < P.rep_ld ? h[j] : dt[j - P.rep_ld];
+        if (x >= it.x0 && x < it.x1)
+          atomicOr(&rmask[(x - it.x0) >> 5], 1u << ((x - it.x0) & 31));
+      }
+    }
+
     const float T = tk.T, top_p = tk.top_p;
     const int y = tk.y, pos = tk.pos;
     const uint32_t rid = tk.rid;
     // the accept uniform depends only on (seed, position, request): draw it
     // while the slices load
     const float u_row = uniform_from_bits(philox4x32_10(make_uint4(0u, (uint32_t)pos, rid, 1u), k0, k1).x);
-    const bool params_ok = (T >= 0.0f) && (T <= FLT_MAX) && (top_p > 0.0f) && (top_p <= 1.0f);
+    const bool params_ok = (T >= 0.0f) && (T <= FLT_MAX) && (top_p > 0.0f) && (top_p <= 1.0f) &&
+                           theta_valid(theta);
     const bool y_ok = !has_d || (y >= 0 && y < P.V);
     const bool greedy = T == 0.0f;
     RowP rt, rd;
@@ -1379,6 +1449,18 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
       if (has_d) landed &= mbar_wait(&sm.bar[1], phase_d, P.err);
       phase_t ^= 1u;
       if (has_d) phase_d ^= 1u;
+    }
+    if (rep) {
+      __syncthreads();  // the bitmap is complete
+      const bool pen_d = has_d && P.rep_draft;
+      for (int w = tid; w < (it.x1 - it.x0 + 31) >> 5; w += kThreads) {
+        for (uint32_t m = rmask[w]; m; m &= m - 1u) {
+          const int e = (w << 5) + __ffs(m) - 1;
+          penalise_elem<EBT>(s_t, e, theta);
+          if (pen_d) penalise_elem<EBD>(s_d, e, theta);
+        }
+      }
+      __syncthreads();
     }
 #pragma unroll
     for (int blk = 0; blk < kMaxBlk; ++blk) {

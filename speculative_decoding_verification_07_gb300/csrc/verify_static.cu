@@ -111,6 +111,8 @@ extern "C" sv_status spec_verify_static(const sv_verify_args* a, sv_stream_t str
       !a->status)
     return SV_ERR_INVALID;
   if (a->kmax > 0 && (!a->draft || !a->draft_tokens)) return SV_ERR_INVALID;
+  if (a->rep_penalty && (a->rep_ld < 0 || a->rep_ld > kMaxRepLd || (a->rep_ld > 0 && !a->rep_tokens)))
+    return SV_ERR_INVALID;
   if (a->target_ld < a->V || (a->target_ld * ebt) % 16 || !aligned16(a->target))
     return SV_ERR_INVALID;
   if (a->kmax > 0 && (a->draft_ld < a->V || (a->draft_ld * ebd) % 16 || !aligned16(a->draft)))
@@ -153,6 +155,9 @@ extern "C" sv_status spec_verify_static(const sv_verify_args* a, sv_stream_t str
   P.slice = slice, P.d_off = d_off, P.n_tickets = (int)rows;
   P.spin_limit = kDefaultSpin;
   P.eos = a->eos_id, P.max_new = a->max_new;
+  P.rep_penalty = a->rep_penalty, P.rep_tokens = a->rep_tokens;
+  P.rep_ld = a->rep_penalty ? (int)a->rep_ld : 0;
+  P.rep_draft = a->draft_kind == SV_DRAFT_LOGITS;
 
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];

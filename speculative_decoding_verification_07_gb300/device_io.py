@@ -40,6 +40,9 @@ def to_device(inp: dict, device="cuda", pin=False) -> dict:
         extra["eos"] = t(inp["eos"], np.int32)
     if inp.get("max_new") is not None:
         extra["max_new"] = t(inp["max_new"], np.int32)
+    if inp.get("rep_penalty") is not None:
+        extra["rep_penalty"] = t(inp["rep_penalty"], np.float32)
+        extra["rep_tokens"] = t(inp["rep_tokens"], np.int32)
     return dict(
         **extra,
         target=rows_to_device(inp["target"], inp["target_dtype"], dev, pin=pin),

@@ -28,7 +28,7 @@ def _oracle_request(inp, b, force=None, keep_rows=False):
     return S.verify_request(tr, dr, inp["tokens"][b, :kb], kb, inp["temperature"][b],
                             inp["top_p"][b], inp["draft_kind"], inp["seed"],
                             int(inp["request_id"][b]), int(inp["seq_len"][b]),
-                            force=force, keep_rows=keep_rows)
+                            force=force, keep_rows=keep_rows, **S.request_options(inp, b))
 
 
 def _tokens(r, kmax):

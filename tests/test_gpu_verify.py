@@ -144,6 +144,84 @@ def test_eos_and_output_caps(ver, V):
     assert (nem[stopped] == acc[stopped]).all()
 
 
+def _add_repetition_penalty(inp, seed, H=300, thetas=(1.0, 1.1, 1.3, 2.0, 0.7)):
+    """A generated history per request: random ids, some of the request's own
+    proposals (so p(y) and q(y) move too), repeats, ids >= V and -1 padding."""
+    rng = np.random.default_rng(seed)
+    B, k = inp["tokens"].shape
+    V = inp["target"].shape[-1]
+    hist = rng.integers(0, V, (B, H)).astype(np.int32)
+    for b in range(B):
+        for i in range(k):
+            if rng.random() < 0.5:
+                hist[b, rng.integers(2, H - 8)] = inp["tokens"][b, i]
+    hist[:, 1] = hist[:, 0]
+    hist[::3, -6] = V + 11
+    hist[:, -5:] = -1
+    inp["rep_tokens"] = hist
+    inp["rep_penalty"] = rng.choice(np.array(thetas, np.float32), B)
+
+
+@pytest.mark.parametrize("name", ["bf16 logits V=128256", "fp32 logits V=1024",
+                                  "fp32 probabilities V=128256", "greedy V=151936"])
+def test_repetition_penalty(ver, name):
+    """Repetition penalty on target and draft logits (CTRL's rule; draft
+    probabilities untouched), with histories that hold the proposals, repeats
+    and ignored ids; two requests with an invalid theta end as bad input."""
+    if name.startswith("bf16"):
+        inp = W.verify_b64_k4()
+    elif name.startswith("fp32 logits"):
+        inp = W.small_fp32(B=48)
+        inp["temperature"][:] = 0.9
+        inp["top_p"][::2] = 0.9
+    elif name.startswith("fp32 prob"):
+        inp = W.ragged_probs(B=32)
+    else:
+        inp = W.greedy_shared(B=32)
+    _add_repetition_penalty(inp, 77)
+    inp["rep_penalty"][3] = 0.0
+    inp["rep_penalty"][5] = np.nan
+    out, dbg, _, _ = run(ver, inp, debug=True)
+    rep = parity.compare(inp, out)
+    report(f"repetition penalty, {name}", rep)
+    st = out["status"].cpu().numpy()
+    assert st[3] == binding.ST_BAD_INPUT and st[5] == binding.ST_BAD_INPUT
+    assert parity.compare_debug(inp, dbg) > 0
+    # the penalty matters: without it some request's outcome differs
+    plain = dict(inp)
+    plain.pop("rep_penalty"), plain.pop("rep_tokens")
+    ref = S.verify_batch(plain)
+    ok = np.ones(len(st), bool)
+    ok[[3, 5]] = False
+    assert (ref["out_tokens"][ok] != out["out_tokens"].cpu().numpy()[ok]).any()
+
+
+def test_repetition_penalty_normalised_rows(ver):
+    """Every row's normalised p and q after the penalty (rows after a rejection
+    processed too), bf16 rows, V = 4093."""
+    inp = W.verify_b64_k4(B=16, V=4093)
+    _add_repetition_penalty(inp, 78, H=64, thetas=(1.5, 3.0))
+    _, _, pp, pq = run(ver, inp, flags=binding.FLAG_NO_SKIP, probs=True)
+    pp, pq = pp.cpu().numpy(), pq.cpu().numpy()
+    checked = 0
+    for b in range(inp["k"].shape[0]):
+        T, tp, th = inp["temperature"][b], inp["top_p"][b], inp["rep_penalty"][b]
+        for i in range(int(inp["k"][b]) + 1):
+            ids = list(inp["rep_tokens"][b]) + list(inp["tokens"][b, :i])
+            row = S.repetition_penalty(S.decode(inp["target"][b, i], "bf16"), ids, th, "bf16")
+            p, info = S.transform(row, "logits", T, tp)
+            if info["margin"] >= parity.TOL:
+                np.testing.assert_allclose(pp[b, i], p, atol=parity.PROB_TOL, rtol=0)
+                checked += 1
+            if i < inp["k"][b]:
+                row = S.repetition_penalty(S.decode(inp["draft"][b, i], "bf16"), ids, th, "bf16")
+                q, info = S.transform(row, "logits", T, tp)
+                if info["margin"] >= parity.TOL:
+                    np.testing.assert_allclose(pq[b, i], q, atol=parity.PROB_TOL, rtol=0)
+                    checked += 1
+    assert checked > 60
+
+
 @pytest.mark.parametrize("top_p", [0.95, 1.0])
 def test_verify_b64_k4(ver, top_p):
     inp = W.verify_b64_k4(top_p=top_p)
