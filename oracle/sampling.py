@@ -23,6 +23,11 @@ Readings taken where the pages leave a step open (each also listed in the design doc)
     distributions"): z = logit / T, or ln(prob) / T for draft probabilities;
     dist = softmax(z).  T = 0 is the limit T -> 0+: uniform over the tied
     maximum set.
+  * top-k (named by [SD] section 4 among the transforms, not defined): set
+    based like top-p; tau_k = the top_k-th largest entry of the transformed
+    distribution (repeats counted), keep every x with dist_x >= tau_k (so
+    ties at tau_k are all kept), renormalise.  Applied before top-p, to p and
+    q alike; top_k <= 0 or >= V means none; no effect at T = 0.
   * top-p: set-based nucleus.  tau = the largest value t with
     sum_{x: dist_x >= t} dist_x >= top_p; keep every x with dist_x >= tau (all
     ties at tau), renormalise.  Applied to p and to q alike; no effect at T = 0.
@@ -162,20 +167,37 @@ def nucleus(dist: np.ndarray, top_p: float):
     return out / out.sum(), kept, tau, float(abs(margin))
 
 
-def transform(row: np.ndarray, kind: str, T: float, top_p: float):
-    """The decoding transform applied identically to target and draft rows.
+def top_k_set(dist: np.ndarray, top_k: int) -> np.ndarray:
+    """Set-based top-k (reading; the pages name top-k without defining it):
+    tau_k = the top_k-th largest entry of dist, repeats counted; keep every x
+    with dist_x >= tau_k (all ties at tau_k) and dist_x > 0."""
+    tau = np.sort(dist)[::-1][top_k - 1]
+    return (dist >= tau) & (dist > 0)
+
+
+def transform(row: np.ndarray, kind: str, T: float, top_p: float, top_k: int = 0):
+    """The decoding transform applied identically to target and draft rows:
+    temperature and softmax, then top-k (0 < top_k < V), then top-p on the
+    renormalised top-k distribution.
 
     Returns (dist, info) where info holds the kept mask and the kept fraction of
-    the pre-filter mass (1 when no top-p filtering happens).
+    the pre-filter mass (1 when nothing is filtered).
     """
     if T == 0.0:
         dist = greedy_limit(row)
         return dist, {"kept": dist > 0, "kept_mass": 1.0, "margin": np.inf}
     dist = softmax_T(row, kind, T)
+    base, kept = dist, dist > 0
+    if 0 < top_k < dist.size:
+        kept = top_k_set(dist, top_k)
+        base = np.where(kept, dist, 0.0)
+        base = base / base.sum()
     if top_p < 1.0:
-        filt, kept, _, margin = nucleus(dist, top_p)
+        filt, kept, _, margin = nucleus(base, top_p)
         return filt, {"kept": kept, "kept_mass": float(dist[kept].sum()), "margin": margin}
-    return dist, {"kept": dist > 0, "kept_mass": 1.0, "margin": np.inf}
+    if base is not dist:
+        return base, {"kept": kept, "kept_mass": float(dist[kept].sum()), "margin": np.inf}
+    return dist, {"kept": kept, "kept_mass": 1.0, "margin": np.inf}
 
 
 # --------------------------------------------------------------------------- #
@@ -216,7 +238,7 @@ def exponential_race(w: np.ndarray, E: np.ndarray) -> int:
 # --------------------------------------------------------------------------- #
 def verify_request(target_rows, draft_rows, tokens, k, T, top_p, draft_kind,
                    seed, request_id, seq_len, force=None, keep_rows=False, eos=-1, cap=None,
-                   rep=None):
+                   rep=None, top_k=0):
     """Run the walk for one request on decoded fp64 rows.
 
     target_rows [>= k+1][V], draft_rows [>= k][V], tokens [>= k] (ints).
@@ -225,7 +247,8 @@ def verify_request(target_rows, draft_rows, tokens, k, T, top_p, draft_kind,
     eos: end-of-sequence token id (< 0: none); cap: most tokens to emit (None:
     no cap).  rep: optional (theta, history ids, target dtype, draft dtype):
     row i's logits get the repetition penalty for history + tokens[:i]
-    (probability drafts are taken as given).
+    (probability drafts are taken as given).  top_k: keep the top_k largest
+    entries of p and of q before top-p (<= 0 or >= V: no top-k).
     Returns a dict: accepted (-1 on bad input), tokens (emitted list), status,
     rows (per-row record: p_y, q_y, u, accept, kept masses, and p/q if keep_rows).
     """
@@ -254,7 +277,7 @@ def verify_request(target_rows, draft_rows, tokens, k, T, top_p, draft_kind,
             trow = repetition_penalty(trow, list(rep[1]) + [int(t) for t in tokens[:i]], rep[0], rep[2])
         if not row_is_valid(trow, "logits"):
             return bad
-        p, pinfo = transform(trow, "logits", T, top_p)
+        p, pinfo = transform(trow, "logits", T, top_p, top_k)
         rec = {"pos": pos, "p_kept_mass": pinfo["kept_mass"], "p_margin": pinfo["margin"]}
         if keep_rows:
             rec["p"] = p
@@ -271,7 +294,7 @@ def verify_request(target_rows, draft_rows, tokens, k, T, top_p, draft_kind,
         y = int(tokens[i])
         if not row_is_valid(drow, draft_kind) or not (0 <= y < V):
             return bad
-        q, qinfo = transform(drow, draft_kind, T, top_p)
+        q, qinfo = transform(drow, draft_kind, T, top_p, top_k)
         u = philox.accept_uniform(seed, request_id, pos)
         rec.update(q_kept_mass=qinfo["kept_mass"], q_margin=qinfo["margin"],
                    p_y=float(p[y]), q_y=float(q[y]), u=u)
@@ -303,9 +326,10 @@ def verify_request(target_rows, draft_rows, tokens, k, T, top_p, draft_kind,
 
 
 def request_options(inp: dict, b: int) -> dict:
-    """The optional per-request inputs of request b (EOS id, output cap,
-    repetition penalty) as verify_request keywords."""
+    """The optional per-request inputs of request b (top-k, EOS id, output
+    cap, repetition penalty) as verify_request keywords."""
     return dict(
+        top_k=int(inp["top_k"][b]) if inp.get("top_k") is not None else 0,
         eos=int(inp["eos"][b]) if inp.get("eos") is not None else -1,
         cap=int(inp["max_new"][b]) if inp.get("max_new") is not None else None,
         rep=None if inp.get("rep_penalty") is None else
@@ -319,7 +343,7 @@ def verify_batch(inp: dict, force=None, keep_rows=False):
     inp keys: target [B][kmax+1][V] (bf16 bits or fp32), target_dtype,
     draft [B][kmax][V], draft_dtype, draft_kind ('logits' | 'probs'),
     tokens [B][kmax], k [B], temperature [B], top_p [B], seed, request_id [B],
-    seq_len [B]; optional eos [B], max_new [B], and rep_penalty [B] with
+    seq_len [B]; optional top_k [B], eos [B], max_new [B], and rep_penalty [B] with
     rep_tokens [B][H] (-1 padded).  force: optional {b: {row: bool}}.
     Returns accepted [B], out_tokens [B][kmax+1] (-1 padded), num_emitted [B],
     status [B] and the per-request records.

@@ -462,3 +462,55 @@ def test_repetition_penalty_closed_forms():
         r = S.verify_request(rows, rows[:4], y, 4, 1.0, 1.0, "logits", 5, 2, 10,
                              rep=(bad, [], "f32", "f32"))
         assert r["accepted"] == -1 and r["status"] == S.ST_BAD_INPUT
+
+
+def test_top_k_against_brute_force_and_closed_forms():
+    """Top-k ([SD] section 4 names it; set-based reading): x is kept iff fewer
+    than top_k entries are strictly larger than dist_x (a characterisation
+    independent of the sort in the oracle), checked by brute force on small
+    rows with many ties; top_k = 1 equals the greedy limit at any T > 0;
+    top-k applies before top-p (a hand example where the order matters)."""
+    rng = np.random.default_rng(43)
+    for _ in range(300):
+        V = int(rng.integers(2, 9))
+        row = rng.integers(-3, 3, V).astype(np.float64)       # many ties
+        tk = int(rng.integers(1, V))
+        d, info = S.transform(row, "logits", 1.0, 1.0, tk)
+        dist = S.softmax_T(row, "logits", 1.0)
+        keep = np.array([(dist > dist[x]).sum() < tk for x in range(V)])
+        assert (info["kept"] == keep).all()
+        want = np.where(keep, dist, 0.0)
+        np.testing.assert_allclose(d, want / want.sum(), rtol=0, atol=1e-15)
+        assert abs(info["kept_mass"] - dist[keep].sum()) < 1e-15
+        # top_k = 1: the tied maxima, uniformly
+        d1, _ = S.transform(row, "logits", 0.7, 1.0, 1)
+        np.testing.assert_allclose(d1, S.greedy_limit(row), rtol=0, atol=1e-15)
+        # top_k <= 0 and top_k >= V filter nothing
+        for off in (0, -1, V, V + 3):
+            np.testing.assert_allclose(S.transform(row, "logits", 1.0, 1.0, off)[0], dist)
+    # q = (0.4, 0.3, 0.2, 0.1), top_k = 3 then top_p = 0.75: the renormalised
+    # top-3 masses 4/9, 3/9, 2/9 reach 0.75 after two entries -> (4/7, 3/7);
+    # top-p first would keep three entries
+    q = np.array([0.4, 0.3, 0.2, 0.1])
+    d, info = S.transform(q, "probs", 1.0, 0.75, 3)
+    np.testing.assert_allclose(d, [4 / 7, 3 / 7, 0.0, 0.0], rtol=0, atol=1e-15)
+    assert abs(info["kept_mass"] - 0.7) < 1e-15
+    d, _ = S.transform(q, "probs", 1.0, 0.75, 0)
+    np.testing.assert_allclose(d, [4 / 9, 3 / 9, 2 / 9, 0.0], rtol=0, atol=1e-15)
+    # at T = 0 top-k changes nothing
+    row = np.array([1.0, 3.0, 3.0, 2.0])
+    np.testing.assert_allclose(S.transform(row, "logits", 0.0, 1.0, 1)[0], [0, 0.5, 0.5, 0])
+
+
+def test_top_k_walk_q_equals_p():
+    """With q = p after the same top-k on both sides every proposal inside the
+    top-k set is accepted, and a proposal outside it has q(y) = 0."""
+    rng = np.random.default_rng(44)
+    rows = rng.standard_normal((4, 12))
+    order = np.argsort(-rows[0])
+    y = np.array([order[0], order[1], order[2]])
+    r = S.verify_request(rows, rows[:3], y, 3, 1.0, 1.0, "logits", 1, 0, 5, top_k=12 - 1)
+    assert r["accepted"] == 3
+    y_out = np.array([order[5], order[1], order[2]])               # rank 6 of row 0
+    r = S.verify_request(rows, rows[:3], y_out, 3, 1.0, 1.0, "logits", 1, 0, 5, top_k=3)
+    assert r["rows"][0]["q_y"] == 0.0 and r["status"] & S.ST_Q_ZERO
