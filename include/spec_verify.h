@@ -139,6 +139,14 @@ typedef struct {
  *              only when rep_penalty is set.  The inputs are read, never
  *              written; the penalty costs each CTA one pass over rep_ld + i ids
  *              per row.
+ * top_k        [B] int32; NULL = none.  0 < top_k_b < V keeps, in p and in q,
+ *              every token whose transformed probability is at least the
+ *              top_k_b-th largest one (repeats counted, so ties at that value
+ *              are all kept), renormalised; top-p then applies to the
+ *              renormalised top-k distribution.  Any other value: no top-k.
+ *              No effect at T = 0.  ([SD] s4 names top-k among the transforms
+ *              p and q are taken after; the set-based reading is this
+ *              library's.)
  * Outputs: accepted [B] (a_b in [0, k_b], or -1 when the request's input is
  *   bad), out_tokens [B][kmax+1] (the a_b accepted drafts, then the correction
  *   or bonus token unless EOS or the cap ended the walk, then -1), num_emitted
@@ -177,6 +185,7 @@ typedef struct {
   const float* rep_penalty;
   const int32_t* rep_tokens;
   int64_t rep_ld;
+  const int32_t* top_k;
 } sv_verify_args;
 
 /* Paged block pool: a LIFO free stack plus per-block reference counts

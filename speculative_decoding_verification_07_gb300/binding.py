@@ -68,7 +68,8 @@ class SvVerifyArgs(ctypes.Structure):
                 ("accepted", c_void_p), ("out_tokens", c_void_p), ("num_emitted", c_void_p),
                 ("status", c_void_p), ("debug", c_void_p), ("probs_p", c_void_p),
                 ("probs_q", c_void_p), ("eos_id", c_void_p), ("max_new", c_void_p),
-                ("rep_penalty", c_void_p), ("rep_tokens", c_void_p), ("rep_ld", c_int64)]
+                ("rep_penalty", c_void_p), ("rep_tokens", c_void_p), ("rep_ld", c_int64),
+                ("top_k", c_void_p)]
 
 
 class BflState(ctypes.Structure):
@@ -176,7 +177,7 @@ def sv_destroy(handle) -> None:
 def make_args(*, target, draft, draft_tokens, temperature, accepted, out_tokens, num_emitted,
               status, V=None, k=None, top_p=None, seed=0, request_id=None, seq_len=None,
               draft_kind="logits", flags=0, debug=None, probs_p=None, probs_q=None,
-              eos=None, max_new=None, rep_penalty=None, rep_tokens=None):
+              eos=None, max_new=None, rep_penalty=None, rep_tokens=None, top_k=None):
     B, rows, _ = target.shape
     kmax = rows - 1
     a = SvVerifyArgs()
@@ -194,7 +195,7 @@ def make_args(*, target, draft, draft_tokens, temperature, accepted, out_tokens,
     a.num_emitted, a.status = _ptr(num_emitted), _ptr(status)
     a.debug, a.probs_p, a.probs_q = _ptr(debug), _ptr(probs_p), _ptr(probs_q)
     a.eos_id, a.max_new = _ptr(eos), _ptr(max_new)
-    a.rep_penalty = _ptr(rep_penalty)
+    a.rep_penalty, a.top_k = _ptr(rep_penalty), _ptr(top_k)
     if rep_tokens is not None:
         if rep_tokens.dim() != 2 or rep_tokens.stride(1) != 1:
             raise ValueError("rep_tokens must be [B][H] with unit stride along H")

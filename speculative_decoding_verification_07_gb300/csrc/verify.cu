@@ -11,18 +11,24 @@ namespace sv {
 // host side
 // ---------------------------------------------------------------------------
 struct Variant {
-  KernelFn fn;
+  KernelFn fn, fn_topk;
   int eb_t, eb_d;
   bool probs;
 };
 
 static const Variant kVariants[] = {
-    {kernel_bf16_bf16_logits(), 2, 2, false},  // bf16 target, bf16 draft logits
-    {kernel_bf16_f32_probs(), 2, 4, true},     // bf16 target, fp32 draft probabilities
-    {kernel_bf16_f32_logits(), 2, 4, false},   // bf16 target, fp32 draft logits
-    {kernel_f32_f32_logits(), 4, 4, false},    // fp32 target, fp32 draft logits
-    {kernel_f32_f32_probs(), 4, 4, true},      // fp32 target, fp32 draft probabilities
-    {kernel_f32_bf16_logits(), 4, 2, false},   // fp32 target, bf16 draft logits
+    // bf16 target, bf16 draft logits
+    {kernel_bf16_bf16_logits(), kernel_bf16_bf16_logits_topk(), 2, 2, false},
+    // bf16 target, fp32 draft probabilities
+    {kernel_bf16_f32_probs(), kernel_bf16_f32_probs_topk(), 2, 4, true},
+    // bf16 target, fp32 draft logits
+    {kernel_bf16_f32_logits(), kernel_bf16_f32_logits_topk(), 2, 4, false},
+    // fp32 target, fp32 draft logits
+    {kernel_f32_f32_logits(), kernel_f32_f32_logits_topk(), 4, 4, false},
+    // fp32 target, fp32 draft probabilities
+    {kernel_f32_f32_probs(), kernel_f32_f32_probs_topk(), 4, 4, true},
+    // fp32 target, bf16 draft logits
+    {kernel_f32_bf16_logits(), kernel_f32_bf16_logits_topk(), 4, 2, false},
 };
 
 static int elem_bytes(int dt) { return dt == SV_BF16 ? 2 : 4; }
@@ -76,6 +82,7 @@ extern "C" sv_status spec_verify(sv_handle* h, const sv_verify_args* a, void* ws
   for (const Variant& v : kVariants)
     if (v.eb_t == ebt && v.eb_d == ebd && v.probs == probs) var = &v;
   if (!var) return SV_ERR_UNSUPPORTED;
+  const KernelFn fn = a->top_k ? var->fn_topk : var->fn;
 
   // Cluster size: smallest power of two whose slices fit kMaxBlk TMA blocks,
   // then grown while the grid would leave SMs idle.
@@ -105,6 +112,7 @@ extern "C" sv_status spec_verify(sv_handle* h, const sv_verify_args* a, void* ws
   P.slice = slice, P.d_off = d_off, P.n_tickets = (int)n_tickets;
   P.spin_limit = kDefaultSpin;
   P.eos = a->eos_id, P.max_new = a->max_new;
+  P.top_k = a->top_k;
   P.rep_penalty = a->rep_penalty, P.rep_tokens = a->rep_tokens;
   P.rep_ld = a->rep_penalty ? (int)a->rep_ld : 0;
   P.rep_draft = a->draft_kind == SV_DRAFT_LOGITS;
@@ -122,22 +130,22 @@ extern "C" sv_status spec_verify(sv_handle* h, const sv_verify_args* a, void* ws
   cfg.stream = (cudaStream_t)stream;
   int max_clusters = 0;
   for (int i = 0; i < h->occ_n; ++i)
-    if (h->occ_fn[i] == (const void*)var->fn && h->occ_c[i] == C && h->occ_smem[i] == dyn)
+    if (h->occ_fn[i] == (const void*)fn && h->occ_c[i] == C && h->occ_smem[i] == dyn)
       max_clusters = h->occ_val[i];
   // the attribute is per function: set it for every launch (other shapes may
   // have lowered it since the occupancy of this shape was cached)
-  SV_CUDA_TRY(cudaFuncSetAttribute(var->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
+  SV_CUDA_TRY(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
   if (max_clusters == 0) {
     if (C > 8)
-      SV_CUDA_TRY(cudaFuncSetAttribute(var->fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
+      SV_CUDA_TRY(cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
     cfg.gridDim = dim3((unsigned)C);
-    if (cudaOccupancyMaxActiveClusters(&max_clusters, var->fn, &cfg) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, fn, &cfg) != cudaSuccess ||
         max_clusters < 1) {
       (void)cudaGetLastError();
       return SV_ERR_UNSUPPORTED;
     }
     if (h->occ_n < sv_handle::kCache) {
-      h->occ_fn[h->occ_n] = (const void*)var->fn;
+      h->occ_fn[h->occ_n] = (const void*)fn;
       h->occ_c[h->occ_n] = C;
       h->occ_smem[h->occ_n] = dyn;
       h->occ_val[h->occ_n] = max_clusters;
@@ -146,7 +154,7 @@ extern "C" sv_status spec_verify(sv_handle* h, const sv_verify_args* a, void* ws
   }
   const size_t nclusters = rows < (size_t)max_clusters ? rows : (size_t)max_clusters;
   cfg.gridDim = dim3((unsigned)(nclusters * C));
-  if (cudaLaunchKernelEx(&cfg, var->fn, P) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, fn, P) != cudaSuccess) {
     (void)cudaGetLastError();
     return SV_ERR_CUDA;
   }

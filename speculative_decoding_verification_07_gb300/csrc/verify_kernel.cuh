@@ -100,6 +100,7 @@ struct KParams {
   int spin_limit;
   const int32_t* eos;      // [B] or null
   const int32_t* max_new;  // [B] or null
+  const int32_t* top_k;       // [B] or null
   const float* rep_penalty;   // [B] or null
   const int32_t* rep_tokens;  // [B][rep_ld]
   int rep_ld;
@@ -284,7 +285,7 @@ struct TopLv {
   uint32_t lo;  // distance offset of the current level's bin 0
   int shift;    // bin width 2^shift (0: exact keys)
   float above;  // mass of bins above the current range
-  float R;      // target mass top_p * S
+  float R;      // target: mass top_p * S, or a count (top-k)
   int window;   // the current level is the exact bf16 count window
   int done;
   int guess;    // the window floor is the guessed one (a miss retries with the bound)
@@ -306,6 +307,7 @@ struct Ticket {
   int eos;                 // the request's end-of-sequence id, or -1
   int cap_row;             // 1: accepting this row reaches the output cap
   float theta;             // repetition penalty (1: none)
+  int top_k;               // <= 0: none
 };
 
 // One warp's statistics partial: a = (target max, target sum, draft raw
@@ -720,9 +722,9 @@ __device__ __forceinline__ void window_row_bf16(const char* s, const SliceIter& 
 // so together they hold at most half the excluded mass and the boundary lies
 // at or above v_lo.  With n = V this is a bound; clamped to the 256-bin window
 // below kmax.
-__device__ __forceinline__ uint32_t window_lo_key(const RowP& r, float top_p, int n) {
+__device__ __forceinline__ uint32_t window_lo_key_x(const RowP& r, float excl, int n) {
   const uint32_t floor_key = r.kmax >= 255u ? r.kmax - 255u : 0u;
-  const float wlo = (1.0f - top_p) * r.S / (2.0f * (float)n);
+  const float wlo = excl / (2.0f * (float)n);
   if (!(wlo > 0.0f)) return floor_key;
   const float vlo = r.m + lg2(wlo) / r.c - 1.0f / r.c;  // one log2 unit of slack
   if (!(vlo > -FLT_MAX)) return floor_key;
@@ -732,9 +734,14 @@ __device__ __forceinline__ uint32_t window_lo_key(const RowP& r, float top_p, in
   return k > floor_key ? k : floor_key;
 }
 
+// The same with the excluded mass (1 - top_p) S of a plain top-p row.
+__device__ __forceinline__ uint32_t window_lo_key(const RowP& r, float top_p, int n) {
+  return window_lo_key_x(r, (1.0f - top_p) * r.S, n);
+}
+
 // General histogram level: every element whose distance D lies in
-// [lo, lo + 256 << shift) adds its weight to bin (D - lo) >> shift.
-template <int EB, bool PROBS>
+// [lo, lo + 256 << shift) adds its weight (top-k: 1) to bin (D - lo) >> shift.
+template <int EB, bool PROBS, bool CNT>
 __device__ __forceinline__ void level_group(const Grp<EB>& g, const RowP& r, uint32_t lo, int shift,
                                             uint32_t* hist) {
   const uint32_t span = shift >= 24 ? 0xFFFFFFFFu : ((256u << shift) - 1u);
@@ -744,7 +751,7 @@ __device__ __forceinline__ void level_group(const Grp<EB>& g, const RowP& r, uin
     const uint32_t D = r.kmax - vkey<EB>(v);
     const uint32_t u = D - lo;
     if (D >= lo && u <= span && v > (PROBS ? 0.0f : -INFINITY))
-      atomicAdd(reinterpret_cast<float*>(&hist[u >> shift]), weight<PROBS>(v, r));
+      atomicAdd(reinterpret_cast<float*>(&hist[u >> shift]), CNT ? 1.0f : weight<PROBS>(v, r));
   }
 }
 
@@ -752,7 +759,7 @@ __device__ __forceinline__ void level_group(const Grp<EB>& g, const RowP& r, uin
 // histograms (lane l owns bins 8l .. 8l+7; the remote loads of four ranks
 // are in flight together), scans them in the warp, and picks the boundary bin.  Every CTA
 // runs the same arithmetic on the same data, so all reach the same result.
-template <int EB, bool PROBS>
+template <int EB, bool PROBS, bool CNT>
 __device__ __forceinline__ void resolve_level(cg::cluster_group& cluster, const uint32_t* hist, int C,
                                               TopLv& lv, RowP& r) {
   const int lane = threadIdx.x & 31;
@@ -780,7 +787,7 @@ __device__ __forceinline__ void resolve_level(cg::cluster_group& cluster, const 
       }
     }
   }
-  if (lv.window) {
+  if (lv.window && !CNT) {  // counts to weights (top-k keeps the counts)
 #pragma unroll
     for (int k = 0; k < 8; ++k)
       h[k] = h[k] > 0.0f ? h[k] * weight<PROBS>(vkey_value<2>(r.kmax - (uint32_t)(8 * lane + k)), r) : 0.0f;
@@ -847,18 +854,24 @@ __device__ __forceinline__ void resolve_level(cg::cluster_group& cluster, const 
 }
 
 // Top-p threshold of the target row and (if has_d) the draft row held in
-// shared memory across the cluster.  Sets Dstar, Z, invZ, vstar.  All control
-// flow depends only on cluster-reduced values, so every CTA takes the same path.
-template <int EBT, int EBD, bool PROBS>
+// shared memory across the cluster: the largest boundary whose kept mass
+// reaches Rt / Rd (a window floor may assume the rows exclude at least Xt / Xd
+// of their mass).  With cnt the targets are a count instead (top-k: the
+// boundary keeps at least that many elements) and the kept mass is summed
+// afterwards.  Sets Dstar, Z, invZ, vstar.  All control flow depends only on
+// cluster-reduced values, so every CTA takes the same path.
+template <int EBT, int EBD, bool PROBS, bool CNT>
 __device__ __noinline__ void top_p_rows(cg::cluster_group& cluster, Smem& sm, const char* st,
                                         const char* sd, const SliceIter& it, bool has_d,
-                                        float top_p, RowP& rt, RowP& rd, bool pre_t, bool pre_d) {
+                                        float Rt, float Rd, float Xt, float Xd,
+                                        RowP& rt, RowP& rd, bool pre_t, bool pre_d) {
   const int C = cluster.num_blocks();
   const int tid = threadIdx.x;
+  constexpr bool cnt = CNT;
   TopLv L[2];
-  L[0] = {0u, EBT == 2 ? 0 : 24, 0.0f, top_p * rt.S, EBT == 2, 0, EBT == 2, EBT != 2};
-  L[1] = {0u, EBD == 2 ? 0 : 24, 0.0f, top_p * rd.S, EBD == 2 && !PROBS, !has_d,
-          EBD == 2 && !PROBS, !(EBD == 2 && !PROBS)};
+  L[0] = {0u, EBT == 2 ? 0 : 24, 0.0f, Rt, EBT == 2, 0, EBT == 2 && !cnt, EBT != 2};
+  L[1] = {0u, EBD == 2 ? 0 : 24, 0.0f, Rd, EBD == 2 && !PROBS, !has_d,
+          EBD == 2 && !PROBS && !cnt, !(EBD == 2 && !PROBS)};
   // window floors as distances below the row maxima (bf16 rows only)
   uint32_t lo_t = 255u, lo_d = 255u;
   // The first floor assumes at most kWindowGuess elements below the boundary
@@ -874,9 +887,13 @@ __device__ __noinline__ void top_p_rows(cg::cluster_group& cluster, Smem& sm, co
     const bool bt = !L[0].done && !(first && pre_t);  // rows counted in this round
     const bool bd = !L[1].done && !(first && pre_d);
     if (bt || bd) {
-    if constexpr (EBT == 2) lo_t = rt.kmax - window_lo_key(rt, top_p, L[0].guess ? nguess : it.V);
+    // (top-k: the whole 256-value window below the maximum)
+    if constexpr (EBT == 2)
+      lo_t = rt.kmax - (cnt ? (rt.kmax >= 255u ? rt.kmax - 255u : 0u)
+                            : window_lo_key_x(rt, Xt, L[0].guess ? nguess : it.V));
     if constexpr (EBD == 2 && !PROBS)
-      lo_d = rd.kmax - window_lo_key(rd, top_p, L[1].guess ? nguess : it.V);
+      lo_d = rd.kmax - (cnt ? (rd.kmax >= 255u ? rd.kmax - 255u : 0u)
+                            : window_lo_key_x(rd, Xd, L[1].guess ? nguess : it.V));
     if (bt) for (int j = tid; j < 256; j += kThreads) sm.hist[buf][0][j] = 0u;
     if (bd) for (int j = tid; j < 256; j += kThreads) sm.hist[buf][1][j] = 0u;
     __syncthreads();
@@ -898,12 +915,12 @@ __device__ __noinline__ void top_p_rows(cg::cluster_group& cluster, Smem& sm, co
         if (gen_t) {
           Grp<EBT> g;
           lds_group<EBT, false>(g, st, it.x0, x, it.x1);
-          level_group<EBT, false>(g, rt, L[0].lo, L[0].shift, sm.hist[buf][0]);
+          level_group<EBT, false, CNT>(g, rt, L[0].lo, L[0].shift, sm.hist[buf][0]);
         }
         if (gen_d) {
           Grp<EBD> g;
           lds_group<EBD, PROBS>(g, sd, it.x0, x, it.x1);
-          level_group<EBD, PROBS>(g, rd, L[1].lo, L[1].shift, sm.hist[buf][1]);
+          level_group<EBD, PROBS, CNT>(g, rd, L[1].lo, L[1].shift, sm.hist[buf][1]);
         }
       }
     }
@@ -914,11 +931,11 @@ __device__ __noinline__ void top_p_rows(cg::cluster_group& cluster, Smem& sm, co
     // publishes both results to the whole CTA
     const int warp = tid >> 5;
     if (warp == 0 && !L[0].done) {
-      resolve_level<EBT, false>(cluster, &sm.hist[buf][0][0], C, L[0], rt);
+      resolve_level<EBT, false, CNT>(cluster, &sm.hist[buf][0][0], C, L[0], rt);
       if ((tid & 31) == 0) sm.lv[0] = L[0], sm.rres[0] = {rt.Dstar, rt.Z, rt.invZ, rt.vstar};
     }
     if (warp == 1 && !L[1].done) {
-      resolve_level<EBD, PROBS>(cluster, &sm.hist[buf][1][0], C, L[1], rd);
+      resolve_level<EBD, PROBS, CNT>(cluster, &sm.hist[buf][1][0], C, L[1], rd);
       if ((tid & 31) == 0) sm.lv[1] = L[1], sm.rres[1] = {rd.Dstar, rd.Z, rd.invZ, rd.vstar};
     }
     __syncthreads();
@@ -936,8 +953,9 @@ __device__ __noinline__ void top_p_rows(cg::cluster_group& cluster, Smem& sm, co
   // A boundary from the radix descent comes with a kept mass summed by float
   // atomics, whose rounding grows with the number of elements sharing a bin
   // (a plateau of tied values).  Recompute it as per-thread sums reduced in a
-  // fixed order across the cluster, as the row sum S is.
-  const bool fix_t = L[0].radix, fix_d = has_d && L[1].radix;
+  // fixed order across the cluster, as the row sum S is.  A top-k boundary
+  // comes with a count only: its mass is summed the same way.
+  const bool fix_t = L[0].radix || cnt, fix_d = has_d && (L[1].radix || cnt);
   if (fix_t || fix_d) {
     float zt = 0.0f, zd = 0.0f;
 #pragma unroll 1
@@ -989,6 +1007,35 @@ __device__ __noinline__ void top_p_rows(cg::cluster_group& cluster, Smem& sm, co
     if (fix_t) rt.Z = sm.kz_all[0], rt.invZ = 1.0f / rt.Z;
     if (fix_d) rd.Z = sm.kz_all[1], rd.invZ = 1.0f / rd.Z;
     cluster.sync();  // peers are done reading kz before it can be rewritten
+  }
+}
+
+// The row filters: top-k (top_k > 0) and then top-p on the renormalised
+// top-k rows, or top-p alone.  One call site in the row loop keeps the loop's
+// register allocation independent of the filters.
+template <int EBT, int EBD, bool PROBS>
+__device__ __noinline__ void filter_rows(cg::cluster_group& cluster, Smem& sm, const char* st,
+                                         const char* sd, const SliceIter& it, bool has_d, float top_p,
+                                         int top_k, RowP& rt, RowP& rd, bool pre_t, bool pre_d) {
+  if (top_k <= 0) {
+    top_p_rows<EBT, EBD, PROBS, false>(cluster, sm, st, sd, it, has_d, top_p * rt.S, top_p * rd.S,
+                                       (1.0f - top_p) * rt.S, (1.0f - top_p) * rd.S, rt, rd, pre_t,
+                                       pre_d);
+    return;
+  }
+  const float K = (float)top_k;
+  top_p_rows<EBT, EBD, PROBS, true>(cluster, sm, st, sd, it, has_d, K, K, 0.0f, 0.0f, rt, rd, false,
+                                    false);
+  if (top_p < 1.0f) {
+    // the boundary keeps top_p of the top-k mass, so it lies at or above the
+    // top-k boundary (rounding aside: then the top-k boundary stands)
+    const RowRes kt = {rt.Dstar, rt.Z, rt.invZ, rt.vstar}, kd = {rd.Dstar, rd.Z, rd.invZ, rd.vstar};
+    const float Rt = top_p * kt.Z, Rd = top_p * kd.Z;
+    top_p_rows<EBT, EBD, PROBS, false>(cluster, sm, st, sd, it, has_d, Rt, Rd, rt.S - Rt, rd.S - Rd,
+                                       rt, rd, false, false);
+    if (rt.Dstar > kt.Dstar) rt.Dstar = kt.Dstar, rt.Z = kt.Z, rt.invZ = kt.invZ, rt.vstar = kt.vstar;
+    if (has_d && rd.Dstar > kd.Dstar)
+      rd.Dstar = kd.Dstar, rd.Z = kd.Z, rd.invZ = kd.invZ, rd.vstar = kd.vstar;
   }
 }
 
@@ -1217,7 +1264,7 @@ __device__ __forceinline__ void penalise_elem(char* s, int e, float th) {
 template <int EBT, int EBD>
 __device__ void settle_ticket(const KParams& P, Smem& sm, int t, int slot, uint32_t tag) {
   const int lane = threadIdx.x & 31;
-  Ticket tk = {0, kDone, 0, 0, 0, 0u, 0.0f, 1.0f, 0.0f, 0.0f, -1, 0, 1.0f};
+  Ticket tk = {0, kDone, 0, 0, 0, 0u, 0.0f, 1.0f, 0.0f, 0.0f, -1, 0, 1.0f, 0};
   t = __shfl_sync(0xffffffffu, t, 0);
   while (t < P.n_tickets) {
     const int i = t / P.B, b = t - i * P.B;
@@ -1251,6 +1298,9 @@ __device__ void settle_ticket(const KParams& P, Smem& sm, int t, int slot, uint3
       float th = 1.0f;
       if (lane == 5 && P.rep_penalty) th = P.rep_penalty[b];
       th = __shfl_sync(0xffffffffu, th, 5);
+      int tkk = 0;
+      if (lane == 6 && P.top_k) tkk = P.top_k[b];
+      tkk = __shfl_sync(0xffffffffu, tkk, 6);
       T = __shfl_sync(0xffffffffu, T, 0);
       tp = __shfl_sync(0xffffffffu, tp, 1);
       y = __shfl_sync(0xffffffffu, y, 2);
@@ -1282,7 +1332,7 @@ __device__ void settle_ticket(const KParams& P, Smem& sm, int t, int slot, uint3
       }
       const int eos = P.eos ? P.eos[b] : -1;
       tk = {t, kWork, kb, y, sl + 1 + i, rid, T, tp, vt, vd, eos < 0 ? -1 : eos, cap <= kb && i == cap - 1,
-            th};
+            th, tkk};
       break;
     }
     int nt = 0;
@@ -1341,7 +1391,7 @@ __device__ __forceinline__ int warp_wait_earlier(const KParams& P, int b, int i,
 // (target row i and draft row i of request b) at a time, every CTA on its
 // slice of both rows in shared memory.
 // ---------------------------------------------------------------------------
-template <int EBT, int EBD, bool PROBS>
+template <int EBT, int EBD, bool PROBS, bool TOPK>
 __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
   cg::cluster_group cluster = cg::this_cluster();
   __shared__ Smem sm;
@@ -1482,7 +1532,10 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
     const float mt = rmt;
     const float md = (PROBS && !greedy) ? (rmd > 0.0f ? lg2(rmd) * rd.invT : -INFINITY) : rmd;
     // bf16 logit rows with top_p < 1 count their top-p window during sweep 2
-    const bool topp = !greedy && top_p < 1.0f && params_ok;
+    // top-k (0 < top_k < V) runs before top-p; its rows count no prebuilt
+    // top-p window (the top-p target depends on the top-k mass)
+    const bool topk = TOPK && !greedy && params_ok && tk.top_k > 0 && tk.top_k < P.V;
+    const bool topp = !greedy && top_p < 1.0f && params_ok && !topk;
     const bool win_t = EBT == 2 && topp;
     const bool win_d = EBD == 2 && !PROBS && topp && has_d;
     if (win_t || win_d)
@@ -1629,8 +1682,9 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
     }
 
     // ---------------------------------------------------------------- top-p
-    if (!row_bad && !greedy && top_p < 1.0f)
-      top_p_rows<EBT, EBD, PROBS>(cluster, sm, s_t, s_d, it, has_d, top_p, rt, rd, win_t, win_d);
+    if (!row_bad && (topk || (!greedy && top_p < 1.0f)))
+      filter_rows<EBT, EBD, PROBS>(cluster, sm, s_t, s_d, it, has_d, top_p, topk ? tk.top_k : 0, rt, rd,
+                                   win_t, win_d);
 
     // ---------------------------------------------------------- accept test
     // Every CTA evaluates the test identically from the same values.
@@ -1760,12 +1814,21 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
 using KernelFn = void (*)(KParams);
 
 // One getter per translation unit that instantiates kernel variants.
+// The _topk variants also run the top-k filter; the others never do (the
+// filter's code in the row loop costs the plain variants about 2% of their
+// time, so a call without top_k runs a variant without it).
 KernelFn kernel_bf16_bf16_logits();
 KernelFn kernel_bf16_f32_probs();
 KernelFn kernel_bf16_f32_logits();
 KernelFn kernel_f32_f32_logits();
 KernelFn kernel_f32_f32_probs();
 KernelFn kernel_f32_bf16_logits();
+KernelFn kernel_bf16_bf16_logits_topk();
+KernelFn kernel_bf16_f32_probs_topk();
+KernelFn kernel_bf16_f32_logits_topk();
+KernelFn kernel_f32_f32_logits_topk();
+KernelFn kernel_f32_f32_probs_topk();
+KernelFn kernel_f32_bf16_logits_topk();
 
 size_t workspace_bytes_for(int B, int kmax);
 

@@ -2,6 +2,6 @@
 #include "verify_kernel.cuh"
 
 namespace sv {
-KernelFn kernel_bf16_f32_probs() { return &verify_kernel<2, 4, true>; }
-KernelFn kernel_bf16_f32_logits() { return &verify_kernel<2, 4, false>; }
+KernelFn kernel_bf16_f32_probs() { return &verify_kernel<2, 4, true, false>; }
+KernelFn kernel_bf16_f32_logits() { return &verify_kernel<2, 4, false, false>; }
 }  // namespace sv

@@ -83,13 +83,14 @@ sv_status setup_device(int dev, StaticDevice** out) {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-sv::KernelFn pick_kernel(int ebt, int ebd, bool probs) {
-  if (ebt == 2 && ebd == 2 && !probs) return sv::kernel_bf16_bf16_logits();
-  if (ebt == 2 && ebd == 4 && probs) return sv::kernel_bf16_f32_probs();
-  if (ebt == 2 && ebd == 4 && !probs) return sv::kernel_bf16_f32_logits();
-  if (ebt == 4 && ebd == 4 && !probs) return sv::kernel_f32_f32_logits();
-  if (ebt == 4 && ebd == 4 && probs) return sv::kernel_f32_f32_probs();
-  if (ebt == 4 && ebd == 2 && !probs) return sv::kernel_f32_bf16_logits();
+sv::KernelFn pick_kernel(int ebt, int ebd, bool probs, bool topk) {
+  using namespace sv;
+  if (ebt == 2 && ebd == 2 && !probs) return topk ? kernel_bf16_bf16_logits_topk() : kernel_bf16_bf16_logits();
+  if (ebt == 2 && ebd == 4 && probs) return topk ? kernel_bf16_f32_probs_topk() : kernel_bf16_f32_probs();
+  if (ebt == 2 && ebd == 4 && !probs) return topk ? kernel_bf16_f32_logits_topk() : kernel_bf16_f32_logits();
+  if (ebt == 4 && ebd == 4 && !probs) return topk ? kernel_f32_f32_logits_topk() : kernel_f32_f32_logits();
+  if (ebt == 4 && ebd == 4 && probs) return topk ? kernel_f32_f32_probs_topk() : kernel_f32_f32_probs();
+  if (ebt == 4 && ebd == 2 && !probs) return topk ? kernel_f32_bf16_logits_topk() : kernel_f32_bf16_logits();
   return nullptr;
 }
 
@@ -118,7 +119,7 @@ extern "C" sv_status spec_verify_static(const sv_verify_args* a, sv_stream_t str
   if (a->kmax > 0 && (a->draft_ld < a->V || (a->draft_ld * ebd) % 16 || !aligned16(a->draft)))
     return SV_ERR_INVALID;
   const bool probs = a->draft_kind == SV_DRAFT_PROBS;
-  const KernelFn fn = pick_kernel(ebt, ebd, probs);
+  const KernelFn fn = pick_kernel(ebt, ebd, probs, a->top_k != nullptr);
   if (!fn) return SV_ERR_UNSUPPORTED;
 
   int dev = 0;
@@ -155,6 +156,7 @@ extern "C" sv_status spec_verify_static(const sv_verify_args* a, sv_stream_t str
   P.slice = slice, P.d_off = d_off, P.n_tickets = (int)rows;
   P.spin_limit = kDefaultSpin;
   P.eos = a->eos_id, P.max_new = a->max_new;
+  P.top_k = a->top_k;
   P.rep_penalty = a->rep_penalty, P.rep_tokens = a->rep_tokens;
   P.rep_ld = a->rep_penalty ? (int)a->rep_ld : 0;
   P.rep_draft = a->draft_kind == SV_DRAFT_LOGITS;

@@ -40,6 +40,8 @@ def to_device(inp: dict, device="cuda", pin=False) -> dict:
         extra["eos"] = t(inp["eos"], np.int32)
     if inp.get("max_new") is not None:
         extra["max_new"] = t(inp["max_new"], np.int32)
+    if inp.get("top_k") is not None:
+        extra["top_k"] = t(inp["top_k"], np.int32)
     if inp.get("rep_penalty") is not None:
         extra["rep_penalty"] = t(inp["rep_penalty"], np.float32)
         extra["rep_tokens"] = t(inp["rep_tokens"], np.int32)

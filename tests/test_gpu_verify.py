@@ -222,6 +222,70 @@ def test_repetition_penalty_normalised_rows(ver):
     assert checked > 60
 
 
+@pytest.mark.parametrize("name", ["bf16 V=128256 top-p 0.95", "bf16 V=128256 top-p 1",
+                                  "fp32 logits V=1024", "fp32 probabilities V=128256",
+                                  "bf16 plateaus V=4093"])
+def test_top_k(ver, name):
+    """Top-k before top-p on p and q: small k (inside the 256-value window
+    below the maximum), large k (past it: the radix descent), k = 1, and values
+    that mean no top-k (0, -1, V, > V)."""
+    rng = np.random.default_rng(len(name))
+    if name.startswith("bf16 V"):
+        inp = W.verify_b64_k4(top_p=0.95 if "0.95" in name else 1.0)
+    elif name.startswith("fp32 logits"):
+        inp = W.small_fp32(B=48)
+        inp["temperature"][:] = 0.9
+        inp["top_p"][::2] = 0.9
+    elif name.startswith("fp32 prob"):
+        inp = W.ragged_probs(B=32)
+    else:
+        # integer logits: thousands of ties at every value, so the top-k
+        # boundary always falls inside a tied group
+        inp = W.verify_b64_k4(B=32, V=4093, top_p=0.95, sample_tokens=False)
+        t = rng.integers(-4, 5, inp["target"].shape).astype(np.float32)
+        inp["target"] = W.to_bf16_bits(t)
+        inp["draft"] = W.to_bf16_bits(t[:, :-1] + rng.integers(-1, 2, inp["draft"].shape))
+        d = W.bf16_bits_to_f32(inp["draft"])
+        for b in range(d.shape[0]):                  # proposals among the draft's top values
+            for i in range(d.shape[1]):
+                inp["tokens"][b, i] = rng.choice(np.flatnonzero(d[b, i] >= d[b, i].max() - 1))
+    B, V = inp["k"].shape[0], inp["target"].shape[-1]
+    choices = np.array([1, 2, 5, 20, 50, 300, 1000, 6000, 40000, 0, -1, V, V + 7])
+    inp["top_k"] = rng.choice(choices[choices < V + 8], B).astype(np.int32)
+    out, dbg, _, _ = run(ver, inp, debug=True)
+    rep = parity.compare(inp, out)
+    report(f"top-k, {name}", rep)
+    assert parity.compare_debug(inp, dbg) > 0
+    plain = dict(inp)
+    plain.pop("top_k")
+    ref = S.verify_batch(plain)
+    assert (ref["out_tokens"] != out["out_tokens"].cpu().numpy()).any()
+
+
+def test_top_k_normalised_rows(ver):
+    """Every row's normalised p and q after top-k and top-p (rows after a
+    rejection processed too), bf16 rows, V = 4093."""
+    inp = W.verify_b64_k4(B=16, V=4093)
+    inp["top_k"] = np.array([1, 3, 10, 40, 100, 400, 1500, 3000] * 2, np.int32)
+    inp["top_p"][8:] = 1.0
+    _, _, pp, pq = run(ver, inp, flags=binding.FLAG_NO_SKIP, probs=True)
+    pp, pq = pp.cpu().numpy(), pq.cpu().numpy()
+    checked = 0
+    for b in range(inp["k"].shape[0]):
+        T, tp, kk = inp["temperature"][b], inp["top_p"][b], int(inp["top_k"][b])
+        for i in range(int(inp["k"][b]) + 1):
+            p, info = S.transform(S.decode(inp["target"][b, i], "bf16"), "logits", T, tp, kk)
+            if info["margin"] >= parity.TOL:
+                np.testing.assert_allclose(pp[b, i], p, atol=parity.PROB_TOL, rtol=0)
+                checked += 1
+            if i < inp["k"][b]:
+                q, info = S.transform(S.decode(inp["draft"][b, i], "bf16"), "logits", T, tp, kk)
+                if info["margin"] >= parity.TOL:
+                    np.testing.assert_allclose(pq[b, i], q, atol=parity.PROB_TOL, rtol=0)
+                    checked += 1
+    assert checked > 60
+
+
 @pytest.mark.parametrize("top_p", [0.95, 1.0])
 def test_verify_b64_k4(ver, top_p):
     inp = W.verify_b64_k4(top_p=top_p)
