@@ -220,7 +220,7 @@ def run_ours(args):
     import torch
     import torch.distributed as dist
 
-    from speculative_decoding_verification_07_gb300 import binding, device_io
+    from speculative_decoding_verification_07_gb300 import binding, device_io, replicas
 
     ws, rank, local = dist_env()
     if ws > 1:
@@ -237,8 +237,8 @@ def run_ours(args):
     rows = rows_per_step(sets[0])
     ver = binding.Verifier(local)
     dsets = [device_io.to_device(s, dev) for s in sets]
-    for d, s in zip(dsets, sets):
-        d["request_id"] = d["request_id"] + rank * 1000003
+    for d in dsets:
+        d["request_id"] = replicas.rank_request_ids(d["request_id"], rank)
     BS = 16
     steps_total = args.warmup + args.steps + 64 * 4 + 16
     max_blocks = (8192 + (k + 1) * steps_total) // BS + 4
@@ -304,11 +304,7 @@ def run_ours(args):
     barrier()
     ms = t0e.elapsed_time(t1e)
     assert ver.error() == 0, "device error in the timed region"
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = ws * rows * K / (ms / 1e3)
+    value, ms = replicas.whole_job_rate(ms, rows * K, device=dev)
 
     # verify-kernel duration: CUDA events around each launch of G more steps
     nv = 4 * G
