@@ -242,7 +242,7 @@ class BlockPool:
         return n_freed
 
 
-def commit_copy(stage, accepted, seq_len, block_table, kv, block_size) -> None:
+def commit_copy(stage, accepted, seq_len, block_table, kv, block_size, path=None) -> None:
     """Commit by copy ([KV]: candidate K/V is written provisionally and only the
     accepted part is kept; [RJ] paragraph 1: allocation is not acceptance).
 
@@ -252,6 +252,12 @@ def commit_copy(stage, accepted, seq_len, block_table, kv, block_size) -> None:
     kv[table[b, p // BS], :, :, :, p % BS, :]; a_b = -1 copies nothing, and
     rejected entries are never written.  seq_len: S_b, the length before
     commit_rollback updates it.
+
+    Token tree ([CV] paragraph 3: gather the accepted path into the cache
+    layout): stage holds one entry per tree node (entry 0 the pending token)
+    and path[b][i - 1] names the node whose entry goes to position S_b + i.
+    Entries of nodes off the path (siblings of the accepted branch and their
+    descendants) are never written, so no cache position refers to them.
     """
     for b in range(len(accepted)):
         S, a = int(seq_len[b]), int(accepted[b])
@@ -260,7 +266,8 @@ def commit_copy(stage, accepted, seq_len, block_table, kv, block_size) -> None:
             blk = int(block_table[b, p // block_size])
             if blk < 0:
                 raise CacheError(f"request {b}: position {p} has no block")
-            kv[blk, :, :, :, p % block_size, :] = stage[b, i]
+            e = i if path is None or i == 0 else int(path[b][i - 1])
+            kv[blk, :, :, :, p % block_size, :] = stage[b, e]
 
 
 def rollback_contiguous(accepted, write_ptr) -> None:

@@ -93,10 +93,12 @@ def raw_words(seed, request_id, pos, stream, x):
                               axis=-1)[..., 0]
 
 
-def accept_uniform(seed, request_id, pos) -> float:
-    """u for the accept test of the draft token decided at absolute position pos."""
+def accept_uniform(seed, request_id, pos, slot=0) -> float:
+    """u for the accept test of the draft token decided at absolute position
+    pos; slot = the proposal's rank among its siblings in a token tree (0 for a
+    linear chain of drafts)."""
     return float(uniform_from_bits(raw_words(seed, request_id, pos, STREAM_ACCEPT,
-                                             np.zeros(1, np.uint64)))[0])
+                                             np.full(1, slot, np.uint64)))[0])
 
 
 def race_exponentials(seed, request_id, pos, V) -> np.ndarray:

@@ -52,6 +52,13 @@ Readings taken where the pages leave a step open (each also listed in the design doc)
     row i, in fp32, rounded back to bf16 for bf16 rows; target and draft logit
     rows alike; probability drafts are taken as given.  theta must be a finite
     number > 0 (1: no penalty), else bad input.
+  * token trees ([CV] paragraphs 3 and 5 name tree verification and branch
+    switches, not the law): the children of the current node are tested in
+    ascending order, each against the running residual of p (a rejection
+    replaces p_r by normalize(max(0, p_r - q))); the first accepted child
+    becomes the current node; when all are rejected the correction comes from
+    the last residual; a node without children gets the bonus.  Sibling rank r
+    is the accept uniform's slot, so a chain is the linear walk exactly.
 """
 
 from __future__ import annotations
@@ -323,6 +330,151 @@ def verify_request(target_rows, draft_rows, tokens, k, T, top_p, draft_kind,
         return dict(accepted=i, tokens=[int(t) for t in tokens[:i]] + [tok],
                     status=status, rows=rows)
     raise AssertionError("unreachable")
+
+
+# --------------------------------------------------------------------------- #
+# a token tree  ([CV] paragraphs 3 and 5; the per-step law of [SD] sections 2-3)
+# --------------------------------------------------------------------------- #
+def tree_children(parent, n):
+    """children[j] = the nodes whose parent is j, in ascending node order.
+    Nodes are 1..n (node 0 is the root: the pending token); parent[i - 1] is
+    the parent of node i."""
+    ch = {j: [] for j in range(n + 1)}
+    for i in range(1, n + 1):
+        ch[int(parent[i - 1])].append(i)
+    return ch
+
+
+def verify_tree(target_rows, draft_rows, parent, tokens, n, T, top_p, draft_kind, seed,
+                request_id, seq_len, top_k=0, force=None):
+    """Verify one request's token tree ([CV] paragraph 3: a tree implementation
+    keeps the accepted path; paragraph 5: test tree branch switches).
+
+    Node i (1..n) proposes tokens[i - 1] as the child of parent[i - 1] (a node
+    with a lower index; 0 is the root).  target_rows[j] is the target's
+    distribution of the token after node j; draft_rows[j] the draft's, from
+    which j's children were drawn (independently, with repeats allowed).
+
+    Reading (the pages name tree verification without giving its law): start
+    at the root; at node j with children c_1 .. c_m (ascending) and residual
+    p_1 = p_j, test c_r as in the linear walk with target p_r: accept iff
+    u_r * q_j(y) < p_r(y); on rejection p_{r+1} = normalize(max(0, p_r - q_j)).
+    An accepted child becomes the current node.  If every child is rejected
+    the correction is drawn from p_{m+1}; at a node without children the bonus
+    is drawn from p_j.  Each test is one step of the linear law with target p_r,
+    so the emitted token is distributed as p_j whatever the branching.  A
+    residual that becomes numerically empty stops the tests and draws from p_j
+    (ST_RESIDUAL_EMPTY).  Positions: node depth d puts its token at S + d; the
+    tests among j's children use pos = S + d_j + 1 and sibling rank r - 1 as
+    the uniform's slot; the correction or bonus after node j uses pos = S +
+    d_j + 1.  A chain-shaped tree is the linear walk exactly.
+    force: optional {(node, rank): bool} overriding an accept decision.
+    Returns accepted (path length, -1 on bad input), path (node ids), tokens
+    (path tokens then the correction or bonus), status, and per-test records.
+    """
+    force = force or {}
+    V = target_rows.shape[-1]
+    T = float(np.float32(T))
+    top_p = float(np.float32(top_p))
+    recs = []
+    bad = dict(accepted=-1, path=[], tokens=[], status=ST_BAD_INPUT, tests=recs)
+    if not (T >= 0.0) or not (0.0 < top_p <= 1.0) or n < 0:
+        return bad
+    for i in range(1, n + 1):
+        if not (0 <= int(parent[i - 1]) < i) or not (0 <= int(tokens[i - 1]) < V):
+            return bad
+    ch = tree_children(parent, n)
+    status = 0
+    cur, depth, path = 0, 0, []
+    while True:
+        pos = int(seq_len) + depth + 1
+        trow = target_rows[cur]
+        if not row_is_valid(trow, "logits"):
+            return bad
+        p, pinfo = transform(trow, "logits", T, top_p, top_k)
+        kids = ch[cur]
+        if not kids:                                   # bonus after a leaf
+            E = philox.race_exponentials(seed, request_id, pos, V)
+            tok = exponential_race(p, E)
+            recs.append({"node": cur, "race": {"w": p, "E": E, "token": tok},
+                         "p_margin": pinfo["margin"]})
+            return dict(accepted=len(path), path=path,
+                        tokens=[int(tokens[j - 1]) for j in path] + [tok], status=status,
+                        tests=recs)
+        drow = draft_rows[cur]
+        if not row_is_valid(drow, draft_kind):
+            return bad
+        q, qinfo = transform(drow, draft_kind, T, top_p, top_k)
+        pr = p
+        nxt = None
+        for r, j in enumerate(kids):
+            y = int(tokens[j - 1])
+            u = philox.accept_uniform(seed, request_id, pos, r)
+            if q[y] == 0.0:
+                status |= ST_Q_ZERO
+            ok = bool(accepts(u, pr[y], q[y]))
+            rec = {"node": j, "rank": r, "p_y": float(pr[y]), "q_y": float(q[y]), "u": u,
+                   "p_margin": pinfo["margin"], "q_margin": qinfo["margin"]}
+            if (j, r) in force:
+                rec["forced_from"] = ok
+                ok = bool(force[(j, r)])
+            rec["accept"] = ok
+            recs.append(rec)
+            if ok:
+                nxt = j
+                break
+            w = residual(pr, q)
+            if not (w > 0).any():
+                status |= ST_RESIDUAL_EMPTY
+                pr = None
+                break
+            pr = w / w.sum()
+        if nxt is not None:
+            path.append(nxt)
+            cur, depth = nxt, depth + 1
+            continue
+        wr = p if pr is None else pr                  # correction
+        E = philox.race_exponentials(seed, request_id, pos, V)
+        tok = exponential_race(wr, E)
+        recs.append({"node": cur, "race": {"w": wr, "E": E, "token": tok},
+                     "p_margin": pinfo["margin"], "q_margin": qinfo["margin"]})
+        return dict(accepted=len(path), path=path,
+                    tokens=[int(tokens[j - 1]) for j in path] + [tok], status=status, tests=recs)
+
+
+def verify_tree_batch(inp: dict, force=None):
+    """verify_tree over every request of a tree workload dict: target
+    [B][N+1][V], draft [B][N+1][V], parent [B][N], tokens [B][N], n [B],
+    temperature, top_p, optional top_k, seed, request_id, seq_len.  Returns
+    accepted [B], path [B][N] and out_tokens [B][N+1] (-1 padded), num_emitted,
+    status and the per-request records."""
+    B, N = inp["parent"].shape
+    acc = np.zeros(B, np.int32)
+    path = np.full((B, N), -1, np.int32)
+    out = np.full((B, N + 1), -1, np.int32)
+    nem = np.zeros(B, np.int32)
+    st = np.zeros(B, np.uint32)
+    recs = []
+    for b in range(B):
+        nb = int(inp["n"][b])
+        if not (0 <= nb <= N):
+            r = dict(accepted=-1, path=[], tokens=[], status=ST_BAD_INPUT, tests=[])
+        else:
+            tr = decode(inp["target"][b, :nb + 1], inp["target_dtype"])
+            dr = decode(inp["draft"][b, :nb + 1], inp["draft_dtype"])
+            r = verify_tree(tr, dr, inp["parent"][b], inp["tokens"][b], nb,
+                            inp["temperature"][b], inp["top_p"][b], inp["draft_kind"],
+                            inp["seed"], int(inp["request_id"][b]), int(inp["seq_len"][b]),
+                            top_k=int(inp["top_k"][b]) if inp.get("top_k") is not None else 0,
+                            force=(force or {}).get(b))
+        acc[b] = r["accepted"]
+        st[b] = r["status"]
+        path[b, :len(r["path"])] = r["path"]
+        out[b, :len(r["tokens"])] = r["tokens"]
+        nem[b] = len(r["tokens"])
+        recs.append(r)
+    return dict(accepted=acc, path=path, out_tokens=out, num_emitted=nem, status=st,
+                records=recs)
 
 
 def request_options(inp: dict, b: int) -> dict:

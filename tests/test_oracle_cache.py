@@ -398,3 +398,46 @@ def test_copy_on_write_keeps_forked_prefixes_isolated():
     assert t2[0, 2] == 2 and t2[1, 2] != 2 and pool2.refcount[2] == 1
     np.testing.assert_array_equal(kv2[t2[1, 2], :, :, :, :S % BS], 7.0)
     _check_invariants(pool2, t2)
+
+
+@pytest.mark.parametrize("forced_path", [[1, 3], [2, 4, 5], [2], []])
+def test_tree_commit_gathers_the_accepted_branch(forced_path):
+    """A token tree's candidate K/V sits in a staging buffer in node order; the
+    accepted path (a branch switch when it starts at the second root child) is
+    gathered into positions S..S+a and the cache equals a recompute of the
+    committed history; no entry of a node off the path reaches the cache."""
+    BS = 16
+    m = ToyAttention(seed=11)
+    rng = np.random.default_rng(12)
+    pool = BlockPool(32, BS)
+    kv = np.full((32, m.L, 2, m.H, BS, m.d), np.nan, np.float32)
+    table = np.full((1, 16), -1, np.int32)
+    S = 29
+    history = list(rng.integers(0, 1000, S + 1))
+    seq = np.array([0], np.int32)
+    pool.reserve(seq, [S - 1], table)
+    stage0 = m.kv(history[:S], list(range(S)))
+    for j in range(S):
+        kv[table[0, j // BS], :, :, :, j % BS, :] = stage0[j]
+    seq[0] = S
+    # nodes 1, 2 under the root; 3 under 1; 4 under 2; 5 under 4
+    parent = [0, 0, 1, 2, 4]
+    depth = [0, 1, 1, 2, 2, 3]
+    toks = list(rng.integers(0, 1000, 5))
+    for i in range(1, len(forced_path)):
+        assert parent[forced_path[i] - 1] == forced_path[i - 1]
+    dmax = max(depth)
+    pool.reserve(seq, [dmax], table)
+    stage = m.kv([history[-1]] + toks, [S + d for d in depth])[None]
+    # nodes off the path get poisoned entries: any leak shows up as a mismatch
+    off = [j for j in range(1, 6) if j not in forced_path]
+    stage[0, off] = np.float32(1e30)
+    a = len(forced_path)
+    commit_copy(stage, [a], seq.copy(), table, kv, BS, path=[forced_path])
+    pool.commit_rollback([dmax], [a], seq, table)
+    committed = history + [toks[j - 1] for j in forced_path]
+    n = int(seq[0])
+    assert n == S + 1 + a
+    np.testing.assert_array_equal(_gather(kv, table[0], n, BS),
+                                  m.kv(committed, list(range(n))))
+    _check_invariants(pool, table, seq)

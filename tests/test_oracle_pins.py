@@ -514,3 +514,79 @@ def test_top_k_walk_q_equals_p():
     y_out = np.array([order[5], order[1], order[2]])               # rank 6 of row 0
     r = S.verify_request(rows, rows[:3], y_out, 3, 1.0, 1.0, "logits", 1, 0, 5, top_k=3)
     assert r["rows"][0]["q_y"] == 0.0 and r["status"] & S.ST_Q_ZERO
+
+
+def test_tree_chain_is_the_linear_walk():
+    """A chain-shaped token tree (node i the child of node i - 1) is the
+    linear walk exactly: same accepted count, tokens and status bits."""
+    rng = np.random.default_rng(45)
+    for t in range(60):
+        V, k = int(rng.integers(3, 12)), int(rng.integers(0, 5))
+        rows = rng.standard_normal((k + 1, V)) * 2
+        drows = rows + rng.standard_normal((k + 1, V))
+        y = rng.integers(0, V, k)
+        T, tp, tk = [(1.0, 1.0, 0), (0.7, 0.8, 0), (0.0, 1.0, 0), (1.2, 0.9, 3)][t % 4]
+        lin = S.verify_request(rows, drows[:k], y, k, T, tp, "logits", 5 + t, 3, 40, top_k=tk)
+        tree = S.verify_tree(rows, drows, np.arange(k), y, k, T, tp, "logits", 5 + t, 3, 40,
+                             top_k=tk)
+        assert tree["accepted"] == lin["accepted"] and tree["tokens"] == lin["tokens"]
+        assert tree["status"] == lin["status"]
+        assert tree["path"] == list(range(1, lin["accepted"] + 1))
+
+
+def test_tree_root_law_chi_square():
+    """Tree verification keeps the target law: m children drawn i.i.d. from q
+    at the root, tested in turn against the running residual, then the
+    correction; the first emitted token must follow p (chi-square), and the
+    first child is accepted with probability sum_x min(p, q)."""
+    rng = np.random.default_rng(46)
+    V, m, n_trials = 6, 3, 6000
+    p_logits = np.array([1.0, 0.2, -0.5, 0.8, -1.0, 0.0])
+    q_logits = np.array([-0.3, 1.1, 0.4, 0.0, 0.6, -0.8])
+    p = S.softmax_T(p_logits, "logits", 1.0)
+    q = S.softmax_T(q_logits, "logits", 1.0)
+    rows_t = np.stack([p_logits] + [np.zeros(V)] * m)
+    rows_d = np.stack([q_logits] + [np.zeros(V)] * m)
+    counts = np.zeros(V)
+    first_acc = 0
+    for t in range(n_trials):
+        kids = rng.choice(V, m, p=q)
+        r = S.verify_tree(rows_t, rows_d, np.zeros(m, np.int64), kids, m, 1.0, 1.0, "logits",
+                          1000 + t, 7, 0)
+        counts[r["tokens"][0]] += 1
+        first_acc += r["path"][:1] == [1]
+    exp = p * n_trials
+    assert stats.chisquare(counts, exp).pvalue > 1e-3
+    beta = np.minimum(p, q).sum()
+    assert abs(first_acc / n_trials - beta) < 4 * np.sqrt(beta * (1 - beta) / n_trials)
+
+
+def test_tree_branch_switch_and_repeated_siblings():
+    """Branch switch worked by hand: root children y_1 (node 1) and y_2 (node
+    2) with q = (1/2 at y_1, 1/2 at y_2) and p concentrated on y_2.  Node 1 has
+    p(y_1) = 0 and is rejected; the residual max(0, p - q) normalised is 1 at
+    y_2, so node 2 is accepted whatever u, and the walk continues below node 2
+    (its child, node 3, with q = p there, is accepted too).  Then: a repeated
+    sibling is never accepted after its twin was rejected."""
+    V = 4
+    NEG = -np.inf
+    t_rows = np.array([[NEG, NEG, 0.0, NEG],        # root: p = y_2 only
+                       [0.0, 0.0, 0.0, 0.0],
+                       [0.0, 1.0, 2.0, 3.0],        # after node 2
+                       [0.0, 0.0, 0.0, 0.0]])
+    d_rows = np.array([[NEG, 0.0, 0.0, NEG],        # root: q = 1/2 on tokens 1 and 2
+                       [0.0, 0.0, 0.0, 0.0],
+                       [0.0, 1.0, 2.0, 3.0],        # node 2: q = p
+                       [0.0, 0.0, 0.0, 0.0]])
+    parent, tokens = np.array([0, 0, 2]), np.array([1, 2, 3])
+    for seed in range(20):
+        r = S.verify_tree(t_rows, d_rows, parent, tokens, 3, 1.0, 1.0, "logits", seed, 0, 10)
+        assert r["path"] == [2, 3] and r["tokens"][:2] == [2, 3] and r["accepted"] == 2
+        assert r["tests"][0]["accept"] is False and r["tests"][1]["p_y"] == 1.0
+    rng = np.random.default_rng(47)
+    for seed in range(200):
+        tr, dr = rng.standard_normal((3, 5)), rng.standard_normal((3, 5))
+        y = int(rng.integers(0, 5))
+        r = S.verify_tree(tr, dr, np.array([0, 0]), np.array([y, y]), 2, 1.0, 1.0, "logits",
+                          seed, 1, 0)
+        assert r["path"] != [2]                      # the twin is never accepted
