@@ -14,8 +14,10 @@
  *   [RJ] "Rejected speculative tokens remain in KV", paragraphs 1-3
  *        (allocation is not acceptance; partially valid blocks).
  *   [CV] "Keep cache validity aligned with the committed token history",
- *        paragraphs 1-4 (pending-token convention; block tables, ownership and
- *        reference counts; shared-prefix isolation).
+ *        paragraphs 1-5 (pending-token convention; block tables, ownership and
+ *        reference counts; shared-prefix isolation; tree implementations keep
+ *        the accepted path; the cases to test: EOS, output caps, tree branch
+ *        switches).
  *
  * Conventions shared by every entry point
  *   - Every pointer argument is a DEVICE pointer owned by the caller, unless
@@ -268,6 +270,77 @@ sv_status spec_verify(sv_handle* handle, const sv_verify_args* args, void* works
  *    reported in status[] only. */
 sv_status spec_verify_static(const sv_verify_args* args, sv_stream_t stream);
 
+/*
+ * Token-tree verification ([CV] paragraph 3: a tree implementation keeps the
+ * accepted path; paragraph 5: test tree branch switches; the law of each test
+ * is [SD] s2-s3).  Request b proposes a tree of n_b <= N nodes below its
+ * pending token (node 0, the root).  Node i (1..n_b) is the proposal
+ * tokens[b][i-1] following parent[b][i-1], a node with a LOWER index (so a
+ * node's ancestors come before it).  Children of one node are independent
+ * draws from the draft's distribution at that node (repeats allowed).
+ *
+ * Walk (reading; the pages give no law for trees): from the root, the
+ * children c_1 .. c_m of the current node j (ascending index) are tested in
+ * turn: accept c_r iff u_r * q_j(y) < p_r(y), with p_1 = p_j and p_{r+1} =
+ * normalize(max(0, p_r - q_j)) after a rejection.  The first accepted child
+ * becomes the current node.  If every child is rejected, the correction is
+ * drawn from p_{m+1} (from p_j with SV_ST_RESIDUAL_EMPTY if that residual is
+ * numerically empty); at a node without children the bonus is drawn from p_j.
+ * Each test is one step of the linear law, so the emitted tokens follow the
+ * target's distribution however the tree branches.  Transforms (T, top-k,
+ * top-p) are those of spec_verify, applied to p_j and q_j.
+ * Randomness: node depth d puts its token at position S_b + d; the tests
+ * among j's children use the accept uniform of position S_b + d_j + 1 with
+ * slot r - 1 (counter (slot >> 2, pos, request_id, 1), word slot & 3); the
+ * correction or bonus after node j races with position S_b + d_j + 1.  A
+ * chain-shaped tree gives exactly spec_verify's result.
+ *
+ * target [B][N+1][target_ld]: row j = the target's distribution of the token
+ *        after node j (row 0: after the pending token).  draft [B][N+1]
+ *        [draft_ld]: row j = the draft's distribution at node j (rows of
+ *        leaves are never read).  Layout rules as in sv_verify_args.
+ * parent, tokens [B][N] int32; n_nodes [B] (NULL = N); temperature [B];
+ * top_p [B] (NULL = 1); top_k [B] (NULL = none); request_id [B] (NULL = b);
+ * seq_len [B] S_b (NULL = 0); seed.
+ * Outputs: accepted [B] = length a_b of the accepted path (-1 on bad input:
+ *   a bad T / top_p / n_b, a parent not below its node, a token outside
+ *   [0, V), or a NaN / +inf / empty row on the walk); path [B][N] = the
+ *   accepted node ids in depth order, then -1; out_tokens [B][N+1] = their
+ *   tokens, then the correction or bonus token, then -1; num_emitted [B] =
+ *   a_b + 1 (0 on bad input); status [B] (SV_ST_* bits).
+ * Each cluster of CTAs walks one request at a time; no workspace is needed.
+ */
+#define SV_TREE_MAX_NODES 4096
+typedef struct {
+  int32_t B, N, V;
+  uint32_t flags; /* reserved, 0 */
+  const void* target;
+  int64_t target_ld;
+  int32_t target_dtype; /* sv_dtype */
+  int32_t draft_dtype;  /* sv_dtype */
+  int32_t draft_kind;   /* sv_draft_kind */
+  int32_t reserved0;
+  const void* draft;
+  int64_t draft_ld;
+  const int32_t* parent;
+  const int32_t* tokens;
+  const int32_t* n_nodes;
+  const float* temperature;
+  const float* top_p;
+  const int32_t* top_k;
+  const uint32_t* request_id;
+  const int32_t* seq_len;
+  uint64_t seed;
+  int32_t* accepted;
+  int32_t* path;
+  int32_t* out_tokens;
+  int32_t* num_emitted;
+  uint32_t* status;
+} sv_tree_args;
+
+size_t sv_tree_args_size(void);
+sv_status spec_verify_tree(sv_handle* handle, const sv_tree_args* args, sv_stream_t stream);
+
 /* stack = [n-1, ..., 1, 0] (blocks pop as 0, 1, 2, ...), free_top = n,
  * refcount = 0. */
 sv_status bfl_init(sv_handle* handle, const bfl_state* st, sv_stream_t stream);
@@ -278,7 +351,7 @@ sv_status bfl_init(sv_handle* handle, const bfl_state* st, sv_stream_t stream);
  * ceil(S_b/BS) more, popped in request order.  All-or-nothing: on a shortage
  * the device error word gets SV_ERR_OOM and nothing changes.  Appending into
  * a partially filled block whose refcount is above 1 is refused
- * (SV_ERR_STATE): copy-on-write is not provided.
+ * (SV_ERR_STATE); bfl_reserve_cow copies such a block first.
  * seq_len [B], k [B] (NULL = 0), block_table [B][max_blocks] in/out. */
 sv_status bfl_reserve(sv_handle* handle, const bfl_state* st, int32_t B, const int32_t* seq_len,
                       const int32_t* k, int32_t* block_table, int32_t max_blocks,
@@ -346,6 +419,23 @@ sv_status kv_commit_copy(sv_handle* handle, int32_t B, int32_t kmax, const int32
                          const int32_t* seq_len, const int32_t* block_table, int32_t max_blocks,
                          int32_t block_size, int32_t num_blocks, const void* stage,
                          const kv_payload* kv, sv_stream_t stream);
+
+/* Commit by copy for a token tree ([CV] paragraph 3: gather the accepted path
+ * into the cache layout and drop the sibling states).  stage [B][N+1][L][2]
+ * [H][D] holds one K/V entry per tree node (entry 0: the pending token).
+ * Position S_b receives entry 0 and position S_b + i (1 <= i <= a_b) the entry
+ * of path[b][i-1]; entries of nodes off the path are never written, so no
+ * cache position refers to them.  accepted [B] (a_b <= max_depth, the
+ * longest path any tree of the batch can give), path [B][N] from
+ * spec_verify_tree, seq_len [B] = S_b before kv_commit_rollback (called with
+ * k_b = max_depth, or the request's own depth).  A position without a block,
+ * or a path entry outside [1, N]: SV_ERR_STATE in the error word, that entry
+ * skipped. */
+sv_status kv_commit_tree(sv_handle* handle, int32_t B, int32_t N, int32_t max_depth,
+                         const int32_t* accepted, const int32_t* path, const int32_t* seq_len,
+                         const int32_t* block_table, int32_t max_blocks, int32_t block_size,
+                         int32_t num_blocks, const void* stage, const kv_payload* kv,
+                         sv_stream_t stream);
 
 /* Draft-cache realignment ([SD] section 4, "update cache state": the draft
  * cache is reconciled with the corrected token; [CV] paragraph 4: the draft

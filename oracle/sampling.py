@@ -413,7 +413,7 @@ def verify_tree(target_rows, draft_rows, parent, tokens, n, T, top_p, draft_kind
             if q[y] == 0.0:
                 status |= ST_Q_ZERO
             ok = bool(accepts(u, pr[y], q[y]))
-            rec = {"node": j, "rank": r, "p_y": float(pr[y]), "q_y": float(q[y]), "u": u,
+            rec = {"node": j, "parent": cur, "rank": r, "p_y": float(pr[y]), "q_y": float(q[y]), "u": u,
                    "p_margin": pinfo["margin"], "q_margin": qinfo["margin"]}
             if (j, r) in force:
                 rec["forced_from"] = ok

@@ -38,7 +38,9 @@ ROW_NONE, ROW_ACCEPTED, ROW_REJECTED, ROW_SKIPPED, ROW_INVALID, ROW_BONUS, ROW_T
 EXPORTS = ("sv_verify_args_size", "sv_create", "sv_destroy", "sv_workspace_size",
            "spec_verify", "bfl_init", "bfl_reserve", "bfl_fork_prefix", "bfl_release",
            "kv_commit_rollback", "kv_rollback_contig", "sv_get_error", "spec_verify_static",
-           "kv_commit_draft", "bfl_reserve_cow", "kv_commit_copy")
+           "kv_commit_draft", "bfl_reserve_cow", "kv_commit_copy", "sv_tree_args_size",
+           "spec_verify_tree", "kv_commit_tree")
+SV_TREE_MAX_NODES = 4096
 
 
 class KvPayload(ctypes.Structure):
@@ -70,6 +72,19 @@ class SvVerifyArgs(ctypes.Structure):
                 ("probs_q", c_void_p), ("eos_id", c_void_p), ("max_new", c_void_p),
                 ("rep_penalty", c_void_p), ("rep_tokens", c_void_p), ("rep_ld", c_int64),
                 ("top_k", c_void_p)]
+
+
+class SvTreeArgs(ctypes.Structure):
+    _fields_ = [("B", c_int32), ("N", c_int32), ("V", c_int32), ("flags", c_uint32),
+                ("target", c_void_p), ("target_ld", c_int64),
+                ("target_dtype", c_int32), ("draft_dtype", c_int32),
+                ("draft_kind", c_int32), ("reserved0", c_int32),
+                ("draft", c_void_p), ("draft_ld", c_int64),
+                ("parent", c_void_p), ("tokens", c_void_p), ("n_nodes", c_void_p),
+                ("temperature", c_void_p), ("top_p", c_void_p), ("top_k", c_void_p),
+                ("request_id", c_void_p), ("seq_len", c_void_p), ("seed", c_uint64),
+                ("accepted", c_void_p), ("path", c_void_p), ("out_tokens", c_void_p),
+                ("num_emitted", c_void_p), ("status", c_void_p)]
 
 
 class BflState(ctypes.Structure):
@@ -114,10 +129,18 @@ def load_library(path: str = LIB_PATH):
                                        c_void_p, c_void_p, c_int32, c_void_p, c_void_p]
     lib.kv_rollback_contig.argtypes = [c_void_p, c_int32, c_void_p, c_void_p, c_void_p]
     lib.sv_get_error.argtypes = [c_void_p, c_void_p, POINTER(c_int32)]
+    lib.sv_tree_args_size.restype = c_size_t
+    lib.spec_verify_tree.argtypes = [c_void_p, POINTER(SvTreeArgs), c_void_p]
+    lib.kv_commit_tree.argtypes = [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p,
+                                   c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p,
+                                   POINTER(KvPayload), c_void_p]
     for name in EXPORTS[1:]:
-        getattr(lib, name).restype = c_int32
+        if name != "sv_tree_args_size":
+            getattr(lib, name).restype = c_int32
     if lib.sv_verify_args_size() != ctypes.sizeof(SvVerifyArgs):
         raise ImportError("sv_verify_args layout mismatch between binding and library")
+    if lib.sv_tree_args_size() != ctypes.sizeof(SvTreeArgs):
+        raise ImportError("sv_tree_args layout mismatch between binding and library")
     _lib = lib
     return lib
 
@@ -285,6 +308,41 @@ def kv_commit_copy(handle, accepted, seq_len, block_table, block_size, num_block
         ctypes.byref(_payload(kv)), _stream(stream)))
 
 
+def make_tree_args(*, target, draft, parent, tokens, temperature, accepted, path, out_tokens,
+                   num_emitted, status, V=None, n_nodes=None, top_p=None, top_k=None, seed=0,
+                   request_id=None, seq_len=None, draft_kind="logits") -> SvTreeArgs:
+    """target, draft: [B, N+1, ld] rows per tree node; parent, tokens: [B, N] int32."""
+    B, rows, _ = target.shape
+    a = SvTreeArgs()
+    a.B, a.N, a.V, a.flags = B, rows - 1, int(V if V is not None else target.shape[-1]), 0
+    a.target, a.target_ld, a.target_dtype = _ptr(target), _row_ld(target), _dtype_code(target)
+    a.draft, a.draft_ld, a.draft_dtype = _ptr(draft), _row_ld(draft), _dtype_code(draft)
+    a.draft_kind = SV_DRAFT_PROBS if draft_kind == "probs" else SV_DRAFT_LOGITS
+    a.parent, a.tokens, a.n_nodes = _ptr(parent), _ptr(tokens), _ptr(n_nodes)
+    a.temperature, a.top_p, a.top_k = _ptr(temperature), _ptr(top_p), _ptr(top_k)
+    a.request_id, a.seq_len, a.seed = _ptr(request_id), _ptr(seq_len), int(seed) & (2 ** 64 - 1)
+    a.accepted, a.path, a.out_tokens = _ptr(accepted), _ptr(path), _ptr(out_tokens)
+    a.num_emitted, a.status = _ptr(num_emitted), _ptr(status)
+    return a
+
+
+def spec_verify_tree(handle, args: SvTreeArgs, stream=None) -> None:
+    _check("spec_verify_tree", load_library().spec_verify_tree(handle, ctypes.byref(args),
+                                                               _stream(stream)))
+
+
+def kv_commit_tree(handle, accepted, path, seq_len, block_table, block_size, num_blocks, stage,
+                   kv, max_depth, stream=None) -> None:
+    """stage: [B, N + 1, layers, 2, heads, head_dim] contiguous (one entry per
+    tree node); path: [B, N] from spec_verify_tree."""
+    if stage.dim() != 6 or not stage.is_contiguous() or stage.dtype != kv.dtype:
+        raise ValueError("stage must be a contiguous [B, N+1, layers, 2, heads, head_dim] tensor")
+    _check("kv_commit_tree", load_library().kv_commit_tree(
+        handle, accepted.numel(), stage.shape[1] - 1, int(max_depth), _ptr(accepted), _ptr(path),
+        _ptr(seq_len), _ptr(block_table), block_table.shape[1], block_size, num_blocks,
+        _ptr(stage), ctypes.byref(_payload(kv)), _stream(stream)))
+
+
 def kv_commit_draft(handle, pool, seq_len, accepted, draft_len, draft_table, n_freed=None,
                     stream=None) -> None:
     _check("kv_commit_draft", load_library().kv_commit_draft(
@@ -383,6 +441,24 @@ class Verifier:
                       temperature=temperature, **out, **kw)
         ws = self.ensure_workspace(a)
         spec_verify(self.handle, a, ws, stream)
+        return out
+
+    def tree_outputs(self, B: int, N: int):
+        d = self.device
+        return dict(accepted=torch.empty(B, dtype=torch.int32, device=d),
+                    path=torch.empty(B, max(N, 1), dtype=torch.int32, device=d),
+                    out_tokens=torch.empty(B, N + 1, dtype=torch.int32, device=d),
+                    num_emitted=torch.empty(B, dtype=torch.int32, device=d),
+                    status=torch.empty(B, dtype=torch.int32, device=d))
+
+    def verify_tree(self, *, target, draft, parent, tokens, temperature, out=None, stream=None,
+                    **kw):
+        """Run spec_verify_tree; returns the output tensors (allocated unless given)."""
+        B, rows, _ = target.shape
+        out = out or self.tree_outputs(B, rows - 1)
+        a = make_tree_args(target=target, draft=draft, parent=parent, tokens=tokens,
+                           temperature=temperature, **out, **kw)
+        spec_verify_tree(self.handle, a, stream)
         return out
 
     def error(self, stream=None) -> int:

@@ -24,7 +24,8 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 
 SOURCES = ["api.cu", "kv_cache.cu", "verify.cu", "verify_bf16.cu", "verify_f32.cu", "verify_mixed.cu",
-           "verify_static.cu", "verify_topk_bf16.cu", "verify_topk_f32.cu", "verify_topk_mixed.cu"]
+           "verify_static.cu", "verify_topk_bf16.cu", "verify_topk_f32.cu", "verify_topk_mixed.cu",
+           "tree_verify.cu", "tree_bf16.cu", "tree_f32.cu"]
 
 
 def nvcc() -> str:

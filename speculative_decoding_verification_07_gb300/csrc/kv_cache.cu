@@ -415,17 +415,31 @@ __global__ void kv_cow_copy_kernel(int B, const int32_t* cow, kv_payload kv, int
 // ---------------------------------------------------------------------------
 constexpr int kCopySplit = 8;
 
-__global__ void __launch_bounds__(256) kv_commit_copy_kernel(int B, int kmax, const int32_t* accepted,
+// rows: positions S_b .. S_b + rows - 1 considered per request; entries: the
+// stage's entries per request; path (tree commits) [B][path_ld]: the entry of
+// position S_b + i is path[b][i - 1] for i >= 1 (NULL: entry i).
+__global__ void __launch_bounds__(256) kv_commit_copy_kernel(int B, int rows, int entries,
+                                                             const int32_t* path, int path_ld,
+                                                             const int32_t* accepted,
                                                              const int32_t* seq_len,
                                                              const int32_t* table, int max_blocks,
                                                              int block_size, int num_blocks,
                                                              const char* stage, kv_payload kv,
                                                              int* err) {
   const int e = blockIdx.x / kCopySplit, part = blockIdx.x % kCopySplit;
-  const int b = e / (kmax + 1), i = e % (kmax + 1);
+  const int b = e / rows, i = e % rows;
   if (b >= B) return;
   const int a = accepted[b];
+  if (i == 0 && part == 0 && a >= rows && threadIdx.x == 0) report(err, SV_ERR_STATE);  // path too long
   if (i > a) return;
+  int src_entry = i;
+  if (path && i > 0) {
+    src_entry = path[(size_t)b * path_ld + i - 1];
+    if (src_entry < 1 || src_entry >= entries) {
+      if (threadIdx.x == 0 && part == 0) report(err, SV_ERR_STATE);
+      return;
+    }
+  }
   const int p = seq_len[b] + i;
   const int j = p / block_size;
   const int blk = (p >= 0 && j < max_blocks) ? table[(size_t)b * max_blocks + j] : -1;
@@ -437,7 +451,7 @@ __global__ void __launch_bounds__(256) kv_commit_copy_kernel(int B, int kmax, co
   const int vrun = kv.head_dim * kv.elem_bytes / 16;  // 16-byte vectors per run
   const size_t run = (size_t)block_size * kv.head_dim * kv.elem_bytes;
   const uint4* src = reinterpret_cast<const uint4*>(
-      stage + ((size_t)b * (kmax + 1) + i) * runs * kv.head_dim * kv.elem_bytes);
+      stage + ((size_t)b * entries + src_entry) * runs * kv.head_dim * kv.elem_bytes);
   char* dst = static_cast<char*>(kv.data) + (size_t)blk * runs * run +
               (size_t)(p % block_size) * kv.head_dim * kv.elem_bytes;
   const int n = runs * vrun;
@@ -682,8 +696,24 @@ extern "C" sv_status kv_commit_copy(sv_handle* h, int32_t B, int32_t kmax, const
   if (B == 0) return SV_OK;
   if (!accepted || !seq_len || !table || !stage) return SV_ERR_INVALID;
   kv_commit_copy_kernel<<<B * (kmax + 1) * kCopySplit, 256, 0, (cudaStream_t)stream>>>(
-      B, kmax, accepted, seq_len, table, max_blocks, block_size, num_blocks,
+      B, kmax + 1, kmax + 1, nullptr, 0, accepted, seq_len, table, max_blocks, block_size, num_blocks,
       static_cast<const char*>(stage), *kv, h->d_err);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+extern "C" sv_status kv_commit_tree(sv_handle* h, int32_t B, int32_t N, int32_t max_depth,
+                                    const int32_t* accepted, const int32_t* path,
+                                    const int32_t* seq_len, const int32_t* table, int32_t max_blocks,
+                                    int32_t block_size, int32_t num_blocks, const void* stage,
+                                    const kv_payload* kv, sv_stream_t stream) {
+  if (!h || B < 0 || N < 0 || max_depth < 0 || max_depth > N || max_blocks < 1 || block_size < 1 ||
+      num_blocks < 0 || bad_payload(kv) || ((uintptr_t)stage & 15u))
+    return SV_ERR_INVALID;
+  if (B == 0) return SV_OK;
+  if (!accepted || !seq_len || !table || !stage || (N > 0 && !path)) return SV_ERR_INVALID;
+  kv_commit_copy_kernel<<<B * (max_depth + 1) * kCopySplit, 256, 0, (cudaStream_t)stream>>>(
+      B, max_depth + 1, N + 1, path, N, accepted, seq_len, table, max_blocks, block_size,
+      num_blocks, static_cast<const char*>(stage), *kv, h->d_err);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 

@@ -60,3 +60,31 @@ def to_device(inp: dict, device="cuda", pin=False) -> dict:
         V=int(inp["target"].shape[-1]),
         draft_kind=inp["draft_kind"],
     )
+
+
+def tree_to_device(inp: dict, device="cuda", pin=False) -> dict:
+    """Token-tree inputs (workloads.tree_batch) as tensors on `device`."""
+    def t(a, dt):
+        x = torch.from_numpy(np.ascontiguousarray(a).astype(dt, copy=False))
+        if pin:
+            x = x.pin_memory()
+        return x if device is None else x.to(device)
+
+    extra = {}
+    if inp.get("top_k") is not None:
+        extra["top_k"] = t(inp["top_k"], np.int32)
+    return dict(
+        **extra,
+        target=rows_to_device(inp["target"], inp["target_dtype"], device, pin=pin),
+        draft=rows_to_device(inp["draft"], inp["draft_dtype"], device, pin=pin),
+        parent=t(inp["parent"], np.int32),
+        tokens=t(inp["tokens"], np.int32),
+        n_nodes=t(inp["n"], np.int32),
+        temperature=t(inp["temperature"], np.float32),
+        top_p=t(inp["top_p"], np.float32),
+        request_id=t(inp["request_id"].view(np.int32), np.int32),
+        seq_len=t(inp["seq_len"], np.int32),
+        seed=int(inp["seed"]),
+        V=int(inp["target"].shape[-1]),
+        draft_kind=inp["draft_kind"],
+    )

@@ -259,6 +259,75 @@ def tiny(V=8, k=3, B=256, T=1.0, top_p=1.0, seed=7, index=9, noise=1.0,
     return inp
 
 
+# --------------------------------------------------------------------------- #
+# token trees
+# --------------------------------------------------------------------------- #
+def tree_shape(shape: str, rng) -> list:
+    """Parents (parent[i - 1] of node i; 0 = the root) of a named tree shape:
+    'chain:k', 'binary:d' (full binary tree of depth d), 'wide:w,d' (w root
+    children, each the head of a chain of depth d), 'random:n' (node i hangs
+    under a uniformly chosen earlier node)."""
+    kind, arg = shape.split(":")
+    if kind == "chain":
+        return list(range(int(arg)))
+    if kind == "binary":
+        par, level = [], [0]
+        for _ in range(int(arg)):
+            nxt = []
+            for p in level:
+                for _ in range(2):
+                    par.append(p)
+                    nxt.append(len(par))
+            level = nxt
+        return par
+    if kind == "wide":
+        w, d = (int(x) for x in arg.split(","))
+        par = []
+        for _ in range(w):
+            par.append(0)
+            for _ in range(d - 1):
+                par.append(len(par))
+        return par
+    if kind == "random":
+        return [int(rng.integers(0, i)) for i in range(1, int(arg) + 1)]
+    raise ValueError(shape)
+
+
+def tree_batch(B=64, V=128256, shape="binary:3", index=6, T=0.8, top_p=0.95, dtype="bf16",
+               draft_kind="logits", ragged=False):
+    """Token-tree verification inputs: one tree per request (the same shape,
+    or ragged node counts), target rows N(0, 3^2) and draft rows target +
+    N(0, 1) per node, children drawn i.i.d. from the draft's own top-p
+    distribution at their parent."""
+    rng = np.random.default_rng(1000 + index)
+    par = tree_shape(shape, rng)
+    N = len(par)
+    inp = dict(B=B, N=N, V=V, target_dtype=dtype, draft_dtype="f32" if draft_kind == "probs" else dtype,
+               draft_kind=draft_kind, seed=2000 + index,
+               parent=np.tile(np.array(par, np.int32), (B, 1)),
+               tokens=np.zeros((B, N), np.int32),
+               n=np.full(B, N, np.int32),
+               temperature=np.full(B, T, np.float32), top_p=np.full(B, top_p, np.float32),
+               request_id=np.arange(B, dtype=np.uint32),
+               seq_len=rng.integers(128, 8193, B).astype(np.int32))
+    if ragged:
+        inp["n"] = rng.integers(0, N + 1, B).astype(np.int32)
+    t = rng.standard_normal((B, N + 1, V), dtype=np.float32) * np.float32(3.0)
+    d = t + rng.standard_normal((B, N + 1, V), dtype=np.float32)
+    if draft_kind == "probs":
+        e = np.exp(d.astype(np.float64) - d.max(axis=-1, keepdims=True))
+        inp["draft"] = (e / e.sum(axis=-1, keepdims=True)).astype(np.float32)
+    else:
+        inp["draft"] = to_bf16_bits(d) if dtype == "bf16" else d
+    inp["target"] = to_bf16_bits(t) if dtype == "bf16" else t
+    srng = np.random.default_rng(3000 + index)
+    for b in range(B):
+        for i in range(1, N + 1):
+            row = _draft_values(inp["draft"][b, par[i - 1]], inp["draft_dtype"])
+            inp["tokens"][b, i - 1] = draft_sample(row, draft_kind, T, top_p, srng)
+    return inp
+
+
 def build(name: str, **kw):
     return {"small_fp32": small_fp32, "paged_bf16": paged_bf16,
             "ragged_probs": ragged_probs, "verify_b64_k4": verify_b64_k4,

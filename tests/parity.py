@@ -119,3 +119,90 @@ def compare_debug(inp, dbg, ref_rows=None):
             assert abs(f[b, j, 3] - rec["p_kept_mass"]) <= 1e-5
             checked += 1
     return checked
+
+
+# --------------------------------------------------------------------------- #
+# token trees
+# --------------------------------------------------------------------------- #
+def _oracle_tree(inp, b, force=None):
+    nb = int(inp["n"][b])
+    tr = S.decode(inp["target"][b, :nb + 1], inp["target_dtype"])
+    dr = S.decode(inp["draft"][b, :nb + 1], inp["draft_dtype"])
+    return S.verify_tree(tr, dr, inp["parent"][b], inp["tokens"][b], nb, inp["temperature"][b],
+                         inp["top_p"][b], inp["draft_kind"], inp["seed"],
+                         int(inp["request_id"][b]), int(inp["seq_len"][b]),
+                         top_k=int(inp["top_k"][b]) if inp.get("top_k") is not None else 0,
+                         force=force)
+
+
+def compare_tree(inp, out, ref=None):
+    """Tree outputs against the oracle: accepted length, path, tokens and
+    status bit-exact, with the same counted tolerances as compare(): a test
+    decided the other way where |u - p_r(y)/q(y)| < TOL (the oracle then
+    follows the GPU's decision), a race near-tie, or a top-p boundary."""
+    acc = out["accepted"].cpu().numpy()
+    pth = out["path"].cpu().numpy()
+    tok = out["out_tokens"].cpu().numpy()
+    nem = out["num_emitted"].cpu().numpy()
+    st = out["status"].cpu().numpy().astype(np.uint32)
+    ref = ref or S.verify_tree_batch(inp)
+    B, N = inp["parent"].shape
+    rep = dict(B=B, exact=0, accept_flips=0, race_ties=0, topp_boundary=0, mismatches=[])
+    for b in range(B):
+        same = (acc[b] == ref["accepted"][b] and (pth[b, :N] == ref["path"][b]).all()
+                and (tok[b] == ref["out_tokens"][b]).all() and nem[b] == ref["num_emitted"][b]
+                and st[b] == ref["status"][b])
+        if same:
+            rep["exact"] += 1
+            continue
+        gp = [int(x) for x in pth[b, :max(acc[b], 0)]]
+        force, ok = {}, False
+        for _ in range(4 * N + 4):
+            r = _oracle_tree(inp, b, force)
+            rp = r["path"]
+            rt = np.full(N + 1, -1, np.int64)
+            rt[:len(r["tokens"])] = r["tokens"]
+            if acc[b] == r["accepted"] and gp == rp and (tok[b] == rt).all():
+                ok = True
+                break
+            if acc[b] < 0 or r["accepted"] < 0:
+                break
+            d = 0
+            while d < min(len(gp), len(rp)) and gp[d] == rp[d]:
+                d += 1
+            if d < len(gp) or d < len(rp):          # a test decided differently
+                parent = 0 if d == 0 else rp[d - 1]
+                want = {gp[d] if d < len(gp) else None, rp[d] if d < len(rp) else None}
+                tests = [t for t in r["tests"] if t.get("parent") == parent and "rank" in t]
+                t = next((t for t in tests if t["node"] in want), None)
+                if t is None:
+                    break
+                if t["q_y"] > 0 and abs(t["u"] - t["p_y"] / t["q_y"]) < TOL:
+                    rep["accept_flips"] += 1
+                    force[(t["node"], t["rank"])] = d < len(gp) and t["node"] == gp[d]
+                    continue
+                if t["p_margin"] < TOL or t["q_margin"] < TOL:
+                    rep["topp_boundary"] += 1
+                    ok = True
+                break
+            last = r["tests"][-1]                   # same path: the correction or bonus
+            g = int(tok[b, len(gp)])
+            if last.get("p_margin", np.inf) < TOL or last.get("q_margin", np.inf) < TOL:
+                rep["topp_boundary"] += 1
+                ok = True
+                break
+            race = last.get("race")
+            if race is not None and 0 <= g < race["w"].size:
+                keys = np.where(race["w"] > 0, race["w"] / race["E"], 0.0)
+                if keys[g] >= keys[race["token"]] * (1 - TOL):
+                    rep["race_ties"] += 1
+                    ok = True
+            break
+        if not ok:
+            rep["mismatches"].append(dict(b=b, gpu=(int(acc[b]), gp, tok[b].tolist(), int(st[b])),
+                                          oracle=(int(ref["accepted"][b]),
+                                                  ref["path"][b].tolist(),
+                                                  ref["out_tokens"][b].tolist(),
+                                                  int(ref["status"][b]))))
+    assert not rep["mismatches"], f"untolerated mismatches: {rep['mismatches'][:4]}"
+    return rep
