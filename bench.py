@@ -332,6 +332,7 @@ def run_ours(args):
     # end to end through the public API with host buffers (pinned)
     e2e = e2e_run(ver, sets, dev, args, pool, table, seq, kk, B, k)
     copy_line = commit_copy_run(ver, sets, outs, dev, peak)
+    tree_line = tree_run(ver, dev, peak)
 
     line = {"metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": ws, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
@@ -352,7 +353,7 @@ def run_ours(args):
                          "frac_of_8tbs": achieved / 8000.0},
             "clocks": clk.summary(),
             "e2e": e2e,
-            "kv_commit_copy": copy_line}
+            "kv_commit_copy": copy_line, "tree_verify": tree_line}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(sets[0])
     if rank == 0:
@@ -448,6 +449,47 @@ def commit_copy_run(ver, sets, outs, dev, peak):
     gbs = nbytes / (us * 1e-6) / 1e9
     return {"us": us, "bytes_per_launch": nbytes, "GB/s": gbs, "peak": peak, "frac": gbs / peak,
             "shape": "32 layers x 8 KV heads x d128 bf16, block 16, staged entries 0..a_b"}
+
+
+def tree_run(ver, dev, peak):
+    """Token-tree verification at the workload's vocabulary: B = 64 full binary
+    trees of depth 3 (14 nodes), V = 128256 bf16, T = 0.8, top-p 0.95.  Bytes
+    needed per call: the target row of every node on the walk and the draft
+    row of every visited node with children."""
+    import torch
+
+    from speculative_decoding_verification_07_gb300 import device_io
+    from speculative_decoding_verification_07_gb300 import workloads as W
+    inp = W.tree_batch(B=64, V=128256, shape="binary:3")
+    d = device_io.tree_to_device(inp, dev)
+    out = ver.tree_outputs(64, inp["parent"].shape[1])
+    for _ in range(3):
+        ver.verify_tree(**d, out=out)
+    torch.cuda.synchronize()
+    n = 20
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n):
+        ver.verify_tree(**d, out=out)
+    e1.record()
+    torch.cuda.synchronize()
+    assert ver.error() == 0, "device error in the tree run"
+    us = e0.elapsed_time(e1) / n * 1e3
+    acc = out["accepted"].cpu().numpy()
+    pth = out["path"].cpu().numpy()
+    V = inp["V"]
+    par = inp["parent"]
+    nbytes = 0
+    for b in range(64):
+        visited = [0] + [int(x) for x in pth[b, :acc[b]]]
+        for j in visited:
+            nbytes += V * 2 + (V * 2 if (par[b] == j).any() else 0)
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"us": us, "requests_per_s": 64 / (us * 1e-6),
+            "tokens_per_s": float((acc + 1).sum()) / (us * 1e-6),
+            "mean_accepted": float(acc.mean()), "bytes_needed_per_call": float(nbytes),
+            "GB/s": gbs, "peak": peak, "frac": gbs / peak,
+            "shape": "64 binary trees of depth 3 (14 nodes), V=128256 bf16, T=0.8, top-p 0.95"}
 
 
 def kernel_source_sha():
