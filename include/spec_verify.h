@@ -308,7 +308,10 @@ sv_status spec_verify_static(const sv_verify_args* args, sv_stream_t stream);
  *   accepted node ids in depth order, then -1; out_tokens [B][N+1] = their
  *   tokens, then the correction or bonus token, then -1; num_emitted [B] =
  *   a_b + 1 (0 on bad input); status [B] (SV_ST_* bits).
- * Each cluster of CTAs walks one request at a time; no workspace is needed.
+ * Each cluster of CTAs walks one request at a time, taking requests from a
+ * counter the handle owns: only one spec_verify_tree call per handle may be in
+ * flight on the GPU at a time (calls in one stream are ordered).  No
+ * workspace is needed.
  */
 #define SV_TREE_MAX_NODES 4096
 typedef struct {

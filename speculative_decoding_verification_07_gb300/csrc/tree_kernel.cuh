@@ -16,8 +16,10 @@
 //
 // The rows of the current node stay in the cluster's shared memory (one TMA
 // bulk copy per row slice); the statistics, the top-k / top-p filters and the
-// exponential race are the linear kernel's.  Requests are independent, so the
-// clusters take them round-robin and never wait on one another.
+// exponential race are the linear kernel's.  Requests are independent: the
+// clusters take them from a ticket counter (walks differ in length, so a
+// cluster that finishes early takes the next request) and never wait on one
+// another.
 #pragma once
 
 #include "verify_kernel.cuh"
@@ -45,6 +47,7 @@ struct TreeParams {
   int32_t* num_emitted;
   uint32_t* status;
   int* err;
+  uint32_t* ctr;  // [2] request ticket and done counters, zero between calls
   int slice, d_off;
 };
 
@@ -228,6 +231,7 @@ template <int EBT, int EBD, bool PROBS>
 __global__ void __launch_bounds__(kThreads, 2) tree_kernel(const TreeParams P) {
   cg::cluster_group cluster = cg::this_cluster();
   __shared__ Smem sm;
+  __shared__ int s_ticket;
   extern __shared__ __align__(128) char dyn[];
   char* s_t = dyn;
   char* s_d = dyn + P.d_off;
@@ -249,8 +253,12 @@ __global__ void __launch_bounds__(kThreads, 2) tree_kernel(const TreeParams P) {
   it.nblk = it.x1 > it.x0 ? (it.x1 - it.x0 + kBlk - 1) / kBlk : 0;
   it.V = P.V;
 
-  const int ncl = (int)gridDim.x / C, cid = (int)blockIdx.x / C;
-  for (int b = cid; b < P.B; b += ncl) {
+  for (;;) {
+    if (lead) s_ticket = (int)atomicAdd(P.ctr, 1u);
+    cluster.sync();  // also: the previous request's shared memory is no longer read
+    const int b = *cluster.map_shared_rank(&s_ticket, 0);
+    cluster.sync();  // every CTA holds b before rank 0 takes the next ticket
+    if (b >= P.B) break;
     const int N = P.N;
     const int n = P.n_nodes ? P.n_nodes[b] : N;
     const float T = P.temperature[b];
@@ -375,6 +383,16 @@ __global__ void __launch_bounds__(kThreads, 2) tree_kernel(const TreeParams P) {
         P.num_emitted[b] = depth + 1;
         P.status[b] = st_bits;
       }
+    }
+  }
+  // the last cluster to finish resets the counters for the next call
+  if (lead) {
+    __threadfence();
+    const uint32_t nclusters = gridDim.x / (uint32_t)C;
+    if (atomicAdd(P.ctr + 1, 1u) == nclusters - 1) {
+      P.ctr[0] = 0u;
+      P.ctr[1] = 0u;
+      __threadfence();
     }
   }
   cluster.sync();  // peers are done reading this CTA's shared memory
