@@ -280,26 +280,36 @@ __global__ void __launch_bounds__(kThreads, 2) tree_kernel(const TreeParams P) {
       }
     bad = __syncthreads_or(bad);
 
-    int cur = 0, depth = 0;
-    uint32_t st_bits = 0u;
-    int emitted = -1;  // the correction or bonus token, once drawn
-    while (!bad && emitted < 0) {
-      cluster.sync();  // the previous node's shared memory is no longer read anywhere
-      const int first = tree_next_child(par, cur, cur + 1, n);
-      const bool has_d = first > 0;
-      const char* trow = P.target + ((size_t)b * (N + 1) + cur) * P.t_ld * EBT;
-      const char* drow = P.draft + ((size_t)b * (N + 1) + cur) * P.d_ld * EBD;
+    // A node's rows head for shared memory as soon as the node is known (at
+    // the request's start, or when its parent's test accepts it): every read
+    // of the slices by this CTA lies before a barrier thread 0 has passed.
+    auto issue = [&](int node) -> int {  // returns the node's first child (0: none)
+      const int fc = tree_next_child(par, node, node + 1, n);
       if (tid == 0 && it.nblk > 0) {
+        const char* tr = P.target + ((size_t)b * (N + 1) + node) * P.t_ld * EBT;
+        const char* dr = P.draft + ((size_t)b * (N + 1) + node) * P.d_ld * EBD;
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         const uint32_t bt = (uint32_t)(((it.x1 - it.x0) * EBT + 15) & ~15);
         mbar_expect_tx(&sm.bar[0], bt);
-        bulk_g2s(s_t, trow + (size_t)it.x0 * EBT, bt, &sm.bar[0]);
-        if (has_d) {
+        bulk_g2s(s_t, tr + (size_t)it.x0 * EBT, bt, &sm.bar[0]);
+        if (fc) {
           const uint32_t bd = (uint32_t)(((it.x1 - it.x0) * EBD + 15) & ~15);
           mbar_expect_tx(&sm.bar[1], bd);
-          bulk_g2s(s_d, drow + (size_t)it.x0 * EBD, bd, &sm.bar[1]);
+          bulk_g2s(s_d, dr + (size_t)it.x0 * EBD, bd, &sm.bar[1]);
         }
       }
+      return fc;
+    };
+
+    int cur = 0, depth = 0;
+    uint32_t st_bits = 0u;
+    int emitted = -1;  // the correction or bonus token, once drawn
+    int first = bad ? 0 : issue(0);
+    while (!bad && emitted < 0) {
+      cluster.sync();  // the previous node's shared memory is no longer read anywhere
+      const bool has_d = first > 0;
+      const char* trow = P.target + ((size_t)b * (N + 1) + cur) * P.t_ld * EBT;
+      const char* drow = P.draft + ((size_t)b * (N + 1) + cur) * P.d_ld * EBD;
       bool landed = true;
       if (it.nblk > 0) {
         landed &= mbar_wait(&sm.bar[0], phase_t, P.err);
@@ -358,6 +368,7 @@ __global__ void __launch_bounds__(kThreads, 2) tree_kernel(const TreeParams P) {
         if (lead) o_path[depth] = taken, o_tok[depth] = tok[taken - 1];
         cur = taken;
         ++depth;
+        first = issue(cur);
         continue;
       }
       // every child rejected: the correction from the last residual (from p
