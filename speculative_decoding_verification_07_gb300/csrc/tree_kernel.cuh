@@ -86,11 +86,15 @@ __device__ __forceinline__ float tree_cluster_sum(cg::cluster_group& cluster, Sm
 
 // Statistics of the current node's target row (and draft row when has_d):
 // raw maxima, then weight sums relative to them, each reduced across the
-// cluster in a fixed order.  Returns false when a row is unusable.
+// cluster in a fixed order.  With win_t / win_d (bf16 logit rows under
+// top-p alone) the sums sweep also counts the first top-p window into
+// sm.hist[0], its floor taken from a lower bound of S known after the maxima
+// (as in the linear kernel).  Returns false when a row is unusable.
 template <int EBT, int EBD, bool PROBS>
 __device__ bool tree_node_stats(cg::cluster_group& cluster, Smem& sm, const char* s_t,
                                 const char* s_d, const SliceIter& it, bool has_d, float T,
-                                bool landed, RowP& rt, RowP& rd) {
+                                float top_p, bool win_t, bool win_d, bool landed, RowP& rt,
+                                RowP& rd) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int C = (int)cluster.num_blocks();
   const bool greedy = T == 0.0f;
@@ -118,17 +122,21 @@ __device__ bool tree_node_stats(cg::cluster_group& cluster, Smem& sm, const char
   rmt = max_value<EBT>(mt2, rmt);
   rmd = max_value<EBD>(md2, rmd);
   const float md = (PROBS && !greedy) ? (rmd > 0.0f ? lg2(rmd) * rd.invT : -INFINITY) : rmd;
+  if (win_t || win_d)
+    for (int j = threadIdx.x; j < 512; j += kThreads) (&sm.hist[0][0][0])[j] = 0u;
   {
-    float Mt = rmt, Md = md, Rm = rmd;
+    // every thread's own maximum weighs 1 relative to itself: the sum over
+    // threads of 2^((m_thread - M) c) is a lower bound of S
+    float Mt = rmt, Lt = rmt == -INFINITY ? 0.0f : 1.0f;
+    float Md = md, Ld = md == -INFINITY ? 0.0f : 1.0f;
+    warp_ms(Mt, Lt, rt.c, greedy);
+    warp_ms(Md, Ld, rd.c, greedy);
+    float Rm = rmd;
 #pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      Mt = fmaxf(Mt, __shfl_xor_sync(0xffffffffu, Mt, o));
-      Md = fmaxf(Md, __shfl_xor_sync(0xffffffffu, Md, o));
-      Rm = fmaxf(Rm, __shfl_xor_sync(0xffffffffu, Rm, o));
-    }
+    for (int o = 16; o; o >>= 1) Rm = fmaxf(Rm, __shfl_xor_sync(0xffffffffu, Rm, o));
     const bool warp_bad = __any_sync(0xffffffffu, !landed);
     if (lane == 0)
-      sm.part[warp] = {make_float4(Mt, 0.0f, Rm, warp_bad ? 1.0f : 0.0f), make_float4(Md, 0.0f, 0.0f, 0.0f)};
+      sm.part[warp] = {make_float4(Mt, Lt, Rm, warp_bad ? 1.0f : 0.0f), make_float4(Md, Ld, 0.0f, 0.0f)};
   }
   __syncthreads();
   if (warp == 0) {
@@ -138,30 +146,68 @@ __device__ bool tree_node_stats(cg::cluster_group& cluster, Smem& sm, const char
   }
   cluster.sync();
   bool slice_bad;
+  float St_lb, Sd_lb;
   {
     const StatPart c = combine_parts(
         lane < C ? cluster.map_shared_rank(&sm, lane)->cpart : neutral_part<PROBS>(), rt.c, rd.c, greedy);
     rt.m = rt.mz = c.a.x;
     rd.m = c.a.z;
     rd.mz = c.d.x;
+    St_lb = c.a.y, Sd_lb = c.d.y;
     slice_bad = c.a.w != 0.0f;
   }
   rt.kmax = vkey<EBT>(rt.m);
   rd.kmax = vkey<EBD>(rd.m);
+  uint32_t thr2_t = 0x7FFF7FFFu, thr2_d = 0x7FFF7FFFu;  // NaN pairs: nothing passes
+  const int nguess = min(it.V, kWindowGuess);
+  if (win_t) {
+    RowP q = rt;
+    q.S = St_lb;
+    thr2_t = bf16_pair_of(vkey_value<2>(window_lo_key(q, top_p, nguess)));
+  }
+  if (win_d) {
+    RowP q = rd;
+    q.S = Sd_lb;
+    thr2_d = bf16_pair_of(vkey_value<2>(window_lo_key(q, top_p, nguess)));
+  }
 
   float st = 0.0f, sd = 0.0f;
+  uint32_t wt_lo = 0u, wt_hi = 0u, wd_lo = 0u, wd_hi = 0u;
+  int wt_n = 0, wd_n = 0;
   for (int blk = 0; blk < it.nblk; ++blk) {
     const int x = it.x(blk);
     if (x < it.x1) {
       Grp<EBT> g;
       lds_group<EBT, false>(g, s_t, it.x0, x, it.x1);
       st += sum_group<EBT, false>(g, greedy, rt.mz, rt.c, rt.invT);
+      if constexpr (EBT == 2) {
+        if (win_t) {
+          const uint32_t m = window_bits_bf16(make_uint4(g.w[0], g.w[1], g.w[2], g.w[3]), thr2_t, x, it.x1);
+          wt_n += __popc(m);
+          if (blk < 4) wt_lo |= m << (8 * blk);
+          else wt_hi |= m << (8 * (blk - 4));
+        }
+      }
       if (has_d) {
         Grp<EBD> h;
         lds_group<EBD, PROBS>(h, s_d, it.x0, x, it.x1);
         sd += sum_group<EBD, PROBS>(h, greedy, rd.mz, rd.c, rd.invT);
+        if constexpr (EBD == 2 && !PROBS) {
+          if (win_d) {
+            const uint32_t m = window_bits_bf16(make_uint4(h.w[0], h.w[1], h.w[2], h.w[3]), thr2_d, x, it.x1);
+            wd_n += __popc(m);
+            if (blk < 4) wd_lo |= m << (8 * blk);
+            else wd_hi |= m << (8 * (blk - 4));
+          }
+        }
       }
     }
+  }
+  if constexpr (EBT == 2) {
+    if (win_t) window_commit_bf16(s_t, rt.kmax, wt_lo, wt_hi, wt_n, it, sm.hist[0][0], sm.wb.bin[warp]);
+  }
+  if constexpr (EBD == 2 && !PROBS) {
+    if (win_d) window_commit_bf16(s_d, rd.kmax, wd_lo, wd_hi, wd_n, it, sm.hist[0][1], sm.wb.bin[warp]);
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
@@ -318,15 +364,19 @@ __global__ void __launch_bounds__(kThreads, 2) tree_kernel(const TreeParams P) {
         if (has_d) phase_d ^= 1u;
       }
       RowP rt, rd;
-      if (!tree_node_stats<EBT, EBD, PROBS>(cluster, sm, s_t, s_d, it, has_d, T, landed, rt, rd)) {
+      const bool greedy = T == 0.0f;
+      const bool topk = !greedy && top_k > 0 && top_k < P.V;
+      // bf16 logit rows under top-p alone count their first window in the sums sweep
+      const bool topp = !greedy && !topk && top_p < 1.0f;
+      const bool win_t = EBT == 2 && topp, win_d = EBD == 2 && !PROBS && topp && has_d;
+      if (!tree_node_stats<EBT, EBD, PROBS>(cluster, sm, s_t, s_d, it, has_d, T, top_p, win_t, win_d,
+                                            landed, rt, rd)) {
         bad = true;
         break;
       }
-      const bool greedy = T == 0.0f;
-      const bool topk = !greedy && top_k > 0 && top_k < P.V;
-      if (topk || (!greedy && top_p < 1.0f))
+      if (topk || topp)
         filter_rows<EBT, EBD, PROBS>(cluster, sm, s_t, s_d, it, has_d, top_p, topk ? top_k : 0, rt,
-                                     rd, false, false);
+                                     rd, win_t, win_d);
       const uint32_t pos = (uint32_t)(S + depth + 1);
       RacePart best = {0.0f, 1.0f, 0x7FFFFFFF};
       if (!has_d) {  // a leaf: the bonus from p
@@ -355,13 +405,15 @@ __global__ void __launch_bounds__(kThreads, 2) tree_kernel(const TreeParams P) {
           break;
         }
         c += W;
+        const int jn = tree_next_child(par, cur, j + 1, n);
+        if (!jn) break;  // the last child: the correction needs c, not the new W
         rdc.invZ = c * rd.invZ;
         W = tree_cluster_sum(cluster, sm, tree_residual_part<EBT, EBD, PROBS>(s_t, s_d, it, rt, rdc));
         if (!(W > 0.0f)) {
           empty = true;
           break;
         }
-        j = tree_next_child(par, cur, j + 1, n);
+        j = jn;
         ++r;
       }
       if (taken) {
@@ -372,12 +424,23 @@ __global__ void __launch_bounds__(kThreads, 2) tree_kernel(const TreeParams P) {
         continue;
       }
       // every child rejected: the correction from the last residual (from p
-      // when that residual is numerically empty)
+      // when that residual is numerically empty: found while testing, or as a
+      // race whose winner weighs nothing)
       RowP rdc = rd;
       rdc.invZ = c * rd.invZ;
-      if (empty) st_bits |= SV_ST_RESIDUAL_EMPTY;
-      race_slice<EBT, EBD, PROBS>(s_t, s_d, it, !empty, rt, rdc, pos, rid, k0, k1, sm.wb.idx[warp], best);
-      emitted = race_reduce(cluster, sm, best, 0).idx;
+      RacePart win = {0.0f, 1.0f, 0x7FFFFFFF};
+      if (!empty) {
+        race_slice<EBT, EBD, PROBS>(s_t, s_d, it, true, rt, rdc, pos, rid, k0, k1, sm.wb.idx[warp], best);
+        win = race_reduce(cluster, sm, best, 0);
+        empty = !(win.w > 0.0f);
+      }
+      if (empty) {
+        st_bits |= SV_ST_RESIDUAL_EMPTY;
+        best = {0.0f, 1.0f, 0x7FFFFFFF};
+        race_slice<EBT, EBD, PROBS>(s_t, s_d, it, false, rt, rd, pos, rid, k0, k1, sm.wb.idx[warp], best);
+        win = race_reduce(cluster, sm, best, 1);
+      }
+      emitted = win.idx;
     }
     if (lead) {
       if (bad) {

@@ -172,3 +172,25 @@ def test_tree_commit_gathers_the_path_bit_exact(ver):
     KC.commit_copy(stage.float().cpu().numpy(), acc.cpu().numpy(), seq0.cpu().numpy(),
                    table.cpu().numpy(), kv_ref, BS, path=out["path"].cpu().numpy())
     np.testing.assert_array_equal(kv.float().cpu().numpy(), kv_ref)
+
+
+def test_tree_empty_residual(ver):
+    """q = p at the root and proposals outside their support: each test rejects
+    (q(y) = 0, p(y) = 0) and max(0, p - q) is empty, after the last child
+    (request 0, one child) or before it (request 1, two children); the
+    correction then comes from p with SV_ST_RESIDUAL_EMPTY and SV_ST_Q_ZERO."""
+    NEG = -np.inf
+    B, V, N = 2, 4, 2
+    t = np.zeros((B, N + 1, V), np.float32)
+    t[:, 0] = [NEG, 0.0, 0.0, 0.0]
+    inp = dict(B=B, N=N, V=V, target_dtype="f32", draft_dtype="f32", draft_kind="logits", seed=5,
+               parent=np.zeros((B, N), np.int32), tokens=np.zeros((B, N), np.int32),
+               n=np.array([1, 2], np.int32), temperature=np.ones(B, np.float32),
+               top_p=np.ones(B, np.float32), request_id=np.arange(B, dtype=np.uint32),
+               seq_len=np.full(B, 3, np.int32), target=t, draft=t.copy())
+    out = run_tree(ver, inp)
+    parity.compare_tree(inp, out)
+    st = out["status"].cpu().numpy()
+    assert (st == binding.ST_Q_ZERO | binding.ST_RESIDUAL_EMPTY).all()
+    assert (out["accepted"].cpu().numpy() == 0).all()
+    assert np.isin(out["out_tokens"].cpu().numpy()[:, 0], [1, 2, 3]).all()
