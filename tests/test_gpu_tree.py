@@ -49,6 +49,7 @@ def report(name, rep):
     ("binary:2", {"dtype": "f32", "V": 1024, "T": 1.0, "top_p": 1.0}),
     ("wide:3,2", {"draft_kind": "probs", "V": 32000}),
     ("random:12", {"T": 0.0, "top_p": 1.0, "V": 151936}),
+    ("random:300", {"B": 8, "V": 32000}),
 ])
 def test_tree_parity(ver, shape, kw):
     args = dict(B=48, V=128256)

@@ -459,3 +459,22 @@ def test_host_checks_launch_nothing(ver):
     assert e.value.code == binding.SV_ERR_INVALID
     empty = {k: (v[:0] if isinstance(v, torch.Tensor) else v) for k, v in dev.items()}
     ver.verify(**empty)                                   # B = 0 is a no-op
+
+
+def test_maximum_sizes(ver):
+    """The largest k (64, every draft accepted: 65 rows per request, none
+    skipped), the largest vocabulary one cluster holds (16 CTAs x 16384 =
+    262144), and k = 65 refused by the host checks."""
+    inp = W.sweep(B=4, V=32000, sigma=0.0, k=64)
+    out, _, _, _ = run(ver, inp)
+    rep = parity.compare(inp, out)
+    report("k=64", rep)
+    assert (out["accepted"].cpu().numpy() == 64).all()
+    inp = W.sweep(B=3, V=262144, sigma=0.5, k=2)
+    out, _, _, _ = run(ver, inp)
+    report("V=262144", parity.compare(inp, out))
+    big = W.sweep(B=1, V=64, sigma=0.5, k=65)
+    dev = device_io.to_device(big, "cuda:0")
+    with pytest.raises(binding.SvError) as e:
+        ver.verify(**dev)
+    assert e.value.code == binding.SV_ERR_INVALID
