@@ -22,7 +22,7 @@ State (all plain arrays, mirrored bit for bit by the CUDA path):
   free_stack [num_blocks] int32, free_top, refcount [num_blocks] int32,
   block_table [B][max_blocks] int32 (-1 = no block), seq_len [B] int32.
 
-Readings (listed in DESIGN.md):
+Readings:
   * seq_len S_b counts processed tokens; the pending token sits at position
     S_b.  The verify pass processes positions S_b .. S_b + k_b, so it needs
     blocks covering [0, S_b + k_b + 1).

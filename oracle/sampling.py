@@ -18,7 +18,7 @@ Per request b with k_b drafts the walk is ([SD] section 2):
   drawn from p_{k_b}.  Both draws are exponential races argmax_x w_x / E_x,
   which sample x with probability w_x / sum(w).
 
-Readings taken where the pages leave a step open (each also listed in the design doc):
+Readings taken where the pages leave a step open:
   * transforms ([SD] sections 3, 4, 6: acceptance uses "the exact transformed
     distributions"): z = logit / T, or ln(prob) / T for draft probabilities;
     dist = softmax(z).  T = 0 is the limit T -> 0+: uniform over the tied
