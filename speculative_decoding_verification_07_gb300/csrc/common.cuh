@@ -11,9 +11,7 @@
 struct sv_handle {
   int device;
   int num_sms;
-  int* d_err;  // 256 device bytes: word 0 the error word (0 or the first sv_status a
-               // kernel reported); bytes 128..135 the tree kernel's request ticket
-               // and done counters (zero between calls)
+  int* d_err;  // device error word: 0 or the first sv_status a kernel reported
   // launch cache: co-resident clusters per (kernel, cluster size), filled on
   // first use so later calls (and stream capture) make no occupancy query
   static constexpr int kCache = 32;

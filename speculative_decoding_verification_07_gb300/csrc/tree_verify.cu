@@ -72,6 +72,8 @@ extern "C" sv_status spec_verify_tree(sv_handle* h, const sv_tree_args* a, sv_st
   P.accepted = a->accepted, P.path = a->path, P.out_tokens = a->out_tokens;
   P.num_emitted = a->num_emitted, P.status = a->status;
   P.err = h->d_err;
+  // the handle's 256 device bytes hold the error word at offset 0 and, at
+  // offset 128, the request ticket and done counters (zero between calls)
   P.ctr = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(h->d_err) + 128);
   P.slice = slice, P.d_off = d_off;
 
