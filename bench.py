@@ -240,7 +240,7 @@ def run_ours(args):
     for d in dsets:
         d["request_id"] = replicas.rank_request_ids(d["request_id"], rank)
     BS = 16
-    steps_total = args.warmup + args.steps + 64 * 4 + 16
+    steps_total = args.warmup + args.steps + 64 * 6 + 16
     max_blocks = (8192 + (k + 1) * steps_total) // BS + 4
     pool = binding.BlockPool(ver.handle, B * max_blocks, BS)
     table = torch.full((B, max_blocks), -1, dtype=torch.int32, device=dev)
@@ -251,13 +251,20 @@ def run_ours(args):
     kk = dsets[0]["k"]
     outs = [ver.outputs(B, k) for _ in range(N_SETS)]
     ev = {}
+    evs = {}
 
-    def step(i, stream=None, timed_verify=False):
+    def step(i, stream=None, timed_verify=False, top_p=None, timed_small=False):
         d = dsets[i % N_SETS]
         o = outs[i % N_SETS]
+        if timed_small:
+            torch.cuda._sleep(200_000)
+            evs[i][0].record()
         pool.reserve(seq, kk, table, stream=stream)
+        if timed_small:
+            evs[i][1].record()
         a = binding.make_args(target=d["target"], draft=d["draft"], draft_tokens=d["draft_tokens"],
-                              temperature=d["temperature"], k=d["k"], top_p=d["top_p"],
+                              temperature=d["temperature"], k=d["k"],
+                              top_p=d["top_p"] if top_p is None else top_p,
                               seed=d["seed"], request_id=d["request_id"], seq_len=seq,
                               draft_kind="logits", **o)
         wsp = ver.ensure_workspace(a)
@@ -269,7 +276,11 @@ def run_ours(args):
         binding.spec_verify(ver.handle, a, wsp, stream)
         if timed_verify:
             ev[i][1].record()
+        if timed_small:
+            evs[i][2].record()
         pool.commit_rollback(kk, o["accepted"], seq, table, stream=stream)
+        if timed_small:
+            evs[i][3].record()
 
     # warm-up (eager), then capture a graph of G steps cycling the input sets
     for i in range(max(args.warmup, 3)):
@@ -319,6 +330,21 @@ def run_ours(args):
                           for i in range(N_SETS)]))
     peak, peak_src = measured_peaks()
     achieved = bfull / (vms / 1e3) / 1e9
+    # the same kernel with top_p = 1 on p and q (no nucleus filter)
+    ones = torch.ones(B, dtype=torch.float32, device=dev)
+    for i in range(nv):
+        step(i, timed_verify=True, top_p=ones)
+    torch.cuda.synchronize()
+    vms1 = float(np.mean([ev[i][0].elapsed_time(ev[i][1]) for i in range(nv)]))
+    # the step's two small kernels on their own
+    for i in range(nv):
+        evs[i] = tuple(torch.cuda.Event(enable_timing=True) for _ in range(4))
+    for i in range(nv):
+        step(i, timed_small=True)
+    torch.cuda.synchronize()
+    reserve_us = float(np.mean([evs[i][0].elapsed_time(evs[i][1]) for i in range(nv)])) * 1e3
+    commit_us = float(np.mean([evs[i][2].elapsed_time(evs[i][3]) for i in range(nv)])) * 1e3
+    assert ver.error() == 0, "device error in the kernel timings"
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "verify_traffic.json")
     if os.path.exists(tpath):
@@ -351,6 +377,9 @@ def run_ours(args):
                          "achieved_needed": bmin / (vms / 1e3) / 1e9,
                          "peak_source": peak_src,
                          "frac_of_8tbs": achieved / 8000.0},
+            "verify_top_p_1": {"kernel_ms": vms1, "achieved": bfull / (vms1 / 1e3) / 1e9,
+                               "frac": bfull / (vms1 / 1e3) / 1e9 / peak},
+            "small_kernels_us": {"bfl_reserve": reserve_us, "kv_commit_rollback": commit_us},
             "clocks": clk.summary(),
             "e2e": e2e,
             "kv_commit_copy": copy_line, "tree_verify": tree_line}

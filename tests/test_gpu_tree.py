@@ -195,3 +195,20 @@ def test_tree_empty_residual(ver):
     assert (st == binding.ST_Q_ZERO | binding.ST_RESIDUAL_EMPTY).all()
     assert (out["accepted"].cpu().numpy() == 0).all()
     assert np.isin(out["out_tokens"].cpu().numpy()[:, 0], [1, 2, 3]).all()
+
+
+def test_tree_repeated_calls_and_many_requests(ver):
+    """The clusters take requests from a counter the handle owns, reset by the
+    last cluster of each call: back-to-back calls (with a linear call between
+    them) and a batch of 600 requests (many per cluster) all match the oracle."""
+    a = W.tree_batch(B=600, V=1000, shape="wide:3,2", index=21)
+    b = W.tree_batch(B=40, V=4093, shape="random:9", index=22, ragged=True)
+    out_a = run_tree(ver, a)
+    lin = W.tiny(V=64, k=3, B=16)
+    ver.verify(**device_io.to_device(lin, "cuda:0"))
+    out_b = run_tree(ver, b)
+    out_a2 = run_tree(ver, a)
+    report("600 requests", parity.compare_tree(a, out_a))
+    report("after a linear call", parity.compare_tree(b, out_b))
+    for key in ("accepted", "path", "out_tokens", "status"):
+        assert torch.equal(out_a[key], out_a2[key]), key
