@@ -72,6 +72,14 @@ typedef enum { SV_DRAFT_LOGITS = 0, SV_DRAFT_PROBS = 1 } sv_draft_kind;
 
 /* sv_verify_args.flags */
 #define SV_FLAG_NO_SKIP 1u /* also process rows after a known rejection (debug) */
+/* Testing aid for the bounded waits: row 0 of request 0 never publishes its
+ * decision, and the waits for earlier rows' decisions give up after 1024 polls
+ * (about 0.25 ms) instead of about 2^20.  A later row of request 0 that needs
+ * row 0's decision then reports SV_ST_TIMEOUT for the request and
+ * SV_ERR_TIMEOUT in the error word; the context stays usable.  Meant for
+ * inputs where row 0 of request 0 is accepted (its outputs are otherwise
+ * written by row 0 itself and may be overwritten by the later row's report). */
+#define SV_FLAG_TEST_WITHHOLD 2u
 
 /* sv_row_debug.state */
 #define SV_ROW_NONE 0

@@ -110,7 +110,7 @@ extern "C" sv_status spec_verify(sv_handle* h, const sv_verify_args* a, void* ws
   P.row_state = (uint32_t*)((char*)ws + kHdrBytes);
   P.err = h->d_err;
   P.slice = slice, P.d_off = d_off, P.n_tickets = (int)n_tickets;
-  P.spin_limit = kDefaultSpin;
+  P.spin_limit = (a->flags & SV_FLAG_TEST_WITHHOLD) ? 1024 : kDefaultSpin;
   P.eos = a->eos_id, P.max_new = a->max_new;
   P.top_k = a->top_k;
   P.rep_penalty = a->rep_penalty, P.rep_tokens = a->rep_tokens;

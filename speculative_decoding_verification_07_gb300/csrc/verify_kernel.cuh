@@ -1705,7 +1705,7 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
     } else {
       state = SV_ROW_BONUS;
     }
-    if (lead) {
+    if (lead && !((P.flags & SV_FLAG_TEST_WITHHOLD) && row_t == 0)) {
       st_relaxed(P.row_state + row_t, tag | (qzero ? kQZeroBit : 0u) | (uint32_t)state);
       if (P.debug) {
         sv_row_debug d;

@@ -154,7 +154,7 @@ extern "C" sv_status spec_verify_static(const sv_verify_args* a, sv_stream_t str
   P.row_state = (uint32_t*)((char*)d->ws + kHdrBytes);
   P.err = nullptr;  // no handle: device conditions go to the status bits only
   P.slice = slice, P.d_off = d_off, P.n_tickets = (int)rows;
-  P.spin_limit = kDefaultSpin;
+  P.spin_limit = (a->flags & SV_FLAG_TEST_WITHHOLD) ? 1024 : kDefaultSpin;
   P.eos = a->eos_id, P.max_new = a->max_new;
   P.top_k = a->top_k;
   P.rep_penalty = a->rep_penalty, P.rep_tokens = a->rep_tokens;

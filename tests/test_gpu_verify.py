@@ -478,3 +478,32 @@ def test_maximum_sizes(ver):
     with pytest.raises(binding.SvError) as e:
         ver.verify(**dev)
     assert e.value.code == binding.SV_ERR_INVALID
+
+
+def test_bounded_wait_reports_timeout(ver):
+    """Failure detection without a fault: with SV_FLAG_TEST_WITHHOLD, row 0 of
+    request 0 (accepted: q = p there) never publishes its decision, so row 1
+    (rejected: p(y_1) = 0) waits for it until its bound runs out.  The request
+    reports SV_ST_TIMEOUT, the error word SV_ERR_TIMEOUT, every other request
+    is unaffected, and the next plain call on the same handle is correct."""
+    inp = W.paged_bf16()                      # request 1: q = p at row 0, rejects at row 1
+    for key in ("target", "draft", "tokens"):
+        inp[key][0] = inp[key][1]
+    inp["temperature"][0] = inp["temperature"][1]
+    ref = S.verify_batch(inp)
+    assert ref["accepted"][0] == 1
+    dev = device_io.to_device(inp, "cuda:0")
+    out = ver.verify(**dev, flags=binding.FLAG_TEST_WITHHOLD)
+    torch.cuda.synchronize()
+    assert ver.error() == binding.SV_ERR_TIMEOUT
+    acc = out["accepted"].cpu().numpy()
+    st = out["status"].cpu().numpy()
+    assert acc[0] == -1 and st[0] == binding.ST_TIMEOUT
+    assert (out["out_tokens"][0] == -1).all()
+    np.testing.assert_array_equal(acc[1:], ref["accepted"][1:])
+    np.testing.assert_array_equal(out["out_tokens"].cpu().numpy()[1:], ref["out_tokens"][1:])
+    out2 = ver.verify(**dev)
+    torch.cuda.synchronize()
+    assert ver.error() == 0
+    np.testing.assert_array_equal(out2["accepted"].cpu().numpy(), ref["accepted"])
+    np.testing.assert_array_equal(out2["out_tokens"].cpu().numpy(), ref["out_tokens"])
