@@ -507,3 +507,27 @@ def test_bounded_wait_reports_timeout(ver):
     assert ver.error() == 0
     np.testing.assert_array_equal(out2["accepted"].cpu().numpy(), ref["accepted"])
     np.testing.assert_array_equal(out2["out_tokens"].cpu().numpy(), ref["out_tokens"])
+
+
+def _subset(inp, idx):
+    """The requests idx of a workload (every per-request array sliced)."""
+    out = dict(inp)
+    B = inp["k"].shape[0]
+    for key, v in inp.items():
+        if isinstance(v, np.ndarray) and v.ndim >= 1 and v.shape[0] == B:
+            out[key] = v[idx]
+    out["B"] = len(idx)
+    return out
+
+
+@pytest.mark.parametrize("B,V,sigma", [(1024, 32000, 1.0), (256, 128256, 0.25), (64, 256000, 4.0)])
+def test_sweep_full_size_sampled(ver, B, V, sigma):
+    """The bandwidth sweep at full batch sizes (k = 8): the whole batch in one
+    launch, 48 sampled requests compared with the oracle one by one."""
+    inp = W.sweep(B=B, V=V, sigma=sigma, k=8)
+    out, _, _, _ = run(ver, inp)
+    idx = np.sort(np.random.default_rng(B + V).choice(B, 48, replace=False))
+    sub = _subset(inp, idx)
+    sub_out = {key: v[torch.as_tensor(idx, device=v.device)] for key, v in out.items()}
+    report(f"sweep B={B} V={V} sigma={sigma} (48 sampled)", parity.compare(sub, sub_out))
+    assert (out["accepted"].cpu().numpy() >= 0).all()
