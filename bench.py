@@ -306,6 +306,8 @@ def run_ours(args):
     t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
+    nvtx = _Nvtx()
+    nvtx.range_push("timed steps (graph replays)")
     with ClockSampler(local) as clk, torch.cuda.stream(s):
         t0e.record(s)
         for _ in range(reps):
@@ -317,7 +319,9 @@ def run_ours(args):
     assert ver.error() == 0, "device error in the timed region"
     value, ms = replicas.whole_job_rate(ms, rows * K, device=dev)
 
+    nvtx.range_pop()
     # verify-kernel duration: CUDA events around each launch of G more steps
+    nvtx.range_push("per-launch kernel timings")
     nv = 4 * G
     for i in range(nv):
         ev[i] = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -356,9 +360,16 @@ def run_ours(args):
             traffic = None
 
     # end to end through the public API with host buffers (pinned)
+    nvtx.range_pop()
+    nvtx.range_push("end to end with host buffers")
     e2e = e2e_run(ver, sets, dev, args, pool, table, seq, kk, B, k)
+    nvtx.range_pop()
+    nvtx.range_push("commit by copy")
     copy_line = commit_copy_run(ver, sets, outs, dev, peak)
+    nvtx.range_pop()
+    nvtx.range_push("token trees")
     tree_line = tree_run(ver, dev, peak)
+    nvtx.range_pop()
 
     line = {"metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": ws, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
@@ -503,6 +514,28 @@ def commit_copy_run(ver, sets, outs, dev, peak):
     gbs = nbytes / (us * 1e-6) / 1e9
     return {"us": us, "bytes_per_launch": nbytes, "GB/s": gbs, "peak": peak, "frac": gbs / peak,
             "shape": "32 layers x 8 KV heads x d128 bf16, block 16, staged entries 0..a_b"}
+
+
+class _Nvtx:
+    """NVTX ranges around the bench's phases, for a profiler's timeline; a
+    no-op where this torch build has no NVTX."""
+
+    def __init__(self):
+        import torch
+        try:
+            torch.cuda.nvtx.range_push("probe")
+            torch.cuda.nvtx.range_pop()
+            self._n = torch.cuda.nvtx
+        except Exception:
+            self._n = None
+
+    def range_push(self, msg):
+        if self._n is not None:
+            self._n.range_push(msg)
+
+    def range_pop(self):
+        if self._n is not None:
+            self._n.range_pop()
 
 
 def tree_run(ver, dev, peak):
