@@ -531,3 +531,21 @@ def test_sweep_full_size_sampled(ver, B, V, sigma):
     sub_out = {key: v[torch.as_tensor(idx, device=v.device)] for key, v in out.items()}
     report(f"sweep B={B} V={V} sigma={sigma} (48 sampled)", parity.compare(sub, sub_out))
     assert (out["accepted"].cpu().numpy() >= 0).all()
+
+
+def test_all_options_together(ver):
+    """Repetition penalty, top-k, top-p, EOS ids and output caps in one batch:
+    the penalty comes first, then temperature, top-k and top-p; EOS and the cap
+    end the walk."""
+    inp = W.verify_b64_k4(B=48, V=32000)
+    rng = np.random.default_rng(31)
+    _add_repetition_penalty(inp, 32, H=120)
+    inp["top_k"] = rng.choice(np.array([0, 3, 40, 700, 9000], np.int32), 48)
+    eos = np.full(48, -1, np.int32)
+    pick = rng.random(48) < 0.5
+    eos[pick] = inp["tokens"][pick, rng.integers(0, 4, pick.sum())]
+    inp["eos"] = eos
+    inp["max_new"] = rng.integers(1, 7, 48).astype(np.int32)
+    out, dbg, _, _ = run(ver, inp, debug=True)
+    report("all options", parity.compare(inp, out))
+    assert parity.compare_debug(inp, dbg) > 0

@@ -10,6 +10,7 @@ passes both alone in a fresh process and after the other GPU tests.
 
 import os
 
+import numpy as np
 import pytest
 import torch
 
@@ -54,8 +55,16 @@ def test_static_scratch_matches_workspace_path(ver):
     # (name, inputs, flags, per-row probabilities requested); the per-row
     # probabilities are compared only with row skipping off, since which rows
     # are skipped depends on timing
+    opts = W.verify_b64_k4(B=32, V=32000)
+    rng = np.random.default_rng(3)
+    opts["top_k"] = rng.choice(np.array([0, 5, 50, 500], np.int32), 32)
+    opts["eos"] = opts["tokens"][:, 1].copy()
+    opts["max_new"] = rng.integers(1, 6, 32).astype(np.int32)
+    opts["rep_penalty"] = rng.choice(np.array([1.0, 1.3], np.float32), 32)
+    opts["rep_tokens"] = rng.integers(-1, 32000, (32, 40)).astype(np.int32)
     batches = [("verify B=64 k=4 V=128256 bf16", W.verify_b64_k4(), 0, False),
-               ("paged bf16 V=32000, no skip", W.paged_bf16(), binding.FLAG_NO_SKIP, True)]
+               ("paged bf16 V=32000, no skip", W.paged_bf16(), binding.FLAG_NO_SKIP, True),
+               ("top-k, EOS, caps, repetition penalty", opts, 0, False)]
     devs = [device_io.to_device(inp, "cuda:0") for _, inp, _, _ in batches]
 
     # the existing entry point, with its own zero-filled workspace
