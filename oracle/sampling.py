@@ -346,7 +346,7 @@ def tree_children(parent, n):
 
 
 def verify_tree(target_rows, draft_rows, parent, tokens, n, T, top_p, draft_kind, seed,
-                request_id, seq_len, top_k=0, force=None):
+                request_id, seq_len, top_k=0, force=None, eos=-1, cap=None):
     """Verify one request's token tree ([CV] paragraph 3: a tree implementation
     keeps the accepted path; paragraph 5: test tree branch switches).
 
@@ -368,6 +368,10 @@ def verify_tree(target_rows, draft_rows, parent, tokens, n, T, top_p, draft_kind
     tests among j's children use pos = S + d_j + 1 and sibling rank r - 1 as
     the uniform's slot; the correction or bonus after node j uses pos = S +
     d_j + 1.  A chain-shaped tree is the linear walk exactly.
+    End of sequence and output caps as in the linear walk ([CV] paragraph 5):
+    an accepted child whose token is the EOS id ends the request (ST_EOS); once
+    cap children are accepted the walk stops (ST_CAPPED); either way no
+    correction or bonus follows.  A cap below 1 is bad input.
     force: optional {(node, rank): bool} overriding an accept decision.
     Returns accepted (path length, -1 on bad input), path (node ids), tokens
     (path tokens then the correction or bonus), status, and per-test records.
@@ -379,6 +383,8 @@ def verify_tree(target_rows, draft_rows, parent, tokens, n, T, top_p, draft_kind
     recs = []
     bad = dict(accepted=-1, path=[], tokens=[], status=ST_BAD_INPUT, tests=recs)
     if not (T >= 0.0) or not (0.0 < top_p <= 1.0) or n < 0:
+        return bad
+    if cap is not None and cap < 1:
         return bad
     for i in range(1, n + 1):
         if not (0 <= int(parent[i - 1]) < i) or not (0 <= int(tokens[i - 1]) < V):
@@ -432,6 +438,11 @@ def verify_tree(target_rows, draft_rows, parent, tokens, n, T, top_p, draft_kind
         if nxt is not None:
             path.append(nxt)
             cur, depth = nxt, depth + 1
+            stop = ST_EOS if (eos >= 0 and int(tokens[nxt - 1]) == eos) else \
+                ST_CAPPED if (cap is not None and depth == cap) else 0
+            if stop:
+                return dict(accepted=depth, path=path, tokens=[int(tokens[j - 1]) for j in path],
+                            status=status | stop, tests=recs)
             continue
         wr = p if pr is None else pr                  # correction
         E = philox.race_exponentials(seed, request_id, pos, V)
@@ -445,7 +456,7 @@ def verify_tree(target_rows, draft_rows, parent, tokens, n, T, top_p, draft_kind
 def verify_tree_batch(inp: dict, force=None):
     """verify_tree over every request of a tree workload dict: target
     [B][N+1][V], draft [B][N+1][V], parent [B][N], tokens [B][N], n [B],
-    temperature, top_p, optional top_k, seed, request_id, seq_len.  Returns
+    temperature, top_p, optional top_k, eos, max_new, seed, request_id, seq_len.  Returns
     accepted [B], path [B][N] and out_tokens [B][N+1] (-1 padded), num_emitted,
     status and the per-request records."""
     B, N = inp["parent"].shape
@@ -466,7 +477,9 @@ def verify_tree_batch(inp: dict, force=None):
                             inp["temperature"][b], inp["top_p"][b], inp["draft_kind"],
                             inp["seed"], int(inp["request_id"][b]), int(inp["seq_len"][b]),
                             top_k=int(inp["top_k"][b]) if inp.get("top_k") is not None else 0,
-                            force=(force or {}).get(b))
+                            force=(force or {}).get(b),
+                            eos=int(inp["eos"][b]) if inp.get("eos") is not None else -1,
+                            cap=int(inp["max_new"][b]) if inp.get("max_new") is not None else None)
         acc[b] = r["accepted"]
         st[b] = r["status"]
         path[b, :len(r["path"])] = r["path"]

@@ -132,7 +132,9 @@ def _oracle_tree(inp, b, force=None):
                          inp["top_p"][b], inp["draft_kind"], inp["seed"],
                          int(inp["request_id"][b]), int(inp["seq_len"][b]),
                          top_k=int(inp["top_k"][b]) if inp.get("top_k") is not None else 0,
-                         force=force)
+                         force=force,
+                         eos=int(inp["eos"][b]) if inp.get("eos") is not None else -1,
+                         cap=int(inp["max_new"][b]) if inp.get("max_new") is not None else None)
 
 
 def compare_tree(inp, out, ref=None):

@@ -590,3 +590,34 @@ def test_tree_branch_switch_and_repeated_siblings():
         r = S.verify_tree(tr, dr, np.array([0, 0]), np.array([y, y]), 2, 1.0, 1.0, "logits",
                           seed, 1, 0)
         assert r["path"] != [2]                      # the twin is never accepted
+
+
+def test_tree_eos_and_cap():
+    """EOS and output caps in a tree ([CV] paragraph 5): with q = p on every
+    row, the first child of each node is accepted, so the walk follows the
+    first children; an EOS id on that path or a cap ends it there, with no
+    correction or bonus."""
+    rng = np.random.default_rng(48)
+    V = 12
+    parent = np.array([0, 0, 1, 1, 3, 3, 5])           # first children: 1, 3, 5, 7
+    tokens = np.array([4, 2, 7, 1, 9, 0, 6])
+    rows = rng.standard_normal((8, V))
+
+    def run(**kw):
+        return S.verify_tree(rows, rows, parent, tokens, 7, 1.0, 1.0, "logits", 3, 0, 20, **kw)
+
+    full = run()
+    assert full["path"] == [1, 3, 5, 7] and full["status"] == 0 and len(full["tokens"]) == 5
+    r = run(eos=9)                                      # node 5's token
+    assert r["path"] == [1, 3, 5] and r["tokens"] == [4, 7, 9] and r["status"] == S.ST_EOS
+    r = run(cap=2)
+    assert r["path"] == [1, 3] and r["tokens"] == [4, 7] and r["status"] == S.ST_CAPPED
+    r = run(cap=4)                                      # the cap equals the path: no bonus
+    assert r["accepted"] == 4 and len(r["tokens"]) == 4 and r["status"] == S.ST_CAPPED
+    r = run(cap=5)
+    assert r["tokens"] == full["tokens"] and r["status"] == 0
+    r = run(eos=7, cap=2)                               # EOS at the cap's last token
+    assert r["path"] == [1, 3] and r["status"] == S.ST_EOS
+    assert run(cap=0)["accepted"] == -1
+    r = run(eos=2)                                      # a sibling off the path: no effect
+    assert r["tokens"] == full["tokens"] and r["status"] == 0
