@@ -310,12 +310,17 @@ sv_status spec_verify_static(const sv_verify_args* args, sv_stream_t stream);
  * parent, tokens [B][N] int32; n_nodes [B] (NULL = N); temperature [B];
  * top_p [B] (NULL = 1); top_k [B] (NULL = none); request_id [B] (NULL = b);
  * seq_len [B] S_b (NULL = 0); seed.
+ * eos_id [B] (NULL = none) and max_new [B] (NULL = no cap; below 1: bad input):
+ * an accepted child whose token is the request's EOS id ends the walk
+ * (SV_ST_EOS), and so does the max_new_b-th accepted child (SV_ST_CAPPED);
+ * then no correction or bonus follows ([CV] paragraph 5).
  * Outputs: accepted [B] = length a_b of the accepted path (-1 on bad input:
  *   a bad T / top_p / n_b, a parent not below its node, a token outside
  *   [0, V), or a NaN / +inf / empty row on the walk); path [B][N] = the
  *   accepted node ids in depth order, then -1; out_tokens [B][N+1] = their
- *   tokens, then the correction or bonus token, then -1; num_emitted [B] =
- *   a_b + 1 (0 on bad input); status [B] (SV_ST_* bits).
+ *   tokens, then the correction or bonus token (none after EOS or the cap),
+ *   then -1; num_emitted [B] = a_b + 1 (a_b after EOS or the cap; 0 on bad
+ *   input); status [B] (SV_ST_* bits).
  * Each cluster of CTAs walks one request at a time, taking requests from a
  * counter the handle owns: only one spec_verify_tree call per handle may be in
  * flight on the GPU at a time (calls in one stream are ordered).  No
@@ -347,6 +352,8 @@ typedef struct {
   int32_t* out_tokens;
   int32_t* num_emitted;
   uint32_t* status;
+  const int32_t* eos_id;  /* [B] or NULL: as in sv_verify_args, for the path's tokens */
+  const int32_t* max_new; /* [B] or NULL: at most max_new_b accepted nodes, then stop */
 } sv_tree_args;
 
 size_t sv_tree_args_size(void);

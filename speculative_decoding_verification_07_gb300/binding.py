@@ -85,7 +85,8 @@ class SvTreeArgs(ctypes.Structure):
                 ("temperature", c_void_p), ("top_p", c_void_p), ("top_k", c_void_p),
                 ("request_id", c_void_p), ("seq_len", c_void_p), ("seed", c_uint64),
                 ("accepted", c_void_p), ("path", c_void_p), ("out_tokens", c_void_p),
-                ("num_emitted", c_void_p), ("status", c_void_p)]
+                ("num_emitted", c_void_p), ("status", c_void_p),
+                ("eos_id", c_void_p), ("max_new", c_void_p)]
 
 
 class BflState(ctypes.Structure):
@@ -311,7 +312,8 @@ def kv_commit_copy(handle, accepted, seq_len, block_table, block_size, num_block
 
 def make_tree_args(*, target, draft, parent, tokens, temperature, accepted, path, out_tokens,
                    num_emitted, status, V=None, n_nodes=None, top_p=None, top_k=None, seed=0,
-                   request_id=None, seq_len=None, draft_kind="logits") -> SvTreeArgs:
+                   request_id=None, seq_len=None, draft_kind="logits", eos=None,
+                   max_new=None) -> SvTreeArgs:
     """target, draft: [B, N+1, ld] rows per tree node; parent, tokens: [B, N] int32."""
     B, rows, _ = target.shape
     a = SvTreeArgs()
@@ -324,6 +326,7 @@ def make_tree_args(*, target, draft, parent, tokens, temperature, accepted, path
     a.request_id, a.seq_len, a.seed = _ptr(request_id), _ptr(seq_len), int(seed) & (2 ** 64 - 1)
     a.accepted, a.path, a.out_tokens = _ptr(accepted), _ptr(path), _ptr(out_tokens)
     a.num_emitted, a.status = _ptr(num_emitted), _ptr(status)
+    a.eos_id, a.max_new = _ptr(eos), _ptr(max_new)
     return a
 
 

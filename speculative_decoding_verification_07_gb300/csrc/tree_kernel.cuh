@@ -46,6 +46,8 @@ struct TreeParams {
   int32_t* out_tokens;  // [B][N+1]
   int32_t* num_emitted;
   uint32_t* status;
+  const int32_t* eos;      // [B] or null
+  const int32_t* max_new;  // [B] or null
   int* err;
   uint32_t* ctr;  // [2] request ticket and done counters, zero between calls
   int slice, d_off;
@@ -312,13 +314,16 @@ __global__ void __launch_bounds__(kThreads, 2) tree_kernel(const TreeParams P) {
     const int top_k = P.top_k ? P.top_k[b] : 0;
     const uint32_t rid = P.request_id ? P.request_id[b] : (uint32_t)b;
     const int S = P.seq_len ? P.seq_len[b] : 0;
+    const int eos = P.eos ? P.eos[b] : -1;
+    const int cap = P.max_new ? P.max_new[b] : 0x7FFFFFFF;
     const int32_t* par = P.parent + (size_t)b * N;
     const int32_t* tok = P.tokens + (size_t)b * N;
     int32_t* o_path = P.path + (size_t)b * N;
     int32_t* o_tok = P.out_tokens + (size_t)b * (N + 1);
 
     // the tree and the parameters are checked before any row is read
-    bool bad = !(T >= 0.0f && T <= FLT_MAX) || !(top_p > 0.0f && top_p <= 1.0f) || n < 0 || n > N;
+    bool bad = !(T >= 0.0f && T <= FLT_MAX) || !(top_p > 0.0f && top_p <= 1.0f) || n < 0 || n > N ||
+               cap < 1;
     if (!bad)
       for (int j = tid + 1; j <= n; j += kThreads) {
         const int pj = par[j - 1], yj = tok[j - 1];
@@ -350,8 +355,9 @@ __global__ void __launch_bounds__(kThreads, 2) tree_kernel(const TreeParams P) {
     int cur = 0, depth = 0;
     uint32_t st_bits = 0u;
     int emitted = -1;  // the correction or bonus token, once drawn
+    uint32_t stop = 0u;  // SV_ST_EOS / SV_ST_CAPPED: the walk ended on an accepted child
     int first = bad ? 0 : issue(0);
-    while (!bad && emitted < 0) {
+    while (!bad && emitted < 0 && !stop) {
       cluster.sync();  // the previous node's shared memory is no longer read anywhere
       const bool has_d = first > 0;
       const char* trow = P.target + ((size_t)b * (N + 1) + cur) * P.t_ld * EBT;
@@ -420,6 +426,10 @@ __global__ void __launch_bounds__(kThreads, 2) tree_kernel(const TreeParams P) {
         if (lead) o_path[depth] = taken, o_tok[depth] = tok[taken - 1];
         cur = taken;
         ++depth;
+        // an accepted EOS id, or the cap's last token, ends the walk here
+        if (eos >= 0 && tok[taken - 1] == eos) stop = SV_ST_EOS;
+        else if (depth == cap) stop = SV_ST_CAPPED;
+        if (stop) break;
         first = issue(cur);
         continue;
       }
@@ -450,12 +460,13 @@ __global__ void __launch_bounds__(kThreads, 2) tree_kernel(const TreeParams P) {
         for (int q = 0; q < N; ++q) o_path[q] = -1;
         for (int q = 0; q <= N; ++q) o_tok[q] = -1;
       } else {
-        o_tok[depth] = emitted;
+        const int ne = stop ? depth : depth + 1;
+        if (!stop) o_tok[depth] = emitted;
         for (int q = depth; q < N; ++q) o_path[q] = -1;
-        for (int q = depth + 1; q <= N; ++q) o_tok[q] = -1;
+        for (int q = ne; q <= N; ++q) o_tok[q] = -1;
         P.accepted[b] = depth;
-        P.num_emitted[b] = depth + 1;
-        P.status[b] = st_bits;
+        P.num_emitted[b] = ne;
+        P.status[b] = st_bits | stop;
       }
     }
   }

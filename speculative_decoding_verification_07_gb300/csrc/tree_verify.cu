@@ -71,6 +71,7 @@ extern "C" sv_status spec_verify_tree(sv_handle* h, const sv_tree_args* a, sv_st
   P.seed_lo = (uint32_t)(a->seed & 0xFFFFFFFFu), P.seed_hi = (uint32_t)(a->seed >> 32);
   P.accepted = a->accepted, P.path = a->path, P.out_tokens = a->out_tokens;
   P.num_emitted = a->num_emitted, P.status = a->status;
+  P.eos = a->eos_id, P.max_new = a->max_new;
   P.err = h->d_err;
   // the handle's 256 device bytes hold the error word at offset 0 and, at
   // offset 128, the request ticket and done counters (zero between calls)

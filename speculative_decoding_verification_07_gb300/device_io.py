@@ -71,8 +71,9 @@ def tree_to_device(inp: dict, device="cuda", pin=False) -> dict:
         return x if device is None else x.to(device)
 
     extra = {}
-    if inp.get("top_k") is not None:
-        extra["top_k"] = t(inp["top_k"], np.int32)
+    for key in ("top_k", "eos", "max_new"):
+        if inp.get(key) is not None:
+            extra[key] = t(inp[key], np.int32)
     return dict(
         **extra,
         target=rows_to_device(inp["target"], inp["target_dtype"], device, pin=pin),

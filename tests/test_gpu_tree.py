@@ -212,3 +212,25 @@ def test_tree_repeated_calls_and_many_requests(ver):
     report("after a linear call", parity.compare_tree(b, out_b))
     for key in ("accepted", "path", "out_tokens", "status"):
         assert torch.equal(out_a[key], out_a2[key]), key
+
+
+def test_tree_eos_and_caps(ver):
+    """EOS ids (drawn from the trees' own tokens, so some sit on accepted
+    paths) and output caps from 1 to beyond the depth, one invalid cap."""
+    inp = W.tree_batch(B=48, V=32000, shape="binary:3", index=23)
+    rng = np.random.default_rng(24)
+    B, N = inp["parent"].shape
+    eos = np.full(B, -1, np.int32)
+    pick = rng.random(B) < 0.7
+    eos[pick] = inp["tokens"][pick, rng.integers(0, 2, pick.sum())]   # a root child's token
+    inp["eos"] = eos
+    inp["max_new"] = rng.integers(1, 5, B).astype(np.int32)
+    inp["max_new"][::4] = 1000
+    inp["max_new"][5] = 0
+    out = run_tree(ver, inp)
+    report("tree EOS / caps", parity.compare_tree(inp, out))
+    st = out["status"].cpu().numpy()
+    assert st[5] == binding.ST_BAD_INPUT
+    assert (st & binding.ST_CAPPED).any() and (st & binding.ST_EOS).any()
+    stopped = (st & (binding.ST_EOS | binding.ST_CAPPED)) != 0
+    assert (out["num_emitted"].cpu().numpy()[stopped] == out["accepted"].cpu().numpy()[stopped]).all()
