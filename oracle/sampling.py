@@ -346,7 +346,7 @@ def tree_children(parent, n):
 
 
 def verify_tree(target_rows, draft_rows, parent, tokens, n, T, top_p, draft_kind, seed,
-                request_id, seq_len, top_k=0, force=None, eos=-1, cap=None):
+                request_id, seq_len, top_k=0, force=None, eos=-1, cap=None, rep=None):
     """Verify one request's token tree ([CV] paragraph 3: a tree implementation
     keeps the accepted path; paragraph 5: test tree branch switches).
 
@@ -372,6 +372,10 @@ def verify_tree(target_rows, draft_rows, parent, tokens, n, T, top_p, draft_kind
     an accepted child whose token is the EOS id ends the request (ST_EOS); once
     cap children are accepted the walk stops (ST_CAPPED); either way no
     correction or bonus follows.  A cap below 1 is bad input.
+    rep: optional (theta, history ids, target dtype, draft dtype): the rows of
+    node j get the repetition penalty for the history plus the tokens of the
+    accepted path up to and including j (as row i of the linear walk does for
+    y_0 .. y_{i-1}).
     force: optional {(node, rank): bool} overriding an accept decision.
     Returns accepted (path length, -1 on bad input), path (node ids), tokens
     (path tokens then the correction or bonus), status, and per-test records.
@@ -386,6 +390,8 @@ def verify_tree(target_rows, draft_rows, parent, tokens, n, T, top_p, draft_kind
         return bad
     if cap is not None and cap < 1:
         return bad
+    if rep is not None and not (0.0 < float(np.float32(rep[0])) < np.inf):
+        return bad
     for i in range(1, n + 1):
         if not (0 <= int(parent[i - 1]) < i) or not (0 <= int(tokens[i - 1]) < V):
             return bad
@@ -395,6 +401,10 @@ def verify_tree(target_rows, draft_rows, parent, tokens, n, T, top_p, draft_kind
     while True:
         pos = int(seq_len) + depth + 1
         trow = target_rows[cur]
+        ids = None
+        if rep is not None:
+            ids = list(rep[1]) + [int(tokens[j - 1]) for j in path]
+            trow = repetition_penalty(trow, ids, rep[0], rep[2])
         if not row_is_valid(trow, "logits"):
             return bad
         p, pinfo = transform(trow, "logits", T, top_p, top_k)
@@ -408,6 +418,8 @@ def verify_tree(target_rows, draft_rows, parent, tokens, n, T, top_p, draft_kind
                         tokens=[int(tokens[j - 1]) for j in path] + [tok], status=status,
                         tests=recs)
         drow = draft_rows[cur]
+        if rep is not None and draft_kind == "logits":
+            drow = repetition_penalty(drow, ids, rep[0], rep[3])
         if not row_is_valid(drow, draft_kind):
             return bad
         q, qinfo = transform(drow, draft_kind, T, top_p, top_k)
@@ -453,10 +465,19 @@ def verify_tree(target_rows, draft_rows, parent, tokens, n, T, top_p, draft_kind
                     tokens=[int(tokens[j - 1]) for j in path] + [tok], status=status, tests=recs)
 
 
+def tree_rep(inp: dict, b: int):
+    """The repetition-penalty option of tree request b (None without one)."""
+    if inp.get("rep_penalty") is None:
+        return None
+    return (float(inp["rep_penalty"][b]), [int(t) for t in inp["rep_tokens"][b]],
+            inp["target_dtype"], inp["draft_dtype"])
+
+
 def verify_tree_batch(inp: dict, force=None):
     """verify_tree over every request of a tree workload dict: target
     [B][N+1][V], draft [B][N+1][V], parent [B][N], tokens [B][N], n [B],
-    temperature, top_p, optional top_k, eos, max_new, seed, request_id, seq_len.  Returns
+    temperature, top_p, optional top_k, eos, max_new, rep_penalty with
+    rep_tokens, seed, request_id, seq_len.  Returns
     accepted [B], path [B][N] and out_tokens [B][N+1] (-1 padded), num_emitted,
     status and the per-request records."""
     B, N = inp["parent"].shape
@@ -479,7 +500,8 @@ def verify_tree_batch(inp: dict, force=None):
                             top_k=int(inp["top_k"][b]) if inp.get("top_k") is not None else 0,
                             force=(force or {}).get(b),
                             eos=int(inp["eos"][b]) if inp.get("eos") is not None else -1,
-                            cap=int(inp["max_new"][b]) if inp.get("max_new") is not None else None)
+                            cap=int(inp["max_new"][b]) if inp.get("max_new") is not None else None,
+                            rep=tree_rep(inp, b))
         acc[b] = r["accepted"]
         st[b] = r["status"]
         path[b, :len(r["path"])] = r["path"]

@@ -134,7 +134,8 @@ def _oracle_tree(inp, b, force=None):
                          top_k=int(inp["top_k"][b]) if inp.get("top_k") is not None else 0,
                          force=force,
                          eos=int(inp["eos"][b]) if inp.get("eos") is not None else -1,
-                         cap=int(inp["max_new"][b]) if inp.get("max_new") is not None else None)
+                         cap=int(inp["max_new"][b]) if inp.get("max_new") is not None else None,
+                         rep=S.tree_rep(inp, b))
 
 
 def compare_tree(inp, out, ref=None):

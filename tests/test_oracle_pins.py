@@ -621,3 +621,21 @@ def test_tree_eos_and_cap():
     assert run(cap=0)["accepted"] == -1
     r = run(eos=2)                                      # a sibling off the path: no effect
     assert r["tokens"] == full["tokens"] and r["status"] == 0
+
+
+def test_tree_repetition_penalty_is_the_linear_one_on_a_chain():
+    """A chain-shaped tree with the repetition penalty gives the linear walk's
+    result with the same penalty (the path tokens play the earlier drafts'
+    role), on random cases with repeated proposals and history hits."""
+    rng = np.random.default_rng(49)
+    for t in range(40):
+        V, k = int(rng.integers(4, 10)), int(rng.integers(1, 5))
+        rows = rng.standard_normal((k + 1, V)) * 2
+        drows = rows + rng.standard_normal((k + 1, V)) * 0.5
+        y = rng.integers(0, min(V, 3), k)                  # repeats likely
+        hist = list(rng.integers(-1, V + 2, 6))
+        opt = (float(rng.choice([0.7, 1.3, 2.0])), hist, "f32", "f32")
+        lin = S.verify_request(rows, drows[:k], y, k, 1.0, 1.0, "logits", 9 + t, 1, 30, rep=opt)
+        tree = S.verify_tree(rows, drows, np.arange(k), y, k, 1.0, 1.0, "logits", 9 + t, 1, 30,
+                             rep=opt)
+        assert tree["tokens"] == lin["tokens"] and tree["status"] == lin["status"]
