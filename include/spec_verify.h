@@ -314,6 +314,9 @@ sv_status spec_verify_static(const sv_verify_args* args, sv_stream_t stream);
  * an accepted child whose token is the request's EOS id ends the walk
  * (SV_ST_EOS), and so does the max_new_b-th accepted child (SV_ST_CAPPED);
  * then no correction or bonus follows ([CV] paragraph 5).
+ * rep_penalty [B], rep_tokens [B][rep_ld], rep_ld: the repetition penalty of
+ * sv_verify_args; node j's rows (target, and draft logits) are penalised for
+ * the history ids plus the tokens of the accepted path up to and including j.
  * Outputs: accepted [B] = length a_b of the accepted path (-1 on bad input:
  *   a bad T / top_p / n_b, a parent not below its node, a token outside
  *   [0, V), or a NaN / +inf / empty row on the walk); path [B][N] = the
@@ -354,6 +357,9 @@ typedef struct {
   uint32_t* status;
   const int32_t* eos_id;  /* [B] or NULL: as in sv_verify_args, for the path's tokens */
   const int32_t* max_new; /* [B] or NULL: at most max_new_b accepted nodes, then stop */
+  const float* rep_penalty;  /* [B] or NULL: as in sv_verify_args */
+  const int32_t* rep_tokens; /* [B][rep_ld] history ids (-1 padded) */
+  int64_t rep_ld;
 } sv_tree_args;
 
 size_t sv_tree_args_size(void);

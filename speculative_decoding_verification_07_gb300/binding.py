@@ -86,7 +86,8 @@ class SvTreeArgs(ctypes.Structure):
                 ("request_id", c_void_p), ("seq_len", c_void_p), ("seed", c_uint64),
                 ("accepted", c_void_p), ("path", c_void_p), ("out_tokens", c_void_p),
                 ("num_emitted", c_void_p), ("status", c_void_p),
-                ("eos_id", c_void_p), ("max_new", c_void_p)]
+                ("eos_id", c_void_p), ("max_new", c_void_p),
+                ("rep_penalty", c_void_p), ("rep_tokens", c_void_p), ("rep_ld", c_int64)]
 
 
 class BflState(ctypes.Structure):
@@ -313,7 +314,7 @@ def kv_commit_copy(handle, accepted, seq_len, block_table, block_size, num_block
 def make_tree_args(*, target, draft, parent, tokens, temperature, accepted, path, out_tokens,
                    num_emitted, status, V=None, n_nodes=None, top_p=None, top_k=None, seed=0,
                    request_id=None, seq_len=None, draft_kind="logits", eos=None,
-                   max_new=None) -> SvTreeArgs:
+                   max_new=None, rep_penalty=None, rep_tokens=None) -> SvTreeArgs:
     """target, draft: [B, N+1, ld] rows per tree node; parent, tokens: [B, N] int32."""
     B, rows, _ = target.shape
     a = SvTreeArgs()
@@ -327,6 +328,13 @@ def make_tree_args(*, target, draft, parent, tokens, temperature, accepted, path
     a.accepted, a.path, a.out_tokens = _ptr(accepted), _ptr(path), _ptr(out_tokens)
     a.num_emitted, a.status = _ptr(num_emitted), _ptr(status)
     a.eos_id, a.max_new = _ptr(eos), _ptr(max_new)
+    a.rep_penalty = _ptr(rep_penalty)
+    if rep_tokens is not None:
+        if rep_tokens.dim() != 2 or rep_tokens.stride(1) != 1:
+            raise ValueError("rep_tokens must be [B][H] with unit stride along H")
+        a.rep_tokens, a.rep_ld = _ptr(rep_tokens), rep_tokens.stride(0)
+    else:
+        a.rep_tokens, a.rep_ld = None, 0
     return a
 
 

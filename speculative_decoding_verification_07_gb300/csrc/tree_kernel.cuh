@@ -48,6 +48,10 @@ struct TreeParams {
   uint32_t* status;
   const int32_t* eos;      // [B] or null
   const int32_t* max_new;  // [B] or null
+  const float* rep_penalty;   // [B] or null
+  const int32_t* rep_tokens;  // [B][rep_ld]
+  int rep_ld;
+  int rep_draft;  // 1: draft rows are logits and take the penalty too
   int* err;
   uint32_t* ctr;  // [2] request ticket and done counters, zero between calls
   int slice, d_off;
@@ -316,6 +320,9 @@ __global__ void __launch_bounds__(kThreads, 2) tree_kernel(const TreeParams P) {
     const int S = P.seq_len ? P.seq_len[b] : 0;
     const int eos = P.eos ? P.eos[b] : -1;
     const int cap = P.max_new ? P.max_new[b] : 0x7FFFFFFF;
+    const float theta = P.rep_penalty ? P.rep_penalty[b] : 1.0f;
+    const bool rep = theta != 1.0f;
+    const int32_t* hist = P.rep_tokens + (size_t)b * P.rep_ld;
     const int32_t* par = P.parent + (size_t)b * N;
     const int32_t* tok = P.tokens + (size_t)b * N;
     int32_t* o_path = P.path + (size_t)b * N;
@@ -323,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 2) tree_kernel(const TreeParams P) {
 
     // the tree and the parameters are checked before any row is read
     bool bad = !(T >= 0.0f && T <= FLT_MAX) || !(top_p > 0.0f && top_p <= 1.0f) || n < 0 || n > N ||
-               cap < 1;
+               cap < 1 || !theta_valid(theta);
     if (!bad)
       for (int j = tid + 1; j <= n; j += kThreads) {
         const int pj = par[j - 1], yj = tok[j - 1];
@@ -362,12 +369,39 @@ __global__ void __launch_bounds__(kThreads, 2) tree_kernel(const TreeParams P) {
       const bool has_d = first > 0;
       const char* trow = P.target + ((size_t)b * (N + 1) + cur) * P.t_ld * EBT;
       const char* drow = P.draft + ((size_t)b * (N + 1) + cur) * P.d_ld * EBD;
+      // repetition penalty: this node's set is the history plus the tokens of
+      // the accepted path up to and including cur; its ids inside this slice
+      // are marked in a bitmap while the rows load (each id once)
+      uint32_t* rmask = reinterpret_cast<uint32_t*>(&sm.wb);
+      const bool pen = rep && it.nblk > 0;
+      if (pen) {
+        for (int j = tid; j < kMaxBlk * kBlk / 32; j += kThreads) rmask[j] = 0u;
+        __syncthreads();
+        auto mark = [&](int x) {
+          if (x >= it.x0 && x < it.x1) atomicOr(&rmask[(x - it.x0) >> 5], 1u << ((x - it.x0) & 31));
+        };
+        for (int j = tid; j < P.rep_ld; j += kThreads) mark(hist[j]);
+        if (tid == 0)
+          for (int a = cur; a > 0; a = par[a - 1]) mark(tok[a - 1]);
+      }
       bool landed = true;
       if (it.nblk > 0) {
         landed &= mbar_wait(&sm.bar[0], phase_t, P.err);
         if (has_d) landed &= mbar_wait(&sm.bar[1], phase_d, P.err);
         phase_t ^= 1u;
         if (has_d) phase_d ^= 1u;
+      }
+      if (pen) {
+        __syncthreads();  // the bitmap is complete
+        const bool pen_d = has_d && P.rep_draft;
+        for (int w = tid; w < (it.x1 - it.x0 + 31) >> 5; w += kThreads) {
+          for (uint32_t m = rmask[w]; m; m &= m - 1u) {
+            const int e = (w << 5) + __ffs(m) - 1;
+            penalise_elem<EBT>(s_t, e, theta);
+            if (pen_d) penalise_elem<EBD>(s_d, e, theta);
+          }
+        }
+        __syncthreads();
       }
       RowP rt, rd;
       const bool greedy = T == 0.0f;
@@ -396,8 +430,18 @@ __global__ void __launch_bounds__(kThreads, 2) tree_kernel(const TreeParams P) {
       bool empty = false;
       while (j > 0) {
         const int y = tok[j - 1];
-        const float p_y = prob<EBT, false>(row_value<EBT>(trow, y), rt);
-        const float vq = row_value<EBD>(drow, y);
+        float vt = row_value<EBT>(trow, y), vq = row_value<EBD>(drow, y);
+        if (rep) {  // is y in this node's penalised set?
+          bool hit = false;
+          for (int h = tid; h < P.rep_ld; h += kThreads) hit |= hist[h] == y;
+          if (tid == 0)
+            for (int a = cur; a > 0; a = par[a - 1]) hit |= tok[a - 1] == y;
+          if (__syncthreads_or(hit)) {
+            vt = penalised<EBT>(vt, theta);
+            if (P.rep_draft) vq = penalised<EBD>(vq, theta);
+          }
+        }
+        const float p_y = prob<EBT, false>(vt, rt);
         const float q_y = prob<EBD, PROBS>(vq, rd);
         RowP rdc = rd;
         rdc.invZ = c * rd.invZ;

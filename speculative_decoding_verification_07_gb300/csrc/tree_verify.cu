@@ -40,6 +40,8 @@ extern "C" sv_status spec_verify_tree(sv_handle* h, const sv_tree_args* a, sv_st
       !a->num_emitted || !a->status)
     return SV_ERR_INVALID;
   if (a->N > 0 && (!a->parent || !a->tokens)) return SV_ERR_INVALID;
+  if (a->rep_penalty && (a->rep_ld < 0 || a->rep_ld > kMaxRepLd || (a->rep_ld > 0 && !a->rep_tokens)))
+    return SV_ERR_INVALID;
   if (a->target_ld < a->V || (a->target_ld * ebt) % 16 || !aligned16(a->target)) return SV_ERR_INVALID;
   if (a->draft_ld < a->V || (a->draft_ld * ebd) % 16 || !aligned16(a->draft)) return SV_ERR_INVALID;
 
@@ -72,6 +74,9 @@ extern "C" sv_status spec_verify_tree(sv_handle* h, const sv_tree_args* a, sv_st
   P.accepted = a->accepted, P.path = a->path, P.out_tokens = a->out_tokens;
   P.num_emitted = a->num_emitted, P.status = a->status;
   P.eos = a->eos_id, P.max_new = a->max_new;
+  P.rep_penalty = a->rep_penalty, P.rep_tokens = a->rep_tokens;
+  P.rep_ld = a->rep_penalty ? (int)a->rep_ld : 0;
+  P.rep_draft = a->draft_kind == SV_DRAFT_LOGITS;
   P.err = h->d_err;
   // the handle's 256 device bytes hold the error word at offset 0 and, at
   // offset 128, the request ticket and done counters (zero between calls)

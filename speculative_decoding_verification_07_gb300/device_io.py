@@ -74,6 +74,9 @@ def tree_to_device(inp: dict, device="cuda", pin=False) -> dict:
     for key in ("top_k", "eos", "max_new"):
         if inp.get(key) is not None:
             extra[key] = t(inp[key], np.int32)
+    if inp.get("rep_penalty") is not None:
+        extra["rep_penalty"] = t(inp["rep_penalty"], np.float32)
+        extra["rep_tokens"] = t(inp["rep_tokens"], np.int32)
     return dict(
         **extra,
         target=rows_to_device(inp["target"], inp["target_dtype"], device, pin=pin),

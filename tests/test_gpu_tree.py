@@ -234,3 +234,29 @@ def test_tree_eos_and_caps(ver):
     assert (st & binding.ST_CAPPED).any() and (st & binding.ST_EOS).any()
     stopped = (st & (binding.ST_EOS | binding.ST_CAPPED)) != 0
     assert (out["num_emitted"].cpu().numpy()[stopped] == out["accepted"].cpu().numpy()[stopped]).all()
+
+
+@pytest.mark.parametrize("kw", [{"V": 32000}, {"V": 4093, "dtype": "f32", "T": 1.0, "top_p": 1.0},
+                                {"V": 32000, "draft_kind": "probs"}])
+def test_tree_repetition_penalty(ver, kw):
+    """Repetition penalty in trees: node j's rows are penalised for the history
+    plus the accepted path's tokens up to j; the history holds some of the
+    trees' own tokens; one request has an invalid theta."""
+    inp = W.tree_batch(B=32, shape="binary:3", index=25, **kw)
+    rng = np.random.default_rng(26)
+    B, N = inp["parent"].shape
+    hist = rng.integers(0, inp["V"], (B, 60)).astype(np.int32)
+    for b in range(B):
+        hist[b, :4] = inp["tokens"][b, rng.integers(0, N, 4)]
+    hist[:, -3:] = -1
+    inp["rep_tokens"] = hist
+    inp["rep_penalty"] = rng.choice(np.array([1.0, 1.2, 2.0, 0.6], np.float32), B)
+    inp["rep_penalty"][7] = np.nan
+    out = run_tree(ver, inp)
+    report(f"tree repetition penalty {kw}", parity.compare_tree(inp, out))
+    assert out["status"].cpu().numpy()[7] == binding.ST_BAD_INPUT
+    plain = dict(inp)
+    plain.pop("rep_penalty"), plain.pop("rep_tokens")
+    ref = S.verify_tree_batch(plain)
+    ok = np.arange(B) != 7
+    assert (ref["out_tokens"][ok] != out["out_tokens"].cpu().numpy()[ok]).any()
