@@ -279,7 +279,9 @@ __device__ __forceinline__ float row_value(const char* row, int y) {
   return EB == 2 ? __uint_as_float((uint32_t)((const uint16_t*)row)[y] << 16) : ((const float*)row)[y];
 }
 
-template <int EBT, int EBD, bool PROBS>
+// OPTS: the request options (EOS ids, output caps, repetition penalty) are
+// compiled in; the plain variants leave their code out of the walk.
+template <int EBT, int EBD, bool PROBS, bool OPTS>
 __global__ void __launch_bounds__(kThreads, 2) tree_kernel(const TreeParams P) {
   cg::cluster_group cluster = cg::this_cluster();
   __shared__ Smem sm;
@@ -318,10 +320,10 @@ __global__ void __launch_bounds__(kThreads, 2) tree_kernel(const TreeParams P) {
     const int top_k = P.top_k ? P.top_k[b] : 0;
     const uint32_t rid = P.request_id ? P.request_id[b] : (uint32_t)b;
     const int S = P.seq_len ? P.seq_len[b] : 0;
-    const int eos = P.eos ? P.eos[b] : -1;
-    const int cap = P.max_new ? P.max_new[b] : 0x7FFFFFFF;
-    const float theta = P.rep_penalty ? P.rep_penalty[b] : 1.0f;
-    const bool rep = theta != 1.0f;
+    const int eos = OPTS && P.eos ? P.eos[b] : -1;
+    const int cap = OPTS && P.max_new ? P.max_new[b] : 0x7FFFFFFF;
+    const float theta = OPTS && P.rep_penalty ? P.rep_penalty[b] : 1.0f;
+    const bool rep = OPTS && theta != 1.0f;
     const int32_t* hist = P.rep_tokens + (size_t)b * P.rep_ld;
     const int32_t* par = P.parent + (size_t)b * N;
     const int32_t* tok = P.tokens + (size_t)b * N;
@@ -471,9 +473,11 @@ __global__ void __launch_bounds__(kThreads, 2) tree_kernel(const TreeParams P) {
         cur = taken;
         ++depth;
         // an accepted EOS id, or the cap's last token, ends the walk here
-        if (eos >= 0 && tok[taken - 1] == eos) stop = SV_ST_EOS;
-        else if (depth == cap) stop = SV_ST_CAPPED;
-        if (stop) break;
+        if constexpr (OPTS) {
+          if (eos >= 0 && tok[taken - 1] == eos) stop = SV_ST_EOS;
+          else if (depth == cap) stop = SV_ST_CAPPED;
+          if (stop) break;
+        }
         first = issue(cur);
         continue;
       }
@@ -534,5 +538,11 @@ TreeKernelFn tree_kernel_bf16_f32_logits();
 TreeKernelFn tree_kernel_f32_f32_logits();
 TreeKernelFn tree_kernel_f32_f32_probs();
 TreeKernelFn tree_kernel_f32_bf16_logits();
+TreeKernelFn tree_kernel_bf16_bf16_logits_opts();
+TreeKernelFn tree_kernel_bf16_f32_probs_opts();
+TreeKernelFn tree_kernel_bf16_f32_logits_opts();
+TreeKernelFn tree_kernel_f32_f32_logits_opts();
+TreeKernelFn tree_kernel_f32_f32_probs_opts();
+TreeKernelFn tree_kernel_f32_bf16_logits_opts();
 
 }  // namespace sv

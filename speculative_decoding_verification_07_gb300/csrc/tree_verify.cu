@@ -10,15 +10,18 @@ using namespace sv;
 namespace {
 
 struct TreeVariant {
-  TreeKernelFn fn;
+  TreeKernelFn fn, fn_opts;  // without / with the request options compiled in
   int eb_t, eb_d;
   bool probs;
 };
 
 const TreeVariant kTreeVariants[] = {
-    {tree_kernel_bf16_bf16_logits(), 2, 2, false}, {tree_kernel_bf16_f32_probs(), 2, 4, true},
-    {tree_kernel_bf16_f32_logits(), 2, 4, false},  {tree_kernel_f32_f32_logits(), 4, 4, false},
-    {tree_kernel_f32_f32_probs(), 4, 4, true},     {tree_kernel_f32_bf16_logits(), 4, 2, false},
+    {tree_kernel_bf16_bf16_logits(), tree_kernel_bf16_bf16_logits_opts(), 2, 2, false},
+    {tree_kernel_bf16_f32_probs(), tree_kernel_bf16_f32_probs_opts(), 2, 4, true},
+    {tree_kernel_bf16_f32_logits(), tree_kernel_bf16_f32_logits_opts(), 2, 4, false},
+    {tree_kernel_f32_f32_logits(), tree_kernel_f32_f32_logits_opts(), 4, 4, false},
+    {tree_kernel_f32_f32_probs(), tree_kernel_f32_f32_probs_opts(), 4, 4, true},
+    {tree_kernel_f32_bf16_logits(), tree_kernel_f32_bf16_logits_opts(), 4, 2, false},
 };
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
@@ -83,7 +86,8 @@ extern "C" sv_status spec_verify_tree(sv_handle* h, const sv_tree_args* a, sv_st
   P.ctr = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(h->d_err) + 128);
   P.slice = slice, P.d_off = d_off;
 
-  const TreeKernelFn fn = var->fn;
+  const bool opts = a->eos_id || a->max_new || a->rep_penalty;
+  const TreeKernelFn fn = opts ? var->fn_opts : var->fn;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
