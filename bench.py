@@ -213,6 +213,42 @@ def cpu_baseline(inp, seconds=12.0):
                       f"batch ({rows} rows, {el:.1f} s, numpy fp64, one thread)"}
 
 
+def _oracle_worker(job):
+    """One process of the all-cores oracle baseline: its own copy of the
+    workload, then request walks (every nproc-th request) for about `seconds`."""
+    rank, nproc, seconds = job
+    from oracle import sampling as S
+    inp = build_sets(1)[0]
+    B = inp["k"].shape[0]
+    rows = n = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds or n < 1:
+        b = (rank + n * nproc) % B
+        kb = int(inp["k"][b])
+        S.verify_request(S.decode(inp["target"][b, :kb + 1], "bf16"),
+                         S.decode(inp["draft"][b, :kb], "bf16"), inp["tokens"][b, :kb], kb,
+                         inp["temperature"][b], inp["top_p"][b], "logits", inp["seed"],
+                         int(inp["request_id"][b]), int(inp["seq_len"][b]))
+        rows += kb + 1
+        n += 1
+    return rows, n, time.perf_counter() - t0
+
+
+def cpu_baseline_all_cores(seconds=12.0):
+    """The oracle on every host core: one spawned process per core (spawned,
+    since the parent has used the GPU), each timing its own walks."""
+    import multiprocessing as mp
+    nproc = os.cpu_count() or 1
+    with mp.get_context("spawn").Pool(nproc) as pool:
+        res = pool.map(_oracle_worker, [(r, nproc, seconds) for r in range(nproc)])
+    rows = sum(r for r, _, _ in res)
+    walks = sum(w for _, w, _ in res)
+    el = max(t for _, _, t in res)
+    return {"value": rows / el, "unit": "rows/s", "cores": nproc, "kind": "oracle",
+            "sample": f"{nproc} processes, {walks} request walks of one verify_b64_k4 batch "
+                      f"({rows} rows, {el:.1f} s each at most, numpy fp64)"}
+
+
 # --------------------------------------------------------------------------- #
 # our arm
 # --------------------------------------------------------------------------- #
@@ -396,6 +432,7 @@ def run_ours(args):
             "kv_commit_copy": copy_line, "tree_verify": tree_line}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(sets[0])
+        line["cpu_baseline_all_cores"] = cpu_baseline_all_cores()
     if rank == 0:
         print(json.dumps(line), flush=True)
     ver.close()
