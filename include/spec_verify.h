@@ -318,7 +318,7 @@ sv_status spec_verify_static(const sv_verify_args* args, sv_stream_t stream);
  * sv_verify_args; node j's rows (target, and draft logits) are penalised for
  * the history ids plus the tokens of the accepted path up to and including j.
  * Outputs: accepted [B] = length a_b of the accepted path (-1 on bad input:
- *   a bad T / top_p / n_b, a parent not below its node, a token outside
+ *   a bad T / top_p / n_b / max_new / rep_penalty, a parent not below its node, a token outside
  *   [0, V), or a NaN / +inf / empty row on the walk); path [B][N] = the
  *   accepted node ids in depth order, then -1; out_tokens [B][N+1] = their
  *   tokens, then the correction or bonus token (none after EOS or the cap),
