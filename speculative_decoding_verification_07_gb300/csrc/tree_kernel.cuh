@@ -70,8 +70,11 @@ __device__ __forceinline__ int tree_next_child(const int32_t* par, int cur, int 
 }
 
 // Cluster-wide sum of one value per thread, reduced in a fixed order (lanes,
-// warps, ranks), so every CTA gets the same bits.
-__device__ __forceinline__ float tree_cluster_sum(cg::cluster_group& cluster, Smem& sm, float v) {
+// warps, ranks), so every CTA gets the same bits.  Consecutive calls alternate
+// the slot: a slot is rewritten only after a later call's barrier, which every
+// peer passes after its reads of the slot.
+__device__ __forceinline__ float tree_cluster_sum(cg::cluster_group& cluster, Smem& sm, float v,
+                                                  int slot) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -80,13 +83,12 @@ __device__ __forceinline__ float tree_cluster_sum(cg::cluster_group& cluster, Sm
   if (threadIdx.x == 0) {
     float a = 0.0f;
     for (int w = 0; w < kWarps; ++w) a += sm.scratch_f[w][0];
-    sm.kz[0] = a;
+    sm.kz[slot] = a;
   }
   cluster.sync();
   float s = 0.0f;
   const int C = (int)cluster.num_blocks();
-  for (int r = 0; r < C; ++r) s += cluster.map_shared_rank(&sm, r)->kz[0];
-  cluster.sync();  // peers are done reading kz before it can be rewritten
+  for (int r = 0; r < C; ++r) s += cluster.map_shared_rank(&sm, r)->kz[slot];
   return s;
 }
 
@@ -460,7 +462,8 @@ __global__ void __launch_bounds__(kThreads, 2) tree_kernel(const TreeParams P) {
         const int jn = tree_next_child(par, cur, j + 1, n);
         if (!jn) break;  // the last child: the correction needs c, not the new W
         rdc.invZ = c * rd.invZ;
-        W = tree_cluster_sum(cluster, sm, tree_residual_part<EBT, EBD, PROBS>(s_t, s_d, it, rt, rdc));
+        W = tree_cluster_sum(cluster, sm, tree_residual_part<EBT, EBD, PROBS>(s_t, s_d, it, rt, rdc),
+                             r & 1);
         if (!(W > 0.0f)) {
           empty = true;
           break;
