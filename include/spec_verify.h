@@ -73,13 +73,17 @@ typedef enum { SV_DRAFT_LOGITS = 0, SV_DRAFT_PROBS = 1 } sv_draft_kind;
 /* sv_verify_args.flags */
 #define SV_FLAG_NO_SKIP 1u /* also process rows after a known rejection (debug) */
 /* Testing aid for the bounded waits: row 0 of request 0 never publishes its
- * decision, and the waits for earlier rows' decisions give up after 1024 polls
- * (about 0.25 ms) instead of about 2^20.  A later row of request 0 that needs
- * row 0's decision then reports SV_ST_TIMEOUT for the request and
- * SV_ERR_TIMEOUT in the error word; the context stays usable.  Meant for
- * inputs where row 0 of request 0 is accepted (its outputs are otherwise
- * written by row 0 itself and may be overwritten by the later row's report). */
+ * decision, and the waits that depend on it give up after 1024 polls (about
+ * 0.25 ms) instead of about 2^20.  Request 0 then never resolves: the call
+ * reports SV_ST_TIMEOUT for it (accepted = -1, no tokens) and SV_ERR_TIMEOUT
+ * in the error word, every other request is unaffected, and the context stays
+ * usable.  Meant for inputs where row 0 of request 0 is accepted (a rejection
+ * there resolves nothing either way, but then the request's outcome would not
+ * depend on the withheld row). */
 #define SV_FLAG_TEST_WITHHOLD 2u
+/* Run the call on the cluster-resident kernel even where the streaming kernel
+ * would serve it (both compute the same results; for comparisons and tests). */
+#define SV_FLAG_CLUSTER_PATH 4u
 
 /* sv_row_debug.state */
 #define SV_ROW_NONE 0

@@ -34,6 +34,7 @@ ST_Q_ZERO, ST_BAD_INPUT, ST_RESIDUAL_EMPTY, ST_TIMEOUT = 1, 2, 4, 8
 ST_EOS, ST_CAPPED = 16, 32
 FLAG_NO_SKIP = 1
 FLAG_TEST_WITHHOLD = 2  # testing aid: see SV_FLAG_TEST_WITHHOLD
+FLAG_CLUSTER_PATH = 4   # run on the cluster-resident kernel (see SV_FLAG_CLUSTER_PATH)
 ROW_NONE, ROW_ACCEPTED, ROW_REJECTED, ROW_SKIPPED, ROW_INVALID, ROW_BONUS, ROW_TERMINAL = range(7)
 
 EXPORTS = ("sv_verify_args_size", "sv_create", "sv_destroy", "sv_workspace_size",

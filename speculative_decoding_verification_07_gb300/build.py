@@ -25,7 +25,8 @@ FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE
 
 SOURCES = ["api.cu", "kv_cache.cu", "verify.cu", "verify_bf16.cu", "verify_f32.cu", "verify_mixed.cu",
            "verify_static.cu", "verify_topk_bf16.cu", "verify_topk_f32.cu", "verify_topk_mixed.cu",
-           "tree_verify.cu", "tree_bf16.cu", "tree_f32.cu", "tree_opts_bf16.cu", "tree_opts_f32.cu"]
+           "tree_verify.cu", "tree_bf16.cu", "tree_f32.cu", "tree_opts_bf16.cu", "tree_opts_f32.cu",
+           "stream.cu", "stream_more.cu"]
 
 
 def nvcc() -> str:

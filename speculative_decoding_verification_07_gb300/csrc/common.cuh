@@ -20,6 +20,11 @@ struct sv_handle {
   size_t occ_smem[kCache];
   int occ_val[kCache];
   int occ_n;
+  // layout of the last spec_verify on a workspace: (pointer, kernel, B, kmax,
+  // V, dtypes, histograms).  A call with another layout clears the scratch
+  // words first, so a workspace may be reused for any shape.
+  const void* ws_last;
+  int64_t ws_key[6];
 };
 
 namespace sv {
@@ -98,6 +103,17 @@ __device__ __forceinline__ float lg2(float x) {
   return y;
 }
 
+// Programmatic dependent launch (sm_90+).  A kernel launched with the
+// programmatic-stream-serialization attribute may start while the kernel
+// before it in the stream is still running: pdl_wait() blocks until that
+// kernel has completed and its writes are visible (for a kernel launched
+// without the attribute it returns at once), and pdl_trigger() lets the next
+// kernel in the stream start early and wait in its own pdl_wait().
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Order-preserving unsigned key of an fp32 value (-0 maps like +0).
 __device__ __forceinline__ uint32_t fkey(float v) {
   uint32_t u = __float_as_uint(v);
@@ -111,6 +127,25 @@ __device__ __forceinline__ float fkey_value(uint32_t k) {
 }
 
 }  // namespace sv
+
+// Host side: launch with the programmatic-stream-serialization attribute (the
+// kernel must call pdl_wait() before it reads anything an earlier kernel in
+// the stream may still write).
+template <typename... KArgs, typename... Args>
+static inline cudaError_t sv_launch_pdl(void (*fn)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                        cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, args...);
+}
 
 // Host-side helper: map a CUDA error to SV_ERR_CUDA.
 #define SV_CUDA_TRY(expr)                      \

@@ -78,6 +78,8 @@ __global__ void __launch_bounds__(kKvThreads) bfl_reserve_kernel(bfl_state st, i
                                                                  const int32_t* seq_len,
                                                                  const int32_t* k, int32_t* table,
                                                                  int max_blocks, int* err) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int scratch[32];
   __shared__ int s_err;
   const int BS = st.block_size, nb = st.num_blocks;
@@ -269,6 +271,8 @@ __global__ void __launch_bounds__(kKvThreads) kv_commit_kernel(bfl_state st, int
                                                                int32_t* seq_len, int32_t* table,
                                                                int max_blocks, int32_t* n_freed,
                                                                int* err) {
+  pdl_wait();
+  pdl_trigger();
   const int BS = st.block_size;
   // accepted outside [-1, k_b] or a held range beyond the table: refuse the call
   __shared__ int s_bad;
@@ -623,9 +627,12 @@ extern "C" sv_status bfl_reserve(sv_handle* h, const bfl_state* st, int32_t B,
   if (!h || bad_state(st) || B < 0 || max_blocks < 1) return SV_ERR_INVALID;
   if (B == 0) return SV_OK;
   if (!seq_len || !table) return SV_ERR_INVALID;
-  bfl_reserve_kernel<<<1, kv_threads(B), 0, (cudaStream_t)stream>>>(*st, B, seq_len, k, table,
-                                                                 max_blocks, h->d_err);
-  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+  if (sv_launch_pdl(bfl_reserve_kernel, dim3(1), dim3(kv_threads(B)), 0, (cudaStream_t)stream, *st, B,
+                    seq_len, k, table, (int)max_blocks, h->d_err) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return SV_ERR_CUDA;
+  }
+  return SV_OK;
 }
 
 extern "C" sv_status bfl_fork_prefix(sv_handle* h, const bfl_state* st, int32_t n_pairs,
@@ -660,9 +667,12 @@ extern "C" sv_status kv_commit_rollback(sv_handle* h, const bfl_state* st, int32
   if (!h || bad_state(st) || B < 0 || max_blocks < 1) return SV_ERR_INVALID;
   if (B == 0) return SV_OK;
   if (!accepted || !seq_len || !table) return SV_ERR_INVALID;
-  kv_commit_kernel<<<1, kv_threads(B), 0, (cudaStream_t)stream>>>(*st, B, k, accepted, seq_len, table,
-                                                               max_blocks, n_freed, h->d_err);
-  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+  if (sv_launch_pdl(kv_commit_kernel, dim3(1), dim3(kv_threads(B)), 0, (cudaStream_t)stream, *st, B, k,
+                    accepted, seq_len, table, (int)max_blocks, n_freed, h->d_err) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return SV_ERR_CUDA;
+  }
+  return SV_OK;
 }
 
 static bool bad_payload(const kv_payload* kv) {

@@ -1,0 +1,523 @@
+#pragma once
+// Streaming verification kernel (device code).  Same method and results as
+// verify_kernel.cuh ("Speculative decoding: accelerate LLM generation without
+// changing its answers", sections 2-4: the transformed p_i and q_i, accept
+// y_i iff u_i q_i(y_i) < p_i(y_i) left to right, the correction from
+// normalize(max(0, p - q)) at the first rejection or the bonus token from
+// p_{k_b}, both drawn by an exponential race), laid out so that HBM streams
+// at full rate.
+//
+// GB300 design
+//  * One persistent CTA per SM with three roles: a producer warp, eight
+//    consumer warps and a finisher warp.  The producer takes work tickets
+//    from a counter in the workspace and pulls each item into a ring of
+//    shared-memory stages with 1-D TMA bulk copies (cp.async.bulk, one
+//    mbarrier per stage).  The consumers work the stages in order, hand each
+//    back through an "empty" mbarrier and pass their results to the finisher
+//    through a small shared-memory ring; the finisher does everything that
+//    waits on global memory (partials, arrival counters, the row-pair
+//    combine, the request resolution), so the consumers only compute.  No CTA
+//    ever waits on another CTA's shared memory: a row's bytes stay on chip
+//    only while its own statistics are taken.
+//  * A row item is one vocabulary chunk of one row pair (target row i and, for
+//    i < k_b, draft row i of request b).  Tickets run in (position, request,
+//    chunk) order, so a row pair's chunks are worked at the same time by
+//    different SMs and the pair is decided within a few microseconds of its
+//    first load.  Rows of a request behind a known rejection are never loaded:
+//    the producer skips them (and jumps the ticket counter past them).
+//  * Per chunk: the maximum (packed bf16x2 max), the weight sum relative to
+//    it, and for bf16 logit rows with top_p < 1 an exact count histogram of
+//    the bf16 values in a window below the row's maximum.  The window floor
+//    uses the largest maximum other chunks of the same row have published so
+//    far and the deepest nucleus seen in this call, so only the few elements
+//    that can border the nucleus are counted; a row whose boundary lies below
+//    every chunk's window is decided exactly by a radix descent over the row
+//    instead (also used for fp32 rows).
+//  * Window histograms are indexed by (-key) mod 256, so every chunk's bins
+//    line up whatever its reference; a chunk contributes only to keys at or
+//    below its own reference, which rules out aliasing.
+//  * The finisher that completes a row pair's last chunk merges the partials,
+//    finds the top-p boundaries, runs the accept test and publishes the
+//    decision in the request's state words (accepted-row mask, first
+//    non-accepted row).  Whoever completes "rows 0..f-1 accepted, row f not"
+//    resolves the request: a rejection or bonus row queues one race item per
+//    chunk of row f, which re-reads that row (from L2: it was just streamed)
+//    and races over the kept tokens only; the last race item writes the
+//    request's outputs.
+//  * Per-call state lives in two halves of the workspace used on alternate
+//    calls: each call zeroes the half the next call will use.
+#include "verify_kernel.cuh"
+
+namespace sv {
+namespace stream {
+
+constexpr int kCW = 8;               // consumer warps (warps 0-7)
+constexpr int kCT = kCW * 32;        // consumer threads (== the helpers' kThreads)
+constexpr int kProducerWarp = kCW;   // warp 8
+constexpr int kFinisherWarp = kCW + 1;  // warps 9 .. 9 + kFW - 1
+constexpr int kFW = 2;               // finisher warps; hand-off slot f goes to finisher f % kFW
+constexpr int kAllThreads = kCT + 32 + 32 * kFW;
+constexpr int kNF = 4;               // finisher hand-off slots
+static_assert(kNF % kFW == 0, "finisher slots split evenly");
+constexpr int kBins = 256;
+constexpr int kMaxNs = 4;
+constexpr int kMaxChunks = 32;
+constexpr uint32_t kNA = 1024u;      // request word na = kNA - first non-accepted row (0: none)
+constexpr float kDepthMargin = 1.0f; // log2 units added to the deepest nucleus seen
+static_assert(kCT == sv::kThreads, "the shared row helpers assume 256 consumer threads");
+
+template <int EBT, int EBD>
+__host__ __device__ constexpr int chunk_elems() {
+  return (EBT == 2 && EBD == 2) ? 16384 : 8192;
+}
+template <int EBT, int EBD>
+__host__ __device__ constexpr int stage_bytes() {
+  return chunk_elems<EBT, EBD>() * (EBT + EBD);
+}
+template <int EBT, int EBD>
+__host__ __device__ constexpr int num_stages() {
+  return stage_bytes<EBT, EBD>() <= 49152 ? 4 : 3;
+}
+
+enum : int { kEnd = 0, kRowItem = 1, kRaceItem = 2, kBadItem = 3 };
+enum : int { kRaceResidual = 1, kRaceBonus = 2 };
+
+// ---------------------------------------------------------------------------
+// Workspace records
+// ---------------------------------------------------------------------------
+struct Hdr {            // fixed words at byte 64 of the workspace header
+  uint32_t parity;      // which state half this call uses
+  uint32_t ticket;      // next work ticket
+  uint32_t exit_cnt;    // CTAs finished
+  uint32_t pad[13];
+};
+
+struct CallSt {         // per call, zeroed by the previous call
+  uint32_t n_slots;     // race slots claimed
+  uint32_t n_resolved;  // requests resolved (any outcome)
+  uint32_t n_done;      // requests whose outputs are written
+  uint32_t depth_t;     // deepest target nucleus seen, log2 units (float bits)
+  uint32_t depth_d;
+  uint32_t pad[11];
+};
+
+struct ReqSt {
+  unsigned long long acc;   // bit i: row i accepted
+  unsigned long long qz;    // bit i: row i's test saw q(y) == 0
+  unsigned long long best;  // race winner: (key bits << 32) | (0xFFFFFFFF - token)
+  uint32_t na;              // kNA - first non-accepted row, or 0
+  uint32_t resolved;        // 0 -> 1 by the resolver (2: timed out)
+  uint32_t race_cnt;        // race items finished
+  uint32_t pad[7];
+};
+static_assert(sizeof(ReqSt) == 64, "");
+
+struct Slot {
+  uint32_t b, row, kind, ready;
+};
+
+struct PairSt {
+  uint32_t arrive;      // chunks finished
+  uint32_t tkey, dkey;  // largest chunk maxima published (order keys)
+  uint32_t state;       // SV_ROW_* once decided
+  uint32_t pad[4];
+};
+
+// One side (target or draft) of a decided row: everything the race and the
+// normalised-row writer need to evaluate prob(v).
+struct RowSide {
+  float m, mz, c, invT;
+  float Z, invZ, vstar;
+  uint32_t Dstar;       // kept iff vkey(m) - vkey(v) <= Dstar; kNoFilter = all
+};
+struct RowRec {
+  RowSide t, d;
+};
+static_assert(sizeof(RowRec) == 64, "");
+
+struct PartHdr {        // one side of a chunk partial
+  float m, S;
+  uint32_t ref, floor;  // window reference and floor keys (bf16 order keys)
+};
+// chunk partial: PartHdr target | PartHdr draft | (vt, vd, has_y, 0) | bins
+constexpr int kPartHead = 48;
+
+// ---------------------------------------------------------------------------
+// Kernel parameters
+// ---------------------------------------------------------------------------
+struct SParams {
+  int B, kmax, V, n_ch;
+  uint32_t flags;
+  const char* target;
+  int64_t t_ld;
+  const char* draft;
+  int64_t d_ld;
+  const int32_t* tokens;
+  const int32_t* k;
+  const float* temperature;
+  const float* top_p;
+  const uint32_t* request_id;
+  const int32_t* seq_len;
+  uint32_t seed_lo, seed_hi;
+  int32_t* accepted;
+  int32_t* out_tokens;
+  int32_t* num_emitted;
+  uint32_t* status;
+  sv_row_debug* debug;
+  const int32_t* eos;
+  const int32_t* max_new;
+  Hdr* hdr;
+  char* state[2];       // per-call state halves
+  size_t state_words;   // u32 words per half
+  RowRec* rows;         // [B][kmax+1]
+  char* parts;          // [B][kmax+1][n_ch] partials
+  int part_bytes;       // kPartHead, plus 2 * 512 with histograms
+  int hist;             // partials carry window histograms
+  int* err;
+  unsigned long long slot_wait_ns;  // bound of a wait for a race slot
+  uint32_t n_static;    // (kmax + 1) * B * n_ch
+};
+
+// state-half layout: CallSt | ReqSt[B] | Slot[B] | PairSt[B][kmax+1]
+__host__ __device__ inline size_t state_bytes_for(int B, int kmax) {
+  return sizeof(CallSt) + (size_t)B * sizeof(ReqSt) + (size_t)B * sizeof(Slot) +
+         (size_t)B * (size_t)(kmax + 1) * sizeof(PairSt);
+}
+__device__ __forceinline__ CallSt* call_st(char* s) { return reinterpret_cast<CallSt*>(s); }
+__device__ __forceinline__ ReqSt* req_st(char* s, int b) {
+  return reinterpret_cast<ReqSt*>(s + sizeof(CallSt)) + b;
+}
+__device__ __forceinline__ Slot* slot_st(char* s, int B, int q) {
+  return reinterpret_cast<Slot*>(s + sizeof(CallSt) + (size_t)B * sizeof(ReqSt)) + q;
+}
+__device__ __forceinline__ PairSt* pair_st(char* s, int B, size_t pair) {
+  return reinterpret_cast<PairSt*>(s + sizeof(CallSt) + (size_t)B * (sizeof(ReqSt) + sizeof(Slot))) +
+         pair;
+}
+
+// ---------------------------------------------------------------------------
+// Shared memory
+// ---------------------------------------------------------------------------
+struct SHdr {           // one stage's item, written by the producer
+  int kind, b, i, c;
+  int x0, n, has_d, kb;
+  float T, top_p;
+  int race, pos;
+  uint32_t rid;
+  int y;                // the row's proposal (draft rows)
+  int pad[2];
+  RowRec rr;            // race items: the decided row
+};
+
+// Consumer -> finisher hand-off of one item.
+struct alignas(16) Fin {
+  int kind, b, i, c;
+  int has_d, kb, race, pos;
+  float T, top_p;
+  uint32_t rid;
+  int y;
+  float Mt, St, Md, Sd;
+  uint32_t ref_t, flo_t, ref_d, flo_d;
+  float vt, vd;         // the values at y when y lies in this chunk
+  int has_y, win;       // win: bit 0 target window, bit 1 draft window
+  float rw, rE;         // race items: the chunk's winner
+  int ridx, pad;
+  RowRec rr;            // race items: the decided row
+  uint32_t hist[2][kBins];  // window counts by ring index (-key) & 255
+};
+
+struct alignas(16) SSmem {
+  unsigned long long full[kMaxNs], empty[kMaxNs];
+  unsigned long long fin_full[kNF], fin_empty[kNF];
+  SHdr hdr[kMaxNs];
+  Fin fin[kNF];
+  float fh[kFW][kBins]; // finisher scratch: row-bin masses / descent histogram
+  float red[kCW][4];
+  uint32_t hint[4];     // row items: max hints and nucleus depths, as thread 0 read them
+  RacePart rp[kCW];
+  union {
+    uint16_t idx[kCW][256];  // race candidates
+    uint8_t bin[kCW][512];   // window bins
+  } wb;
+};
+
+// ---------------------------------------------------------------------------
+// small helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"n"(kCT) : "memory"); }
+
+__device__ __forceinline__ void fence_sc() { asm volatile("fence.sc.gpu;" ::: "memory"); }
+
+__device__ __forceinline__ unsigned long long ld_relaxed64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void mbar_init_n(unsigned long long* bar, int n) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive1(unsigned long long* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_n(unsigned long long* bar, uint32_t n) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long gtimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded mbarrier wait (the bound is time, not a poll count): false, with
+// SV_ERR_TIMEOUT reported, if the phase has not completed after `ns`.
+constexpr unsigned long long kStageWaitNs = 4000000000ull;   // consumers, producer
+constexpr unsigned long long kFinWaitNs = 6000000000ull;     // finishers wait on the consumers
+__device__ __forceinline__ bool mbar_wait_ns(unsigned long long* bar, uint32_t parity, int* err,
+                                             unsigned long long ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = gtimer();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (gtimer() - t0 > ns) break;
+  }
+  report(err, SV_ERR_TIMEOUT);
+  return false;
+}
+
+// Release the stage: each consumer warp arrives once after its last read.
+__device__ __forceinline__ void release_stage(SSmem& sm, int s) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive1(&sm.empty[s]);
+}
+
+__device__ __forceinline__ uint32_t key16(float bf16_value) { return vkey<2>(bf16_value); }
+
+__device__ __forceinline__ unsigned long long race_key(float w, float E, int idx) {
+  const float key = w > 0.0f ? __fdiv_rn(w, E) : 0.0f;
+  return ((unsigned long long)__float_as_uint(key) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)idx);
+}
+
+__device__ __forceinline__ bool row_params_ok(float T, float top_p) {
+  return (T >= 0.0f) && (T <= FLT_MAX) && (top_p > 0.0f) && (top_p <= 1.0f);
+}
+
+template <int EB>
+__device__ __forceinline__ float row_value(const char* row, int y) {
+  return EB == 2 ? __uint_as_float((uint32_t)__ldcg((const unsigned short*)row + y) << 16)
+                 : __ldcg((const float*)row + y);
+}
+
+// Weight-domain maximum from the raw maximum (identical wherever it is used).
+template <bool PROBS>
+__device__ __forceinline__ float weight_max(float m, bool greedy, float invT) {
+  if (PROBS && !greedy) return m > 0.0f ? lg2(m) * invT : -INFINITY;
+  return m;
+}
+
+static __device__ void bad_outputs(const SParams& P, int b, uint32_t st) {
+  P.accepted[b] = -1;
+  P.num_emitted[b] = 0;
+  P.status[b] = st;
+  for (int j = 0; j <= P.kmax; ++j) P.out_tokens[(size_t)b * (P.kmax + 1) + j] = -1;
+}
+
+__device__ __forceinline__ RowP row_p(const RowSide& s, bool greedy) {
+  RowP r;
+  r.m = s.m, r.mz = s.mz, r.c = s.c, r.invT = s.invT, r.greedy = greedy;
+  r.S = s.Z, r.Z = s.Z, r.invZ = s.invZ, r.vstar = s.vstar, r.Dstar = s.Dstar;
+  r.kmax = 0u;
+  return r;
+}
+
+// A warp reads a row from global memory in steps of kUnrollG groups per lane
+// (lane l: groups x0, x0 + 256, ...), so several 16-byte loads are in flight;
+// groups at or beyond V read as neutral values (never loaded).
+constexpr int kUnrollG = 4;
+template <int EB, bool PROBS>
+__device__ __forceinline__ void load_groups_global(Grp<EB> (&g)[kUnrollG], const char* row, int x0,
+                                                   int V) {
+#pragma unroll
+  for (int u = 0; u < kUnrollG; ++u) {
+    const int x = x0 + u * 32 * kGroup;
+    if (x < V) {
+      lds_group<EB, PROBS>(g[u], row, 0, x, V);
+    } else {
+#pragma unroll
+      for (int j = 0; j < EB * 2; ++j) g[u].w[j] = neutral_word<EB, PROBS>();
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Exact top-p boundary of one row read from global memory by one warp: a
+// radix descent over the order key, 8 bits per level (2 levels for bf16, 4
+// for fp32), each level summing the weights of the elements under the
+// current key prefix per bin; the kept mass is then recomputed in a fixed
+// order.  fh is 256 floats of the warp's shared scratch.  Sets Dstar, Z,
+// invZ and vstar of r (r.kmax must hold vkey(m)).
+// ---------------------------------------------------------------------------
+template <int EB, bool PROBS>
+__device__ __noinline__ void exact_top_p_warp(const char* row, int V, RowP& r, float R, float* fh) {
+  const int lane = threadIdx.x & 31;
+  constexpr int KB = EB == 2 ? 16 : 32;
+  uint32_t prefix = 0u;
+  float above = 0.0f;
+  for (int shift = KB - 8; shift >= 0; shift -= 8) {
+    for (int j = lane; j < kBins; j += 32) fh[j] = 0.0f;
+    __syncwarp();
+    const int hi = shift + 8;  // bits above this level's byte must equal the prefix's
+#pragma unroll 1
+    for (int x0 = lane * kGroup; x0 < V; x0 += kUnrollG * 32 * kGroup) {
+      Grp<EB> g[kUnrollG];
+      load_groups_global<EB, PROBS>(g, row, x0, V);
+#pragma unroll
+      for (int u = 0; u < kUnrollG; ++u) {
+#pragma unroll
+        for (int e = 0; e < kGroup; ++e) {
+          const float v = gval<EB>(g[u], e);
+          const uint32_t key = vkey<EB>(v);
+          if (hi < KB && (key >> hi) != (prefix >> hi)) continue;
+          const float w = weight<PROBS>(v, r);
+          if (w > 0.0f) atomicAdd(&fh[(key >> shift) & 255u], w);
+        }
+      }
+    }
+    __syncwarp();
+    // bins in descending key order: lane l holds bins 255 - 8l - q, q = 0..7
+    float h[8], inc[8], t = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) h[q] = fh[255 - 8 * lane - q], t += h[q], inc[q] = t;
+    float off = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float v = __shfl_up_sync(0xffffffffu, off, o);
+      if (lane >= o) off += v;
+    }
+    off -= t;
+    int first = 8;
+#pragma unroll
+    for (int q = 7; q >= 0; --q)
+      if (above + off + inc[q] >= R) first = q;
+    const uint32_t hit = __ballot_sync(0xffffffffu, first < 8);
+    int src, q;
+    if (hit) {
+      src = __ffs(hit) - 1;
+      q = __shfl_sync(0xffffffffu, first, src);
+    } else {  // rounding left R unreachable: keep through the lowest non-empty bin
+      int last = -1;
+#pragma unroll
+      for (int qq = 0; qq < 8; ++qq)
+        if (h[qq] > 0.0f) last = qq;
+      const uint32_t any = __ballot_sync(0xffffffffu, last >= 0);
+      src = any ? 31 - __clz(any) : 0;
+      q = any ? __shfl_sync(0xffffffffu, last, src) : 0;
+    }
+    float mine = off;  // mass of the bins above the chosen one (valid on lane src)
+#pragma unroll
+    for (int qq = 0; qq < 8; ++qq)
+      if (qq < q) mine += h[qq];
+    above += __shfl_sync(0xffffffffu, mine, src);
+    prefix |= (255u - (uint32_t)(8 * src + q)) << shift;
+    __syncwarp();  // fh is rewritten by the next level
+  }
+  float z = 0.0f;  // kept mass, per lane in a fixed order, then a fixed butterfly
+#pragma unroll 1
+  for (int x0 = lane * kGroup; x0 < V; x0 += kUnrollG * 32 * kGroup) {
+    Grp<EB> g[kUnrollG];
+    load_groups_global<EB, PROBS>(g, row, x0, V);
+#pragma unroll
+    for (int u = 0; u < kUnrollG; ++u) {
+#pragma unroll
+      for (int e = 0; e < kGroup; ++e) {
+        const float v = gval<EB>(g[u], e);
+        if (vkey<EB>(v) >= prefix) z += weight<PROBS>(v, r);
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  r.Dstar = r.kmax - prefix;
+  r.Z = z;
+  r.invZ = 1.0f / z;
+  r.vstar = vkey_value<EB>(prefix);
+}
+
+// Window merge and scan of one bf16 row by one warp.  Lane c < n_ch holds
+// chunk c's header (ref, floor).  Row bin j is the key K - j (K = key of the
+// row maximum); only bins with key >= Fstar are complete.  Lane l loads ring
+// bins 8l .. 8l+7 of every chunk (ring index (-key) & 255) and counts a chunk
+// only for keys at or below its reference.  Returns the boundary bin j (or
+// -1 when the kept mass does not reach R inside the complete window) and the
+// kept mass through it in Z.
+__device__ __forceinline__ int window_boundary(const SParams& P, const char* parts, int side,
+                                               uint32_t my_ref, uint32_t K, uint32_t Fstar,
+                                               const RowP& r, float R, float* fh, float& Z) {
+  const int lane = threadIdx.x & 31;
+  const int jmax = K >= Fstar ? (int)min(255u, K - Fstar) : -1;
+  const uint32_t rK = (0u - K) & 255u;
+  uint32_t cnt[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) cnt[q] = 0u;
+  const char* base = parts + kPartHead + side * 512 + 16 * lane;
+#pragma unroll 4
+  for (int c = 0; c < P.n_ch; ++c) {
+    const uint32_t refc = __shfl_sync(0xffffffffu, my_ref, c);
+    const uint4 v = __ldcg(reinterpret_cast<const uint4*>(base + (size_t)c * P.part_bytes));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const uint32_t j = ((uint32_t)(8 * lane + q) - rK) & 255u;
+      const uint32_t key = K - j;
+      if (key <= refc) cnt[q] += (w[q >> 1] >> (16 * (q & 1))) & 0xFFFFu;
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const uint32_t j = ((uint32_t)(8 * lane + q) - rK) & 255u;
+    const uint32_t key = K - j;
+    float mass = 0.0f;
+    if ((int)j <= jmax && j <= K && cnt[q]) mass = (float)cnt[q] * weight<false>(vkey_value<2>(key), r);
+    fh[j] = mass;
+  }
+  __syncwarp();
+  float h[8], inc[8], t = 0.0f;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) h[q] = fh[8 * lane + q], t += h[q], inc[q] = t;
+  float off = t;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float v = __shfl_up_sync(0xffffffffu, off, o);
+    if (lane >= o) off += v;
+  }
+  off -= t;
+  int first = 8;
+#pragma unroll
+  for (int q = 7; q >= 0; --q)
+    if (8 * lane + q <= jmax && off + inc[q] >= R) first = q;
+  const uint32_t hit = __ballot_sync(0xffffffffu, first < 8);
+  __syncwarp();  // fh is reused by the caller
+  if (!hit) return -1;
+  const int src = __ffs(hit) - 1;
+  float z = 0.0f;
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    if (q == first) z = off + inc[q];
+  Z = __shfl_sync(0xffffffffu, z, src);
+  return 8 * src + __shfl_sync(0xffffffffu, first, src);
+}
+
+}  // namespace stream
+
+using StreamFn = void (*)(stream::SParams);
+StreamFn stream_bf16_bf16_logits();
+StreamFn stream_bf16_f32_probs();
+StreamFn stream_bf16_f32_logits();
+StreamFn stream_f32_f32_logits();
+StreamFn stream_f32_f32_probs();
+StreamFn stream_f32_bf16_logits();
+
+}  // namespace sv

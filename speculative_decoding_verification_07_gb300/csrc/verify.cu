@@ -38,6 +38,14 @@ size_t workspace_bytes_for(int B, int kmax) {
   return kHdrBytes + ((rows * 4 + 255) / 256) * 256;
 }
 
+// The streaming kernel (stream.cu) serves most calls; the cluster kernel
+// above serves top-k, the repetition penalty and top-p on fp32 rows.
+bool stream_eligible(const sv_verify_args* a);
+size_t stream_workspace_bytes(const sv_verify_args* a);
+size_t stream_state_bytes(const sv_verify_args* a);  // header + both state halves
+sv_status stream_launch(sv_handle* h, const sv_verify_args* a, void* ws, size_t ws_bytes,
+                        cudaStream_t stream);
+
 }  // namespace sv
 
 using namespace sv;
@@ -46,7 +54,9 @@ extern "C" size_t sv_verify_args_size(void) { return sizeof(sv_verify_args); }
 
 extern "C" sv_status sv_workspace_size(const sv_verify_args* a, size_t* bytes) {
   if (!a || !bytes || a->B < 0 || a->kmax < 0) return SV_ERR_INVALID;
-  *bytes = workspace_bytes_for(a->B, a->kmax);
+  const size_t cl = workspace_bytes_for(a->B, a->kmax);
+  const size_t sb = stream_workspace_bytes(a);
+  *bytes = sb > cl ? sb : cl;
   return SV_OK;
 }
 
@@ -76,6 +86,29 @@ extern "C" sv_status spec_verify(sv_handle* h, const sv_verify_args* a, void* ws
     return SV_ERR_INVALID;
   const size_t n_tickets = (size_t)a->B * (size_t)(a->kmax + 1);
   if (n_tickets > 0x7FFFFFFF) return SV_ERR_UNSUPPORTED;
+
+  const bool use_stream = stream_eligible(a);
+  {
+    // The scratch words of both kernels sit at offsets that depend on the
+    // call's shape: on a change of layout (or of workspace) clear them first.
+    const int64_t key[6] = {use_stream ? 1 : 0, a->B, a->kmax, a->V,
+                            (int64_t)a->target_dtype * 16 + a->draft_dtype * 4 + a->draft_kind,
+                            a->top_p ? 1 : 0};
+    bool same = h->ws_last == ws;
+    for (int j = 0; j < 6 && same; ++j) same = h->ws_key[j] == key[j];
+    if (!same) {
+      size_t n = workspace_bytes_for(a->B, a->kmax);
+      if (use_stream) {
+        const size_t sb = stream_state_bytes(a);
+        if (sb > n) n = sb;
+      }
+      if (n > ws_bytes) n = ws_bytes;
+      SV_CUDA_TRY(cudaMemsetAsync(ws, 0, n, (cudaStream_t)stream));
+      h->ws_last = ws;
+      for (int j = 0; j < 6; ++j) h->ws_key[j] = key[j];
+    }
+  }
+  if (use_stream) return stream_launch(h, a, ws, ws_bytes, (cudaStream_t)stream);
 
   const bool probs = a->draft_kind == SV_DRAFT_PROBS;
   const Variant* var = nullptr;

@@ -25,3 +25,18 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """The tolerated deviations of every GPU-vs-oracle comparison in the run:
+    accept flips (|u - p/q| < 1e-5), race near-ties and top-p boundary cases."""
+    try:
+        from tests import parity
+    except Exception:  # pragma: no cover
+        return
+    t = parity.TALLY
+    if t["calls"]:
+        terminalreporter.write_line(
+            f"parity: {t['calls']} comparisons, {t['requests']} requests, {t['exact']} exact; "
+            f"tolerated: accept flips {t['accept_flips']}, race near-ties {t['race_ties']}, "
+            f"top-p boundary {t['topp_boundary']}")

@@ -9,6 +9,10 @@ deviations (the fp32 path and the fp64 oracle may round a near-tie either way):
   * top-p boundary: a disagreement at a row whose oracle top-p margin (distance
     of top_p to the edge of the cumulative-mass step) is below TOL.
 Per-row probabilities (p(y), q(y), debug rows) must agree within 1e-6.
+
+The tolerated cases are bounded, not only counted: a comparison fails when
+they exceed one per 10^4 verified rows (at least one per call), and TALLY
+sums them over the session (tests/conftest.py prints it at the end of the run).
 """
 
 from __future__ import annotations
@@ -19,6 +23,25 @@ from oracle import philox, sampling as S
 
 TOL = 1e-5
 PROB_TOL = 1e-6
+
+# session totals of the comparisons (printed by tests/conftest.py)
+TALLY = dict(calls=0, requests=0, exact=0, accept_flips=0, race_ties=0, topp_boundary=0)
+
+
+def tolerated_bound(rows):
+    """Tolerated (counted) deviations allowed in one comparison of `rows`
+    verified rows: one per 10^4 rows, at least one."""
+    return max(1, int(rows) // 10000)
+
+
+def _account(rep, rows, max_tolerated):
+    n = rep["accept_flips"] + rep["race_ties"] + rep["topp_boundary"]
+    bound = tolerated_bound(rows) if max_tolerated is None else max_tolerated
+    TALLY["calls"] += 1
+    TALLY["requests"] += rep["B"]
+    for key in ("exact", "accept_flips", "race_ties", "topp_boundary"):
+        TALLY[key] += rep[key]
+    assert n <= bound, f"{n} tolerated deviations in {rows} rows (bound {bound}): {rep}"
 
 
 def _oracle_request(inp, b, force=None, keep_rows=False):
@@ -37,8 +60,9 @@ def _tokens(r, kmax):
     return t
 
 
-def compare(inp, out, ref=None):
-    """Returns a report dict; raises AssertionError on an untolerated mismatch."""
+def compare(inp, out, ref=None, max_tolerated=None):
+    """Returns a report dict; raises AssertionError on an untolerated mismatch
+    or on more tolerated deviations than tolerated_bound() allows."""
     acc = out["accepted"].cpu().numpy()
     tok = out["out_tokens"].cpu().numpy()
     nem = out["num_emitted"].cpu().numpy()
@@ -96,6 +120,7 @@ def compare(inp, out, ref=None):
                                                   ref["out_tokens"][b].tolist(),
                                                   int(ref["status"][b]))))
     assert not rep["mismatches"], f"untolerated mismatches: {rep['mismatches'][:4]}"
+    _account(rep, int((np.asarray(inp["k"]).astype(np.int64) + 1).sum()), max_tolerated)
     return rep
 
 
@@ -138,7 +163,7 @@ def _oracle_tree(inp, b, force=None):
                          rep=S.tree_rep(inp, b))
 
 
-def compare_tree(inp, out, ref=None):
+def compare_tree(inp, out, ref=None, max_tolerated=None):
     """Tree outputs against the oracle: accepted length, path, tokens and
     status bit-exact, with the same counted tolerances as compare(): a test
     decided the other way where |u - p_r(y)/q(y)| < TOL (the oracle then
@@ -208,4 +233,5 @@ def compare_tree(inp, out, ref=None):
                                                   ref["out_tokens"][b].tolist(),
                                                   int(ref["status"][b]))))
     assert not rep["mismatches"], f"untolerated mismatches: {rep['mismatches'][:4]}"
+    _account(rep, int(np.asarray(inp["n"]).astype(np.int64).sum() + B), max_tolerated)
     return rep

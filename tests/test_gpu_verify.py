@@ -294,10 +294,28 @@ def test_verify_b64_k4(ver, top_p):
     assert parity.compare_debug(inp, dbg) > 0
 
 
+@pytest.mark.parametrize("name", ["verify_b64_k4", "greedy_shared", "paged_bf16", "sweep"])
+def test_streaming_and_cluster_kernels_agree(ver, name):
+    """The two kernels behind spec_verify (the streaming kernel, which serves
+    these calls, and the cluster-resident one that top-k and the repetition
+    penalty use) give the same outputs and the same per-row debug records."""
+    inp = W.build(name) if name != "sweep" else W.sweep(B=64, V=128256, sigma=1.0)
+    a, da, _, _ = run(ver, inp, debug=True)
+    b, db, _, _ = run(ver, inp, flags=binding.FLAG_CLUSTER_PATH, debug=True)
+    for key in ("accepted", "out_tokens", "num_emitted", "status"):
+        assert torch.equal(a[key], b[key]), key
+    report(f"{name} (streaming)", parity.compare(inp, a))
+    sa, sb = da.cpu().numpy()[:, :, 5], db.cpu().numpy()[:, :, 5]
+    both = (sa == sb) & np.isin(sa, (1, 2))
+    fa, fb = da.cpu().numpy().view(np.float32), db.cpu().numpy().view(np.float32)
+    assert np.abs(fa[both][:, :2] - fb[both][:, :2]).max(initial=0.0) <= 2 * parity.PROB_TOL
+
+
 def test_greedy_shared(ver):
     inp = W.greedy_shared()
-    out, _, _, _ = run(ver, inp)
+    out, dbg, _, _ = run(ver, inp, debug=True)
     report("greedy_shared", parity.compare(inp, out))
+    assert parity.compare_debug(inp, dbg) > 0
 
 
 @pytest.mark.parametrize("V,sigma", [(32000, 0.25), (32000, 4.0), (128256, 1.0), (256000, 0.25)])
