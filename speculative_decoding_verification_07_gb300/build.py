@@ -43,19 +43,24 @@ def _compile(src: str, extra) -> str:
     return obj
 
 
-def build(verbose: bool = False, extra=()) -> str:
+def build(verbose: bool = False, extra=(), out: str = LIB, only=None) -> str:
+    """Compile the sources and link `out` (default: the package's library).
+    `extra` nvcc flags apply to the translation units compiled; with `only`,
+    just those sources are recompiled and the others' objects are reused."""
     os.makedirs(BUILD, exist_ok=True)
-    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, list(extra)), SOURCES))
-    tmp = LIB + ".tmp"
+    todo = SOURCES if only is None else [s for s in SOURCES if s in only]
+    with cf.ThreadPoolExecutor(max_workers=len(todo)) as ex:
+        list(ex.map(lambda s: _compile(s, list(extra)), todo))
+    objs = [os.path.join(BUILD, os.path.splitext(s)[0] + ".o") for s in SOURCES]
+    tmp = out + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, out)
     if verbose:
-        print("built", LIB, file=sys.stderr)
-    return LIB
+        print("built", out, file=sys.stderr)
+    return out
 
 
 if __name__ == "__main__":

@@ -167,3 +167,16 @@ sv_status stream_launch(sv_handle* h, const sv_verify_args* a, void* ws, size_t 
 }
 
 }  // namespace sv
+
+#ifdef SV_TRACE
+// Trace set-up of the instrumented build: `buf` holds grid x `cap` events of
+// two 64-bit words (CTA c writes events [c * cap, (c + 1) * cap)).
+extern "C" sv_status sv_trace_setup(void* buf, unsigned cap) {
+  unsigned long long* p = (unsigned long long*)buf;
+  const unsigned zero = 0u;
+  SV_CUDA_TRY(cudaMemcpyToSymbol(sv::stream::g_sv_trace, &p, sizeof(p)));
+  SV_CUDA_TRY(cudaMemcpyToSymbol(sv::stream::g_sv_trace_cap, &cap, sizeof(cap)));
+  SV_CUDA_TRY(cudaMemcpyToSymbol(sv::stream::g_sv_trace_n, &zero, sizeof(zero)));
+  return SV_OK;
+}
+#endif

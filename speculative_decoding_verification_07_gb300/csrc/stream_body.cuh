@@ -18,8 +18,33 @@ __device__ __forceinline__ bool cbar_or(bool v) {
 }
 
 // ---------------------------------------------------------------------------
-// Request completion (finisher lane 0)
+// Request state (finisher lane 0 writes, producers read)
 // ---------------------------------------------------------------------------
+constexpr unsigned long long kResolvedOne = 1ull << 32;  // CallSt::cnt, resolved count
+
+__device__ __forceinline__ unsigned long long ld_acquire64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// The first row of request b known to be decided and not accepted (kNA if none).
+__device__ __forceinline__ int first_nonacc(const SParams& P, char* st, int b) {
+  ReqSt* rq = req_st(st, b);
+  if (P.kmax <= kFastK) {
+    const uint32_t na = (uint32_t)(ld_relaxed64(&rq->w) >> 21) & 0x1FFFFFu;
+    return na ? __ffs(na) - 1 : (int)kNA;
+  }
+  const uint32_t na = ld_relaxed(&rq->na);
+  return na ? (int)(kNA - na) : (int)kNA;
+}
+
+// Rows of request b whose test saw q(y) == 0 (bit i: row i).
+__device__ __forceinline__ unsigned long long qz_mask(const SParams& P, ReqSt* rq) {
+  if (P.kmax <= kFastK) return (ld_relaxed64(&rq->w) >> 42) & 0x1FFFFFull;
+  return ld_relaxed64(&rq->qz);
+}
+
 __device__ __forceinline__ uint32_t qz_bits(unsigned long long qz, int last_row) {
   const unsigned long long m = last_row >= 63 ? ~0ull : ((2ull << last_row) - 1ull);
   return (qz & m) ? SV_ST_Q_ZERO : 0u;
@@ -31,24 +56,24 @@ __device__ __forceinline__ void request_done(char* st) {
 }
 
 // Resolve request b at its first non-accepted row f (rows 0 .. f-1 are
-// accepted and row f is decided).
-static __device__ void resolve(const SParams& P, char* st, int b, int f) {
+// accepted and row f is decided); sf is row f's state if the caller knows it.
+static __device__ void resolve(const SParams& P, char* st, int b, int f, int sf) {
   CallSt* cs = call_st(st);
   ReqSt* rq = req_st(st, b);
-  const uint32_t sf = ld_relaxed(&pair_st(st, P.B, (size_t)b * (P.kmax + 1) + f)->state);
+  if (sf < 0) sf = (int)ld_relaxed(&pair_st(st, P.B, (size_t)b * (P.kmax + 1) + f)->state);
   if (sf == SV_ROW_REJECTED || sf == SV_ROW_BONUS) {
-    const uint32_t q = atomicAdd(&cs->n_slots, 1u);
+    // one atomic counts the resolution and claims the race slot: a waiter that
+    // sees every request resolved also sees every slot claimed
+    const uint32_t q = (uint32_t)atomicAdd(&cs->cnt, kResolvedOne | 1ull);
     Slot* sl = slot_st(st, P.B, (int)q);
     sl->b = (uint32_t)b;
     sl->row = (uint32_t)f;
     sl->kind = sf == SV_ROW_REJECTED ? kRaceResidual : kRaceBonus;
-    __threadfence();
-    atomicAdd(&cs->n_resolved, 1u);  // after n_slots: a waiter that sees all resolved sees every slot
     st_release(&sl->ready, 1u);
     return;
   }
   if (sf == SV_ROW_TERMINAL) {
-    const unsigned long long qz = ld_relaxed64(&rq->qz);
+    const unsigned long long qz = qz_mask(P, rq);
     int32_t* ot = P.out_tokens + (size_t)b * (P.kmax + 1);
     for (int j = 0; j <= P.kmax; ++j) ot[j] = j <= f ? P.tokens[(size_t)b * P.kmax + j] : -1;
     const int eos = P.eos ? P.eos[b] : -1;
@@ -60,14 +85,36 @@ static __device__ void resolve(const SParams& P, char* st, int b, int f) {
     bad_outputs(P, b, SV_ST_BAD_INPUT);
   }
   __threadfence();
-  atomicAdd(&cs->n_resolved, 1u);
+  atomicAdd(&cs->cnt, kResolvedOne);
   request_done(st);
 }
 
-// Publish row i's decision in request b's words; resolve the request if this
-// completes "rows 0 .. f-1 accepted, row f decided".
+// The row at which decision word w resolves its request, or -1.
+__device__ __forceinline__ int resolved_at(unsigned long long w) {
+  const uint32_t na = (uint32_t)(w >> 21) & 0x1FFFFFu;
+  if (!na) return -1;
+  const int f = __ffs(na) - 1;
+  const uint32_t need = (1u << f) - 1u;
+  return ((uint32_t)w & need) == need ? f : -1;
+}
+
+// Publish row i's decision in request b's state; resolve the request if this
+// completes "rows 0 .. f-1 accepted, row f decided".  The row's record and
+// state were written before: the fence orders them before the decision.
 static __device__ void publish(const SParams& P, char* st, int b, int i, int state, bool qzero) {
   ReqSt* rq = req_st(st, b);
+  __threadfence();
+  if (P.kmax <= kFastK) {
+    unsigned long long bit = state == SV_ROW_ACCEPTED ? (1ull << i) : (1ull << (21 + i));
+    if (qzero) bit |= 1ull << (42 + i);
+    const unsigned long long old = atomicOr(&rq->w, bit);
+    const int f = resolved_at(old | bit);
+    if (f < 0 || resolved_at(old) >= 0) return;  // exactly one publisher sees the transition
+    if (atomicCAS(&rq->resolved, 0u, 1u) != 0u) return;  // a timeout report came first
+    __threadfence();
+    resolve(P, st, b, f, f == i ? state : -1);
+    return;
+  }
   if (qzero) atomicOr(&rq->qz, 1ull << i);
   __threadfence();
   unsigned long long acc;
@@ -88,7 +135,7 @@ static __device__ void publish(const SParams& P, char* st, int b, int i, int sta
   const unsigned long long need = f >= 64 ? ~0ull : ((1ull << f) - 1ull);
   if ((acc & need) == need && atomicCAS(&rq->resolved, 0u, 1u) == 0u) {
     __threadfence();
-    resolve(P, st, b, f);
+    resolve(P, st, b, f, f == i ? state : -1);
   }
 }
 
@@ -101,21 +148,22 @@ __device__ __forceinline__ uint32_t take_ticket(const SParams& P) {
   return __shfl_sync(0xffffffffu, t, 0);
 }
 
-// Is row (i, b) worth a ticket, given the request's k, cap and na word?
-// 1: a row to load, 2: a bad request's report (i = 0), 0: nothing.
-__device__ __forceinline__ int interest_of(const SParams& P, int i, int kb, int cap, uint32_t na) {
+// Is row (i, b) worth a ticket, given the request's k, cap and first known
+// non-accepted row fna?  1: a row to load, 2: a bad request's report (i = 0),
+// 0: nothing (absent, or behind a known rejection).
+__device__ __forceinline__ int interest_of(const SParams& P, int i, int kb, int cap, int fna) {
   if (kb < 0 || kb > P.kmax || cap < 1) return i == 0 ? 2 : 0;
   const int last = cap <= kb ? cap - 1 : kb;
   if (i > last) return 0;
-  if (!(P.flags & SV_FLAG_NO_SKIP) && i > 0 && na != 0u && (int)(kNA - na) < i) return 0;
+  if (!(P.flags & SV_FLAG_NO_SKIP) && fna < i) return 0;
   return 1;
 }
 
 __device__ __forceinline__ int row_interest(const SParams& P, char* st, int i, int b) {
   const int kb = P.k ? P.k[b] : P.kmax;
   const int cap = P.max_new ? P.max_new[b] : 0x7FFFFFFF;
-  const uint32_t na = (i > 0 && !(P.flags & SV_FLAG_NO_SKIP)) ? ld_relaxed(&req_st(st, b)->na) : 0u;
-  return interest_of(P, i, kb, cap, na);
+  const int fna = (i > 0 && !(P.flags & SV_FLAG_NO_SKIP)) ? first_nonacc(P, st, b) : (int)kNA;
+  return interest_of(P, i, kb, cap, fna);
 }
 
 // After an uninteresting row R = i * B + b: find the next interesting row
@@ -156,7 +204,7 @@ static __device__ void timeout_sweep(const SParams& P, char* st) {
     if (atomicCAS(&rq->resolved, 0u, 2u) == 0u) {
       bad_outputs(P, b, SV_ST_TIMEOUT);
       __threadfence();
-      atomicAdd(&call_st(st)->n_resolved, 1u);
+      atomicAdd(&call_st(st)->cnt, kResolvedOne);
     }
   }
   if (lane == 0) report(P.err, SV_ERR_TIMEOUT);
@@ -195,20 +243,19 @@ __device__ void producer(const SParams& P, SSmem& sm, char* dyn, char* st) {
         // the request's parameters, one per lane, in one round trip
         int iv = 0;
         float fv = 0.0f;
-        uint32_t uv = 0u;
         if (lane == 0) iv = P.k ? P.k[b] : P.kmax;
         if (lane == 1) iv = P.max_new ? P.max_new[b] : 0x7FFFFFFF;
-        if (lane == 2 && i > 0 && !(P.flags & SV_FLAG_NO_SKIP)) uv = ld_relaxed(&req_st(st, b)->na);
+        if (lane == 2) iv = (i > 0 && !(P.flags & SV_FLAG_NO_SKIP)) ? first_nonacc(P, st, b) : (int)kNA;
         if (lane == 3) fv = P.temperature[b];
         if (lane == 4) fv = P.top_p ? P.top_p[b] : 1.0f;
         if (lane == 5 && i < P.kmax) iv = P.tokens[(size_t)b * P.kmax + i];
         const int kb = __shfl_sync(0xffffffffu, iv, 0);
         const int cap = __shfl_sync(0xffffffffu, iv, 1);
-        const uint32_t na = __shfl_sync(0xffffffffu, uv, 2);
+        const int fna = __shfl_sync(0xffffffffu, iv, 2);
         const float T = __shfl_sync(0xffffffffu, fv, 3);
         const float tp = __shfl_sync(0xffffffffu, fv, 4);
         const int y = __shfl_sync(0xffffffffu, iv, 5);
-        const int what = interest_of(P, i, kb, cap, na);
+        const int what = interest_of(P, i, kb, cap, fna);
         if (what == 1 || (what == 2 && c == 0)) {
           h.kind = what == 1 ? kRowItem : kBadItem;
           h.b = b, h.i = i, h.c = c;
@@ -224,6 +271,7 @@ __device__ void producer(const SParams& P, SSmem& sm, char* dyn, char* st) {
           break;
         }
         t = jump_ticket(P, st, R);
+        if (lane == 0) SV_TR(3, R, t);
         continue;
       }
       const uint32_t rt = t - P.n_static;
@@ -238,9 +286,8 @@ __device__ void producer(const SParams& P, SSmem& sm, char* dyn, char* st) {
           go = true;
           break;
         }
-        const uint32_t nr = ld_acquire(&cs->n_resolved);
-        const uint32_t ns = ld_relaxed(&cs->n_slots);
-        if (nr >= (uint32_t)P.B && ns <= (uint32_t)q) break;
+        const unsigned long long c = ld_acquire64(&cs->cnt);
+        if ((uint32_t)(c >> 32) >= (uint32_t)P.B && (uint32_t)c <= (uint32_t)q) break;
         if (gtimer() - t0 > P.slot_wait_ns) {
           timeout_sweep(P, st);
           break;
@@ -267,10 +314,11 @@ __device__ void producer(const SParams& P, SSmem& sm, char* dyn, char* st) {
       h.rid = (uint32_t)__shfl_sync(0xffffffffu, pv, 1);
       break;
     }
+    if (lane == 0) SV_TR(1, (h.kind << 20) | (h.i << 12) | h.c, h.b);
     // ------------------------------------------------ wait for the stage
     if (used & (1u << s)) {
       bool ok = true;
-      if (lane == 0) ok = mbar_wait_ns(&sm.empty[s], (eph >> s) & 1u, P.err, kStageWaitNs);
+      if (lane == 0) ok = mbar_wait_ns(&sm.empty[s], (eph >> s) & 1u, P.err, kStageWaitNs, 256u);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       eph ^= 1u << s;
       if (!ok) h.kind = kEnd;  // the consumers stopped: end this CTA
@@ -305,6 +353,7 @@ __device__ void producer(const SParams& P, SSmem& sm, char* dyn, char* st) {
         mbar_arrive1(&sm.full[s]);
       }
     }
+    if (lane == 0) SV_TR(2, s, t);
     if (h.kind == kEnd) break;
     s = s + 1 == NS ? 0 : s + 1;
     t = tn, tn = take_ticket(P);
@@ -318,7 +367,8 @@ __device__ void producer(const SParams& P, SSmem& sm, char* dyn, char* st) {
 // most 255 keys below it); thr2 is its value as a packed pair.
 __device__ __forceinline__ void window_floor(uint32_t ref, float depth, float c, uint32_t& fk,
                                              uint32_t& thr2) {
-  const float D = depth > 0.0f ? depth + kDepthMargin : INFINITY;
+  const float D = depth > 0.0f ? depth + kDepthMargin
+                              : (SV_STREAM_DEPTH0 > 0.0f ? SV_STREAM_DEPTH0 : INFINITY);
   const float fv = vkey_value<2>(ref) - D / c;
   uint32_t k = 0u;
   if (fv > -INFINITY) k = key16(__uint_as_float(bf16_pair_of(fv) << 16));
@@ -335,7 +385,7 @@ __device__ __forceinline__ void window_chunk(const char* s, const SliceIter& it,
                                              uint32_t* hist, uint8_t* wb) {
   uint32_t lo = 0u, hi = 0u;
   int cnt = 0;
-#pragma unroll
+#pragma unroll kStreamUnroll
   for (int j = 0; j < kMaxBlk; ++j) {
     if (j < it.nblk) {
       const uint4 g = load_group_bf16(s, it, j);
@@ -363,6 +413,7 @@ __device__ void process_row(const SParams& P, SSmem& sm, const SHdr& h, int s, i
   const float cd = PROBS ? 1.0f : ct;
   SliceIter it;
   it.x0 = h.x0, it.x1 = h.x0 + h.n, it.nblk = GPT, it.V = P.V;
+  it.stride = kCT * kGroup, it.tid = (int)threadIdx.x;
   const size_t pair = (size_t)h.b * (P.kmax + 1) + h.i;
   PairSt* ps = pair_st(st, P.B, pair);
   Fin& F = sm.fin[f];
@@ -392,6 +443,7 @@ __device__ void process_row(const SParams& P, SSmem& sm, const SHdr& h, int s, i
   }
   if (lane == 0) sm.red[warp][0] = mt, sm.red[warp][1] = md;
   cbar();
+  if (ctid == 0) SV_TR(11, 0, 0);
   float Mt = -INFINITY, Md = PROBS ? 0.0f : -INFINITY;
 #pragma unroll
   for (int w = 0; w < kCW; ++w) Mt = fmaxf(Mt, sm.red[w][0]), Md = fmaxf(Md, sm.red[w][1]);
@@ -425,7 +477,7 @@ __device__ void process_row(const SParams& P, SSmem& sm, const SHdr& h, int s, i
 
   // ------------------------------------------------- weight sums
   float sumt = 0.0f, sumd = 0.0f;
-#pragma unroll
+#pragma unroll kStreamUnroll
   for (int j = 0; j < GPT; ++j) {
     const int x = it.x(j);
     if (x < it.x1) {
@@ -447,6 +499,7 @@ __device__ void process_row(const SParams& P, SSmem& sm, const SHdr& h, int s, i
   if (lane == 0) sm.red[warp][2] = sumt, sm.red[warp][3] = sumd;
   if (ctid == 0) sm.hint[0] = hv[0], sm.hint[1] = hv[1], sm.hint[2] = hv[2], sm.hint[3] = hv[3];
   cbar();
+  if (ctid == 0) SV_TR(12, 0, 0);
 
   // ------------------------------------------ top-p window counts
   uint32_t ref_t = 0u, flo_t = 0xFFFFFFFFu, ref_d = 0u, flo_d = 0xFFFFFFFFu;
@@ -481,6 +534,7 @@ __device__ void process_row(const SParams& P, SSmem& sm, const SHdr& h, int s, i
   }
   __syncwarp();
   if (lane == 0) mbar_arrive1(&sm.fin_full[f]);
+  if (ctid == 0) SV_TR(13, f, 0);
 }
 
 template <int EBT, int EBD, bool PROBS>
@@ -496,6 +550,7 @@ __device__ void process_race(const SParams& P, SSmem& sm, const SHdr& h, int s, 
   const bool residual = h.race == kRaceResidual;
   SliceIter it;
   it.x0 = h.x0, it.x1 = h.x0 + h.n, it.nblk = GPT, it.V = P.V;
+  it.stride = kCT * kGroup, it.tid = (int)threadIdx.x;
   RacePart best = {0.0f, 1.0f, 0x7FFFFFFF};
   race_slice<EBT, EBD, PROBS>(sT, sD, it, residual, rt, rd, (uint32_t)h.pos, h.rid, P.seed_lo, P.seed_hi,
                               sm.wb.idx[warp], best);
@@ -524,10 +579,10 @@ __device__ void consumer(const SParams& P, SSmem& sm, char* dyn, char* st) {
   uint32_t fph = 0u, fused = 0u, feph = 0u;
   int s = 0, f = 0;
   for (;;) {
-    bool ok = mbar_wait_ns(&sm.full[s], (fph >> s) & 1u, P.err, kStageWaitNs);
+    bool ok = mbar_wait_ns(&sm.full[s], (fph >> s) & 1u, P.err, kStageWaitNs, 128u);
     fph ^= 1u << s;
     if (fused & (1u << f)) {  // the hand-off slot must be free before this item writes it
-      ok = mbar_wait_ns(&sm.fin_empty[f], (feph >> f) & 1u, P.err, kStageWaitNs) && ok;
+      ok = mbar_wait_ns(&sm.fin_empty[f], (feph >> f) & 1u, P.err, kStageWaitNs, 128u) && ok;
       feph ^= 1u << f;
     }
     fused |= 1u << f;
@@ -535,6 +590,7 @@ __device__ void consumer(const SParams& P, SSmem& sm, char* dyn, char* st) {
     // complete in time ends this CTA's work.
     const bool bad = cbar_or(!ok);
     const SHdr h = sm.hdr[s];
+    if (threadIdx.x == 0) SV_TR(10, h.kind, (h.b << 8) | (h.i << 4) | h.c);
     if (bad || h.kind == kEnd) {
       if (threadIdx.x == 0) {  // tell every finisher to stop
         for (int w = 0; w < kFW; ++w) {
@@ -604,8 +660,14 @@ __device__ __noinline__ int race_row_warp(const char* trow, int V, const RowP& r
 
 template <int EBT, int EBD, bool PROBS>
 __device__ __noinline__ void combine_warp(const SParams& P, float* fh, int b, int i, int has_d, int kb,
-                                          float T, float top_p, int win, char* st) {
+                                          float T, float top_p, int win, int y, char* st) {
   const int lane = threadIdx.x & 31;
+  // the request's scalars, one per lane, loaded together with the headers
+  int rv = 0;
+  if (lane == 0) rv = P.seq_len ? P.seq_len[b] : 0;
+  if (lane == 1) rv = P.request_id ? (int)P.request_id[b] : b;
+  if (lane == 2) rv = P.eos ? P.eos[b] : -1;
+  if (lane == 3) rv = P.max_new ? P.max_new[b] : 0x7FFFFFFF;
   const size_t pair = (size_t)b * (P.kmax + 1) + i;
   const char* parts = P.parts + pair * P.n_ch * (size_t)P.part_bytes;
   const bool greedy = T == 0.0f;
@@ -652,12 +714,14 @@ __device__ __noinline__ void combine_warp(const SParams& P, float* fh, int b, in
   rd.vstar = PROBS ? 0.0f : -INFINITY;
   rd.Z = rd.S, rd.invZ = 1.0f / rd.S;
 
+  if (lane == 0) SV_TR(30, 0, pair);
   // the accept-test operands from the chunk that holds the proposal
   const uint32_t ym = __ballot_sync(0xffffffffu, lane < P.n_ch && hv.z != 0.0f);
   const int ysrc = ym ? __ffs(ym) - 1 : 0;
   const float vt = __shfl_sync(0xffffffffu, hv.x, ysrc), vd = __shfl_sync(0xffffffffu, hv.y, ysrc);
-  const int y = has_d ? P.tokens[(size_t)b * P.kmax + i] : 0;
   const bool y_ok = !has_d || (y >= 0 && y < P.V && ym != 0u);
+  const int r_seq = __shfl_sync(0xffffffffu, rv, 0), r_rid = __shfl_sync(0xffffffffu, rv, 1);
+  const int r_eos = __shfl_sync(0xffffffffu, rv, 2), r_cap = __shfl_sync(0xffffffffu, rv, 3);
   const bool bad_t = !(rt.S >= 1.0f && rt.S <= FLT_MAX) || !(rt.m <= FLT_MAX) || rt.m == -INFINITY;
   const bool bad_d = has_d && (!(rd.S >= 1.0f && rd.S <= FLT_MAX) || !(rd.m <= FLT_MAX) ||
                                (PROBS ? !(rd.m > 0.0f) : rd.m == -INFINITY));
@@ -682,6 +746,7 @@ __device__ __noinline__ void combine_warp(const SParams& P, float* fh, int b, in
         }
       }
     }
+    if (lane == 0) SV_TR(31, need_t, pair);
     if (need_t) exact_top_p_warp<EBT, false>(trow, P.V, rt, top_p * rt.S, fh);
     if (has_d) {
       bool need_d = true;
@@ -699,6 +764,7 @@ __device__ __noinline__ void combine_warp(const SParams& P, float* fh, int b, in
           }
         }
       }
+      if (lane == 0) SV_TR(32, need_d, pair);
       if (need_d) exact_top_p_warp<EBD, PROBS>(drow, P.V, rd, top_p * rd.S, fh);
     }
     if (lane == 0) {  // the depth of this nucleus guides later windows
@@ -721,16 +787,13 @@ __device__ __noinline__ void combine_warp(const SParams& P, float* fh, int b, in
     } else if (has_d) {
       p_y = prob<EBT, false>(vt, rt);
       q_y = prob<EBD, PROBS>(vd, rd);
-      const int pos = (P.seq_len ? P.seq_len[b] : 0) + 1 + i;
-      const uint32_t rid = P.request_id ? P.request_id[b] : (uint32_t)b;
+      const int pos = r_seq + 1 + i;
       u = uniform_from_bits(
-          philox4x32_10(make_uint4(0u, (uint32_t)pos, rid, 1u), P.seed_lo, P.seed_hi).x);
+          philox4x32_10(make_uint4(0u, (uint32_t)pos, (uint32_t)r_rid, 1u), P.seed_lo, P.seed_hi).x);
       qzero = q_y == 0.0f;
       state = (u * q_y < p_y) ? SV_ROW_ACCEPTED : SV_ROW_REJECTED;
       if (state == SV_ROW_ACCEPTED) {
-        const int eos = P.eos ? P.eos[b] : -1;
-        const int cap = P.max_new ? P.max_new[b] : 0x7FFFFFFF;
-        if ((eos >= 0 && y == eos) || (cap <= kb && i == cap - 1)) state = SV_ROW_TERMINAL;
+        if ((r_eos >= 0 && y == r_eos) || (r_cap <= kb && i == r_cap - 1)) state = SV_ROW_TERMINAL;
       }
     } else {
       state = SV_ROW_BONUS;
@@ -750,6 +813,7 @@ __device__ __noinline__ void combine_warp(const SParams& P, float* fh, int b, in
       P.debug[pair] = d;
     }
     st_relaxed(&pair_st(st, P.B, pair)->state, (uint32_t)state);
+    SV_TR(33, state, pair);
     const bool withhold = (P.flags & SV_FLAG_TEST_WITHHOLD) && pair == 0;
     if (!withhold) publish(P, st, b, i, state, qzero);
   }
@@ -760,7 +824,7 @@ template <int EBT, int EBD, bool PROBS>
 __device__ void fin_row(const SParams& P, SSmem& sm, int f, float* fh, char* st) {
   const int lane = threadIdx.x & 31;
   Fin& F = sm.fin[f];
-  const int b = F.b, i = F.i, c = F.c, has_d = F.has_d, kb = F.kb, win = F.win;
+  const int b = F.b, i = F.i, c = F.c, has_d = F.has_d, kb = F.kb, win = F.win, y = F.y;
   const float T = F.T, top_p = F.top_p;
   const size_t pair = (size_t)b * (P.kmax + 1) + i;
   char* part = P.parts + (pair * P.n_ch + c) * (size_t)P.part_bytes;
@@ -789,9 +853,11 @@ __device__ void fin_row(const SParams& P, SSmem& sm, int f, float* fh, char* st)
     last = atomicAdd(&pair_st(st, P.B, pair)->arrive, 1u) + 1u == (uint32_t)P.n_ch;
   }
   last = __shfl_sync(0xffffffffu, last, 0);
+  if (lane == 0) SV_TR(21, last, pair);
   if (last) {
     __threadfence();
-    combine_warp<EBT, EBD, PROBS>(P, fh, b, i, has_d, kb, T, top_p, win, st);
+    combine_warp<EBT, EBD, PROBS>(P, fh, b, i, has_d, kb, T, top_p, win, y, st);
+    if (lane == 0) SV_TR(22, 0, pair);
   }
 }
 
@@ -814,6 +880,7 @@ __device__ void fin_race(const SParams& P, SSmem& sm, int f, char* st) {
     last = atomicAdd(&rq->race_cnt, 1u) + 1u == (uint32_t)P.n_ch;
   }
   last = __shfl_sync(0xffffffffu, last, 0);
+  if (lane == 0) SV_TR(23, last, b);
   if (!last) return;
   __threadfence();
   unsigned long long best = 0ull;
@@ -832,7 +899,7 @@ __device__ void fin_race(const SParams& P, SSmem& sm, int f, char* st) {
     token = race_row_warp<EBT>(trow, P.V, rt, (uint32_t)pos, rid, P.seed_lo, P.seed_hi);
   }
   if (lane == 0) {
-    const unsigned long long qz = ld_relaxed64(&rq->qz);
+    const unsigned long long qz = qz_mask(P, rq);
     int32_t* ot = P.out_tokens + (size_t)b * (P.kmax + 1);
     for (int j = 0; j <= P.kmax; ++j)
       ot[j] = j < r ? P.tokens[(size_t)b * P.kmax + j] : (j == r ? token : -1);
@@ -840,6 +907,7 @@ __device__ void fin_race(const SParams& P, SSmem& sm, int f, char* st) {
     P.num_emitted[b] = r + 1;
     P.status[b] = qz_bits(qz, r) | extra;
     request_done(st);
+    SV_TR(24, r, b);
   }
   __syncwarp();
 }
@@ -852,12 +920,13 @@ __device__ void finisher(const SParams& P, SSmem& sm, char* st) {
   uint32_t ph = 0u;
   for (int f = w;; f = f + kFW >= kNF ? f + kFW - kNF : f + kFW) {
     bool ok = true;
-    if (lane == 0) ok = mbar_wait_ns(&sm.fin_full[f], (ph >> f) & 1u, P.err, kFinWaitNs);
+    if (lane == 0) ok = mbar_wait_ns(&sm.fin_full[f], (ph >> f) & 1u, P.err, kFinWaitNs, 512u);
     ok = __shfl_sync(0xffffffffu, ok, 0);
     __syncwarp();  // lane 0's acquire orders the other lanes' reads of the slot too
     ph ^= 1u << f;
     if (!ok) break;
     const int kind = sm.fin[f].kind;
+    if (lane == 0) SV_TR(20, kind, f);
     if (kind == kEnd) break;
     if (kind == kRowItem) {
       fin_row<EBT, EBD, PROBS>(P, sm, f, fh, st);
@@ -872,7 +941,7 @@ __device__ void finisher(const SParams& P, SSmem& sm, char* st) {
         if (atomicCAS(&rq->resolved, 0u, 1u) == 0u) {
           bad_outputs(P, b, SV_ST_BAD_INPUT);
           __threadfence();
-          atomicAdd(&call_st(st)->n_resolved, 1u);
+          atomicAdd(&call_st(st)->cnt, kResolvedOne);
           request_done(st);
         }
       }
@@ -908,6 +977,9 @@ __global__ void __launch_bounds__(kAllThreads, 1) stream_kernel(const SParams P)
   }
   for (int j = tid; j < kNF * 2 * kBins; j += kAllThreads)
     (&sm.fin[j / (2 * kBins)].hist[0][0])[j % (2 * kBins)] = 0u;
+#ifdef SV_TRACE
+  if (tid == 0) trace_slot() = 0u;
+#endif
   __syncthreads();
   if (warp == kProducerWarp) producer<EBT, EBD, PROBS>(P, sm, dyn, st);
   else if (warp >= kFinisherWarp) finisher<EBT, EBD, PROBS>(P, sm, st);

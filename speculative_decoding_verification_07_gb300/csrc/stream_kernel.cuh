@@ -51,10 +51,10 @@
 namespace sv {
 namespace stream {
 
-constexpr int kCW = 8;               // consumer warps (warps 0-7)
-constexpr int kCT = kCW * 32;        // consumer threads (== the helpers' kThreads)
-constexpr int kProducerWarp = kCW;   // warp 8
-constexpr int kFinisherWarp = kCW + 1;  // warps 9 .. 9 + kFW - 1
+constexpr int kCW = 16;              // consumer warps (warps 0-15)
+constexpr int kCT = kCW * 32;        // consumer threads
+constexpr int kProducerWarp = kCW;   // warp 16
+constexpr int kFinisherWarp = kCW + 1;  // warps 17 .. 17 + kFW - 1
 constexpr int kFW = 2;               // finisher warps; hand-off slot f goes to finisher f % kFW
 constexpr int kAllThreads = kCT + 32 + 32 * kFW;
 constexpr int kNF = 4;               // finisher hand-off slots
@@ -64,7 +64,17 @@ constexpr int kMaxNs = 4;
 constexpr int kMaxChunks = 32;
 constexpr uint32_t kNA = 1024u;      // request word na = kNA - first non-accepted row (0: none)
 constexpr float kDepthMargin = 1.0f; // log2 units added to the deepest nucleus seen
-static_assert(kCT == sv::kThreads, "the shared row helpers assume 256 consumer threads");
+// Tuning: unroll of the consumers' group loops (the code must stay small
+// enough for the instruction cache) and the window depth, in log2 units of
+// the weight, used before any nucleus of the call has been measured (0: the
+// full 256-key window).
+#ifndef SV_STREAM_UNROLL
+#define SV_STREAM_UNROLL 8
+#endif
+#ifndef SV_STREAM_DEPTH0
+#define SV_STREAM_DEPTH0 0.0f
+#endif
+constexpr int kStreamUnroll = SV_STREAM_UNROLL;
 
 template <int EBT, int EBD>
 __host__ __device__ constexpr int chunk_elems() {
@@ -93,22 +103,30 @@ struct Hdr {            // fixed words at byte 64 of the workspace header
 };
 
 struct CallSt {         // per call, zeroed by the previous call
-  uint32_t n_slots;     // race slots claimed
-  uint32_t n_resolved;  // requests resolved (any outcome)
+  unsigned long long cnt;  // (requests resolved << 32) | race slots claimed
   uint32_t n_done;      // requests whose outputs are written
   uint32_t depth_t;     // deepest target nucleus seen, log2 units (float bits)
   uint32_t depth_d;
   uint32_t pad[11];
 };
+static_assert(sizeof(CallSt) == 64, "");
 
+// Decisions of a request.  With kmax <= kFastK one 64-bit word holds them
+// all -- bit i: row i accepted; bit 21 + i: row i decided and not accepted;
+// bit 42 + i: row i's test saw q(y) == 0 -- so that one atomic OR both
+// publishes a decision and tells its issuer whether it completed the request
+// ("rows 0 .. f-1 accepted, row f not").  Larger kmax use acc / qz / na with
+// a fence-separated check and a CAS on `resolved`.
+constexpr int kFastK = 20;
 struct ReqSt {
-  unsigned long long acc;   // bit i: row i accepted
-  unsigned long long qz;    // bit i: row i's test saw q(y) == 0
+  unsigned long long acc;   // bit i: row i accepted (kmax > kFastK)
+  unsigned long long qz;    // bit i: row i's test saw q(y) == 0 (kmax > kFastK)
   unsigned long long best;  // race winner: (key bits << 32) | (0xFFFFFFFF - token)
-  uint32_t na;              // kNA - first non-accepted row, or 0
+  unsigned long long w;     // the single decision word (kmax <= kFastK)
+  uint32_t na;              // kNA - first non-accepted row, or 0 (kmax > kFastK)
   uint32_t resolved;        // 0 -> 1 by the resolver (2: timed out)
   uint32_t race_cnt;        // race items finished
-  uint32_t pad[7];
+  uint32_t pad[5];
 };
 static_assert(sizeof(ReqSt) == 64, "");
 
@@ -277,16 +295,48 @@ __device__ __forceinline__ unsigned long long gtimer() {
 constexpr unsigned long long kStageWaitNs = 4000000000ull;   // consumers, producer
 constexpr unsigned long long kFinWaitNs = 6000000000ull;     // finishers wait on the consumers
 __device__ __forceinline__ bool mbar_wait_ns(unsigned long long* bar, uint32_t parity, int* err,
-                                             unsigned long long ns) {
+                                             unsigned long long ns, uint32_t max_sleep = 256u) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = gtimer();
+  // The suspend hint of try_wait parks the warp only briefly: back off with
+  // a sleep between tries, so that waiting warps leave the issue slots (and
+  // the instruction cache) to the warps that have work.
+  uint32_t sleep = 32u;
   for (;;) {
+    __nanosleep(sleep);
     if (mbar_try_wait(bar, parity)) return true;
     if (gtimer() - t0 > ns) break;
+    sleep = sleep < max_sleep ? sleep * 2u : max_sleep;
   }
   report(err, SV_ERR_TIMEOUT);
   return false;
 }
+
+// Optional event trace (built only with -DSV_TRACE): timestamped events of
+// the pipeline roles, for studying where an item's time goes.  Compiled out
+// otherwise.
+#ifdef SV_TRACE
+static __device__ unsigned long long* g_sv_trace = nullptr;
+static __device__ unsigned int g_sv_trace_n = 0u, g_sv_trace_cap = 0u;  // cap: events per CTA
+__device__ __forceinline__ unsigned int& trace_slot() {
+  __shared__ unsigned int n;  // events recorded by this CTA
+  return n;
+}
+__device__ __forceinline__ void trace_ev(uint32_t ev, uint32_t a, uint32_t b) {
+  const unsigned idx = atomicAdd(&trace_slot(), 1u);
+  if (idx < g_sv_trace_cap) {
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    unsigned long long* p = g_sv_trace + 2ull * ((unsigned long long)blockIdx.x * g_sv_trace_cap + idx);
+    p[0] = gtimer();
+    p[1] = ((unsigned long long)(ev & 0xFF) << 56) | ((unsigned long long)(smid & 0xFF) << 48) |
+           ((unsigned long long)(a & 0xFFFFFF) << 24) | (b & 0xFFFFFF);
+  }
+}
+#define SV_TR(ev, a, b) trace_ev((ev), (uint32_t)(a), (uint32_t)(b))
+#else
+#define SV_TR(ev, a, b) ((void)0)
+#endif
 
 // Release the stage: each consumer warp arrives once after its last read.
 __device__ __forceinline__ void release_stage(SSmem& sm, int s) {
@@ -463,16 +513,23 @@ __device__ __forceinline__ int window_boundary(const SParams& P, const char* par
 #pragma unroll
   for (int q = 0; q < 8; ++q) cnt[q] = 0u;
   const char* base = parts + kPartHead + side * 512 + 16 * lane;
-#pragma unroll 4
-  for (int c = 0; c < P.n_ch; ++c) {
-    const uint32_t refc = __shfl_sync(0xffffffffu, my_ref, c);
-    const uint4 v = __ldcg(reinterpret_cast<const uint4*>(base + (size_t)c * P.part_bytes));
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  for (int c0 = 0; c0 < P.n_ch; c0 += 8) {
+    uint4 v[8];  // issue the loads of 8 chunks together (one round trip)
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const uint32_t j = ((uint32_t)(8 * lane + q) - rK) & 255u;
-      const uint32_t key = K - j;
-      if (key <= refc) cnt[q] += (w[q >> 1] >> (16 * (q & 1))) & 0xFFFFu;
+    for (int u = 0; u < 8; ++u)
+      v[u] = c0 + u < P.n_ch ? __ldcg(reinterpret_cast<const uint4*>(base + (size_t)(c0 + u) * P.part_bytes))
+                             : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint32_t refc = __shfl_sync(0xffffffffu, my_ref, (c0 + u) & 31);
+      if (c0 + u >= P.n_ch) continue;
+      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const uint32_t j = ((uint32_t)(8 * lane + q) - rK) & 255u;
+        const uint32_t key = K - j;
+        if (key <= refc) cnt[q] += (w[q >> 1] >> (16 * (q & 1))) & 0xFFFFu;
+      }
     }
   }
 #pragma unroll

@@ -308,6 +308,7 @@ __global__ void __launch_bounds__(kThreads, 2) tree_kernel(const TreeParams P) {
   it.x1 = min(P.V, it.x0 + P.slice);
   it.nblk = it.x1 > it.x0 ? (it.x1 - it.x0 + kBlk - 1) / kBlk : 0;
   it.V = P.V;
+  it.stride = kBlk, it.tid = (int)threadIdx.x;
 
   for (;;) {
     if (lead) s_ticket = (int)atomicAdd(P.ctr, 1u);

@@ -476,9 +476,12 @@ __device__ __forceinline__ void lds_group_or_neutral(Grp<EB>& g, const char* sba
 }
 
 // The thread's groups of a slice: group k starts at element x0 + k*kBlk + tid*8.
+// stride: elements between a thread's consecutive groups (threads x 8);
+// tid: the thread's index among the threads that share the slice.
 struct SliceIter {
   int x0, x1, nblk, V;
-  __device__ __forceinline__ int x(int blk) const { return x0 + blk * kBlk + (int)threadIdx.x * kGroup; }
+  int stride, tid;
+  __device__ __forceinline__ int x(int blk) const { return x0 + blk * stride + tid * kGroup; }
 };
 
 // ---------------------------------------------------------------------------
@@ -664,14 +667,14 @@ __device__ __forceinline__ void window_commit_bf16(const char* s, uint32_t kmax,
   const int total = __shfl_sync(0xffffffffu, incl, 31);
   if (total == 0) return;
   const uint16_t* sv = reinterpret_cast<const uint16_t*>(s);
-  const int base = (int)threadIdx.x * kGroup;  // slice offset of this thread's group 0
+  const int base = it.tid * kGroup;  // slice offset of this thread's group 0
   unsigned long long mk = ((unsigned long long)mhi << 32) | mlo;
   if (total <= 512) {
     int pos = incl - cnt;
     while (mk) {
       const int bit = __ffsll((long long)mk) - 1;
       mk &= mk - 1ull;
-      const uint32_t key = bf16_order_key(sv[base + (bit >> 3) * kBlk + (bit & 7)]);
+      const uint32_t key = bf16_order_key(sv[base + (bit >> 3) * it.stride + (bit & 7)]);
       wb[pos++] = (uint8_t)(kmax - key);
     }
     flush_bins(hist, wb, total);
@@ -688,7 +691,7 @@ __device__ __forceinline__ void window_commit_bf16(const char* s, uint32_t kmax,
     while (m) {
       const int e = __ffs(m) - 1;
       m &= m - 1;
-      const uint32_t key = bf16_order_key(sv[base + blk * kBlk + e]);
+      const uint32_t key = bf16_order_key(sv[base + blk * it.stride + e]);
       wb[pos++] = (uint8_t)(kmax - key);
     }
     flush_bins(hist, wb, tot);
@@ -1121,12 +1124,12 @@ __device__ __noinline__ void race_slice(const char* st, const char* sd, const Sl
       else m_hi |= msk << (8 * (blk - 4));
     }
   }
-  const int base = (int)threadIdx.x * kGroup;  // slice offset of this thread's group 0
+  const int base = it.tid * kGroup;  // slice offset of this thread's group 0
   auto emit = [&](uint32_t m, int half, int pos) {
     while (m) {
       const int bit = __ffs(m) - 1;
       m &= m - 1;
-      wb[pos++] = (uint16_t)(base + (half * 4 + (bit >> 3)) * kBlk + (bit & 7));
+      wb[pos++] = (uint16_t)(base + (half * 4 + (bit >> 3)) * it.stride + (bit & 7));
     }
   };
   const int incl = warp_incl_scan(cnt);
@@ -1435,6 +1438,7 @@ __global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
     it.x1 = min(P.V, it.x0 + P.slice);
     it.nblk = it.x1 > it.x0 ? (it.x1 - it.x0 + kBlk - 1) / kBlk : 0;
     it.V = P.V;
+    it.stride = kBlk, it.tid = (int)threadIdx.x;
 
     // ------------------------------------ TMA: this CTA's slice of both rows
     if (tid == 0) {
