@@ -579,15 +579,21 @@ __device__ void consumer(const SParams& P, SSmem& sm, char* dyn, char* st) {
   uint32_t fph = 0u, fused = 0u, feph = 0u;
   int s = 0, f = 0;
   for (;;) {
-    bool ok = mbar_wait_ns(&sm.full[s], (fph >> s) & 1u, P.err, kStageWaitNs, 128u);
-    fph ^= 1u << s;
-    if (fused & (1u << f)) {  // the hand-off slot must be free before this item writes it
-      ok = mbar_wait_ns(&sm.fin_empty[f], (feph >> f) & 1u, P.err, kStageWaitNs, 128u) && ok;
-      feph ^= 1u << f;
+    // Thread 0 waits for the stage's data and for a free hand-off slot; the
+    // other consumer warps wait in the barrier (issuing nothing), which also
+    // carries the outcome, so every consumer thread takes the same path (a
+    // wait that did not complete in time ends this CTA's work).  The barrier
+    // orders the stage's contents, seen complete by thread 0, before every
+    // thread's reads.
+    bool ok = true;
+    if (threadIdx.x == 0) {
+      ok = mbar_wait_ns(&sm.full[s], (fph >> s) & 1u, P.err, kStageWaitNs, 64u);
+      if (fused & (1u << f))
+        ok = mbar_wait_ns(&sm.fin_empty[f], (feph >> f) & 1u, P.err, kStageWaitNs, 64u) && ok;
     }
+    fph ^= 1u << s;
+    if (fused & (1u << f)) feph ^= 1u << f;
     fused |= 1u << f;
-    // Every consumer thread takes the same path: a wait that did not
-    // complete in time ends this CTA's work.
     const bool bad = cbar_or(!ok);
     const SHdr h = sm.hdr[s];
     if (threadIdx.x == 0) SV_TR(10, h.kind, (h.b << 8) | (h.i << 4) | h.c);
