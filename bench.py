@@ -294,7 +294,8 @@ def run_ours(args):
     for d in dsets:
         d["request_id"] = replicas.rank_request_ids(d["request_id"], rank)
     BS = 16
-    steps_total = args.warmup + args.steps + 64 * 6 + 16
+    N_LONG = 2000  # steps of the longer (context) region below
+    steps_total = args.warmup + args.steps + N_LONG + 64 * 6 + 64
     max_blocks = (8192 + (k + 1) * steps_total) // BS + 4
     pool = binding.BlockPool(ver.handle, B * max_blocks, BS)
     table = torch.full((B, max_blocks), -1, dtype=torch.int32, device=dev)
@@ -337,6 +338,7 @@ def run_ours(args):
             evs[i][3].record()
 
     # warm-up (eager), then capture a graph of G steps cycling the input sets
+    # and a graph of one step, so that exactly args.steps steps are timed
     for i in range(max(args.warmup, 3)):
         step(i)
     torch.cuda.synchronize()
@@ -344,19 +346,21 @@ def run_ours(args):
     G = 8
     s = torch.cuda.Stream(device=dev)
     s.wait_stream(torch.cuda.current_stream())
-    graph = torch.cuda.CUDAGraph()
+    graph, graph1 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     with torch.cuda.stream(s):
         with torch.cuda.graph(graph, stream=s):
             for i in range(G):
                 step(i, stream=s)
+        with torch.cuda.graph(graph1, stream=s):
+            step(0, stream=s)
     torch.cuda.synchronize()
     with torch.cuda.stream(s):
         for _ in range(2):
             graph.replay()
     torch.cuda.synchronize()
 
-    reps = max(1, args.steps // G)
-    K = reps * G
+    K = max(1, args.steps)
+    reps, tail = K // G, K % G
     t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
@@ -366,13 +370,23 @@ def run_ours(args):
         t0e.record(s)
         for _ in range(reps):
             graph.replay()      # replays on the current stream, s
+        for _ in range(tail):
+            graph1.replay()
         t1e.record(s)
         torch.cuda.synchronize()
     barrier()
     ms = t0e.elapsed_time(t1e)
     assert ver.error() == 0, "device error in the timed region"
     value, ms = replicas.whole_job_rate(ms, rows * K, device=dev)
-
+    # the same steps over a longer region (a steadier figure; context only)
+    nlong = max(G, (N_LONG // G) * G)
+    with torch.cuda.stream(s):
+        t0e.record(s)
+        for _ in range(nlong // G):
+            graph.replay()
+        t1e.record(s)
+        torch.cuda.synchronize()
+    long_ms = t0e.elapsed_time(t1e) / nlong
     nvtx.range_pop()
     # verify-kernel duration: CUDA events around each launch of G more steps
     nvtx.range_push("per-launch kernel timings")
@@ -424,16 +438,21 @@ def run_ours(args):
     nvtx.range_push("token trees")
     tree_line = tree_run(ver, dev, peak)
     nvtx.range_pop()
+    nvtx.range_push("configurations")
+    legs = config_legs(ver, dev, peak) if not args.no_legs else {"skipped": "--no-legs"}
+    nvtx.range_pop()
 
     line = {"metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": ws, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": dict(WORKLOAD, parallelism=f"replicas x{ws} (requests shard, no collective)",
                            step="bfl_reserve + spec_verify + kv_commit_rollback",
-                           launch=f"CUDA graph of {G} steps",
+                           launch=f"CUDA graphs of {G} steps and of 1 step (programmatic "
+                                  f"dependent launches between the step's kernels)",
                            l2=f"inputs rotate over {N_SETS} batches of "
                               f"{full_bytes(sets[0]) / 1e6:.1f} MB (> L2)"),
             "gpu_launches": 3 * K,
+            "ms_per_step_long": long_ms, "steps_long": nlong,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "kernel": "verify_kernel<bf16,bf16>",
@@ -447,7 +466,8 @@ def run_ours(args):
             "small_kernels_us": {"bfl_reserve": reserve_us, "kv_commit_rollback": commit_us},
             "clocks": clk.summary(),
             "e2e": e2e,
-            "kv_commit_copy": copy_line, "tree_verify": tree_line}
+            "kv_commit_copy": copy_line, "tree_verify": tree_line,
+            "configs": legs}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(sets[0])
         line["cpu_baseline_all_cores"] = cpu_baseline_all_cores()
@@ -634,6 +654,106 @@ def tree_run(ver, dev, peak):
             "shape": "64 binary trees of depth 3 (14 nodes), V=128256 bf16, T=0.8, top-p 0.95"}
 
 
+CONFIG_LEGS = [
+    # name, batch recipe, notes
+    ("C1", dict(B=1, k=5, V=1024, target_sd=2.0, draft_sd=0.5, temperature=1.0,
+                target_dtype="f32", draft_dtype="f32"), "fp32 logits, contiguous KV"),
+    ("C2", dict(B=8, k=4, V=32000, target_sd=2.0, draft_sd=0.5, temperature="U[0.5,1.2]"),
+     "bf16, T_b ~ U[0.5, 1.2]"),
+    ("C3", dict(B=64, k="U{1..8}", V=128256, temperature=0.8, top_p=0.95, draft_kind="probs"),
+     "bf16 target, fp32 draft probabilities, ragged k, top-p 0.95"),
+    ("M", dict(B=64, k=4, V=128256, temperature=0.8, top_p=0.95), "the metric workload"),
+    ("M_stream", dict(B=64, k=4, V=128256, temperature=0.8, top_p=0.95, stream=True),
+     "the metric workload on the streaming kernel (SV_FLAG_STREAM_PATH)"),
+    ("C4", dict(B=256, k=4, V=151936, temperature="half0"), "half the rows T = 0, half T = 1"),
+] + [(f"C5_B{B}_V{V}", dict(B=B, k=8, V=V, temperature=1.0), "sweep point, sigma 1")
+     for B in (64, 256, 1024) for V in (32000, 128256, 256000)]
+
+
+def config_legs(ver, dev, peak, budget_s=90.0):
+    """Throughput of spec_verify on every configuration of the benchmark set
+    (device-generated inputs, rotated over enough sets to exceed L2): rows/s,
+    GB/s of the full and of the needed bytes, and fractions of the measured
+    peak and of 8 TB/s.  Per leg: the mean of CUDA-event-timed launches."""
+    import torch
+
+    from speculative_decoding_verification_07_gb300 import binding
+    from speculative_decoding_verification_07_gb300 import device_workloads as DW
+    legs = {}
+    t_start = time.perf_counter()
+    for li, (name, r, note) in enumerate(CONFIG_LEGS):
+        if time.perf_counter() - t_start > budget_s:
+            legs[name] = {"skipped": "time budget"}
+            continue
+        B, V = r["B"], r["V"]
+        g = torch.Generator(device="cpu")
+        g.manual_seed(4000 + li)
+        k = r["k"]
+        if k == "U{1..8}":
+            k = torch.randint(1, 9, (B,), generator=g)
+        T = r.get("temperature", 1.0)
+        if T == "U[0.5,1.2]":
+            T = 0.5 + 0.7 * torch.rand(B, generator=g)
+        elif T == "half0":
+            T = torch.tensor([0.0 if b % 2 == 0 else 1.0 for b in range(B)])
+        dt = {"f32": torch.float32, None: torch.bfloat16}
+        kw = dict(target_sd=r.get("target_sd", 3.0), draft_sd=r.get("draft_sd", 1.0),
+                  temperature=T, top_p=r.get("top_p", 1.0), draft_kind=r.get("draft_kind", "logits"),
+                  target_dtype=dt[r.get("target_dtype")], draft_dtype=dt[r.get("draft_dtype")])
+        one = DW.make_batch(B, k, V, device=dev, seed=5000 + 31 * li, **kw)
+        per = DW.full_bytes(one)
+        n_sets = DW.sets_for(per)
+        sets = [one] + [DW.make_batch(B, k, V, device=dev, seed=5000 + 31 * li + s, **kw)
+                        for s in range(1, n_sets)]
+        kmax = one["kmax"]
+        outs = [ver.outputs(B, kmax) for _ in sets]
+        use_top_p = r.get("top_p", 1.0) < 1.0
+        args = [binding.make_args(target=d["target"], draft=d["draft"], draft_tokens=d["draft_tokens"],
+                                  temperature=d["temperature"], k=d["k"],
+                                  top_p=d["top_p"] if use_top_p else None, seed=d["seed"],
+                                  request_id=d["request_id"], seq_len=d["seq_len"],
+                                  draft_kind=d["draft_kind"],
+                                  flags=binding.FLAG_STREAM_PATH if r.get("stream") else 0, **o)
+                for d, o in zip(sets, outs)]
+        wsp = ver.ensure_workspace(max(args, key=lambda a: binding.sv_workspace_size(a)))
+
+        def call(i):
+            a = args[i % len(args)]
+            binding.spec_verify(ver.handle, a, ver.ensure_workspace(a), None)
+
+        for i in range(max(3, len(sets))):
+            call(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call(0)
+        e1.record()
+        torch.cuda.synchronize()
+        est = max(e0.elapsed_time(e1), 1e-3)
+        n = int(min(200, max(10, 40.0 / est)))
+        e0.record()
+        for i in range(n):
+            call(i)
+        e1.record()
+        torch.cuda.synchronize()
+        assert ver.error() == 0, f"device error in config leg {name}"
+        us = e0.elapsed_time(e1) / n * 1e3
+        rows = float(np.mean([(d["k"].long() + 1).sum().item() for d in sets]))
+        bfull = float(np.mean([DW.full_bytes(d) for d in sets]))
+        bneed = float(np.mean([DW.needed_bytes(d, o["accepted"]) for d, o in zip(sets, outs)]))
+        gfull, gneed = bfull / (us * 1e-6) / 1e9, bneed / (us * 1e-6) / 1e9
+        kern = "stream" if r.get("stream") else "cluster"
+        legs[name] = {"B": B, "k": "U{1..8}" if r["k"] == "U{1..8}" else r["k"], "V": V,
+                      "note": note, "kernel": kern, "us": us, "rows_per_s": rows / (us * 1e-6),
+                      "bytes_full": bfull, "bytes_needed": bneed, "GBs_full": gfull,
+                      "GBs_needed": gneed, "frac_full": gfull / peak, "frac_of_8tbs": gfull / 8000.0,
+                      "l2": f"{len(sets)} input sets of {per / 1e6:.1f} MB rotate",
+                      "launches": n}
+        del sets, outs, args, one
+        torch.cuda.empty_cache()
+    return legs
+
+
 def kernel_source_sha():
     import hashlib
     h = hashlib.sha256()
@@ -651,6 +771,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-legs", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

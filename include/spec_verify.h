@@ -81,9 +81,15 @@ typedef enum { SV_DRAFT_LOGITS = 0, SV_DRAFT_PROBS = 1 } sv_draft_kind;
  * there resolves nothing either way, but then the request's outcome would not
  * depend on the withheld row). */
 #define SV_FLAG_TEST_WITHHOLD 2u
-/* Run the call on the cluster-resident kernel even where the streaming kernel
- * would serve it (both compute the same results; for comparisons and tests). */
+/* Kernel selection (both kernels compute the same results).  By default a
+ * call runs on the cluster-resident kernel.  SV_FLAG_STREAM_PATH asks for the
+ * streaming kernel (persistent producer/consumer/finisher CTAs, window and
+ * race items queued across SMs), which serves calls without top-k or the
+ * repetition penalty whose top-p, if any, is on bf16 logit rows; other calls
+ * stay on the cluster kernel.  SV_FLAG_CLUSTER_PATH forces the cluster kernel
+ * and wins over SV_FLAG_STREAM_PATH. */
 #define SV_FLAG_CLUSTER_PATH 4u
+#define SV_FLAG_STREAM_PATH 8u
 
 /* sv_row_debug.state */
 #define SV_ROW_NONE 0

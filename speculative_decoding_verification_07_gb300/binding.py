@@ -34,7 +34,8 @@ ST_Q_ZERO, ST_BAD_INPUT, ST_RESIDUAL_EMPTY, ST_TIMEOUT = 1, 2, 4, 8
 ST_EOS, ST_CAPPED = 16, 32
 FLAG_NO_SKIP = 1
 FLAG_TEST_WITHHOLD = 2  # testing aid: see SV_FLAG_TEST_WITHHOLD
-FLAG_CLUSTER_PATH = 4   # run on the cluster-resident kernel (see SV_FLAG_CLUSTER_PATH)
+FLAG_CLUSTER_PATH = 4   # force the cluster-resident kernel (see SV_FLAG_CLUSTER_PATH)
+FLAG_STREAM_PATH = 8    # ask for the streaming kernel (see SV_FLAG_STREAM_PATH)
 ROW_NONE, ROW_ACCEPTED, ROW_REJECTED, ROW_SKIPPED, ROW_INVALID, ROW_BONUS, ROW_TERMINAL = range(7)
 
 EXPORTS = ("sv_verify_args_size", "sv_create", "sv_destroy", "sv_workspace_size",
@@ -421,6 +422,7 @@ class Verifier:
         self.device = torch.device("cuda", device)
         self.handle = sv_create(device)
         self.workspace = None
+        self.path_flags = 0  # kernel selection added to every verify() call
 
     def close(self):
         if self.handle is not None:
@@ -447,9 +449,12 @@ class Verifier:
                     status=torch.empty(B, dtype=torch.int32, device=d))
 
     def verify(self, *, target, draft, draft_tokens, temperature, out=None, stream=None, **kw):
-        """Run spec_verify; returns the output tensors (allocated unless given)."""
+        """Run spec_verify; returns the output tensors (allocated unless given).
+        The handle's `path_flags` (kernel selection, 0 by default) are added
+        to the call's flags."""
         B, rows, _ = target.shape
         out = out or self.outputs(B, rows - 1)
+        kw["flags"] = int(kw.get("flags", 0)) | self.path_flags
         a = make_args(target=target, draft=draft, draft_tokens=draft_tokens,
                       temperature=temperature, **out, **kw)
         ws = self.ensure_workspace(a)

@@ -67,7 +67,7 @@ const SVariant* find_variant(const sv_verify_args* a) {
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct Layout {
-  size_t state0, state1, state_bytes, rows, parts, total;
+  size_t state0, state1, state_bytes, rows, pstats, parts, total;
   int n_ch, part_bytes, hist;
 };
 
@@ -75,25 +75,27 @@ Layout layout_for(const sv_verify_args* a, const SVariant& v) {
   Layout L;
   L.n_ch = (a->V + v.chunk - 1) / v.chunk;
   L.hist = (a->top_p != nullptr && v.eb_t == 2 && v.eb_d == 2 && !v.probs_kind) ? 1 : 0;
-  L.part_bytes = stream::kPartHead + (L.hist ? 2 * 512 : 0);
+  L.part_bytes = stream::kPartHead + (L.hist ? 2 * 512 : 0);  // 16-byte aligned
   const size_t pairs = (size_t)a->B * (size_t)(a->kmax + 1);
   L.state_bytes = align256(stream::state_bytes_for(a->B, a->kmax));
   L.state0 = align256(workspace_bytes_for(a->B, a->kmax));
   L.state1 = L.state0 + L.state_bytes;
   L.rows = L.state1 + L.state_bytes;
-  L.parts = L.rows + align256(pairs * sizeof(stream::RowRec));
+  L.pstats = L.rows + align256(pairs * sizeof(stream::RowRec));
+  L.parts = L.pstats + align256(pairs * sizeof(stream::PairStats));
   L.total = L.parts + align256(pairs * (size_t)L.n_ch * (size_t)L.part_bytes);
   return L;
 }
 
 }  // namespace
 
-// Calls the streaming kernel serves: no top-k, no repetition penalty, V within
-// 32 chunks, and top-p only on bf16 logit rows (fp32 rows with top-p, and the
-// other options, go to the cluster kernel).  fp32 rows need ld % 8 == 0 so
-// that whole 8-element groups stay inside each row.
+// Calls the streaming kernel serves (when SV_FLAG_STREAM_PATH asks for it): no
+// top-k, no repetition penalty, V within 32 chunks, and top-p only on bf16
+// logit rows (fp32 rows with top-p, and the other options, go to the cluster
+// kernel).  fp32 rows need ld % 8 == 0 so that whole 8-element groups stay
+// inside each row.
 bool stream_eligible(const sv_verify_args* a) {
-  if (a->flags & SV_FLAG_CLUSTER_PATH) return false;
+  if (!(a->flags & SV_FLAG_STREAM_PATH) || (a->flags & SV_FLAG_CLUSTER_PATH)) return false;
   if (a->top_k || a->rep_penalty) return false;
   const SVariant* v = find_variant(a);
   if (!v) return false;
@@ -124,8 +126,11 @@ sv_status stream_launch(sv_handle* h, const sv_verify_args* a, void* ws, size_t 
   const Layout L = layout_for(a, *v);
   if (ws_bytes < L.total) return SV_ERR_INVALID;
   const size_t pairs = (size_t)a->B * (size_t)(a->kmax + 1);
-  const size_t n_static = pairs * (size_t)L.n_ch;
-  if (n_static + (size_t)a->B * (size_t)L.n_ch + 4096 > 0xFFFFFFF0u) return SV_ERR_UNSUPPORTED;
+  const int n_blk = (L.n_ch + stream::kBatch - 1) / stream::kBatch;
+  const size_t n_static = pairs * (size_t)n_blk;
+  const size_t n_slots = stream::slots_for(a->B, a->kmax);
+  if (n_static + 4096 > 0xFFFFFFF0u || (n_slots + 1) * (size_t)L.n_ch + 4096 > 0xFFFFFFF0u)
+    return SV_ERR_UNSUPPORTED;
 
   char* base = (char*)ws;
   stream::SParams P;
@@ -144,12 +149,15 @@ sv_status stream_launch(sv_handle* h, const sv_verify_args* a, void* ws, size_t 
   P.state[1] = base + L.state1;
   P.state_words = L.state_bytes / 4;
   P.rows = reinterpret_cast<stream::RowRec*>(base + L.rows);
+  P.pstats = reinterpret_cast<stream::PairStats*>(base + L.pstats);
   P.parts = base + L.parts;
+  P.n_slots = (uint32_t)n_slots;
   P.part_bytes = L.part_bytes;
   P.hist = L.hist;
   P.err = h->d_err;
   P.slot_wait_ns = (a->flags & SV_FLAG_TEST_WITHHOLD) ? 250000ull : 2000000000ull;
   P.n_static = (uint32_t)n_static;
+  P.n_blk = n_blk;
 
   const StreamFn fn = v->fn();
   SV_CUDA_TRY(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, v->dyn_smem));

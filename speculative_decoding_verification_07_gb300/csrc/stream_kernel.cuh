@@ -8,42 +8,38 @@
 // at full rate.
 //
 // GB300 design
-//  * One persistent CTA per SM with three roles: a producer warp, eight
-//    consumer warps and a finisher warp.  The producer takes work tickets
-//    from a counter in the workspace and pulls each item into a ring of
-//    shared-memory stages with 1-D TMA bulk copies (cp.async.bulk, one
-//    mbarrier per stage).  The consumers work the stages in order, hand each
-//    back through an "empty" mbarrier and pass their results to the finisher
-//    through a small shared-memory ring; the finisher does everything that
-//    waits on global memory (partials, arrival counters, the row-pair
-//    combine, the request resolution), so the consumers only compute.  No CTA
-//    ever waits on another CTA's shared memory: a row's bytes stay on chip
-//    only while its own statistics are taken.
-//  * A row item is one vocabulary chunk of one row pair (target row i and, for
-//    i < k_b, draft row i of request b).  Tickets run in (position, request,
-//    chunk) order, so a row pair's chunks are worked at the same time by
-//    different SMs and the pair is decided within a few microseconds of its
-//    first load.  Rows of a request behind a known rejection are never loaded:
-//    the producer skips them (and jumps the ticket counter past them).
-//  * Per chunk: the maximum (packed bf16x2 max), the weight sum relative to
-//    it, and for bf16 logit rows with top_p < 1 an exact count histogram of
-//    the bf16 values in a window below the row's maximum.  The window floor
-//    uses the largest maximum other chunks of the same row have published so
-//    far and the deepest nucleus seen in this call, so only the few elements
-//    that can border the nucleus are counted; a row whose boundary lies below
-//    every chunk's window is decided exactly by a radix descent over the row
-//    instead (also used for fp32 rows).
-//  * Window histograms are indexed by (-key) mod 256, so every chunk's bins
-//    line up whatever its reference; a chunk contributes only to keys at or
-//    below its own reference, which rules out aliasing.
-//  * The finisher that completes a row pair's last chunk merges the partials,
-//    finds the top-p boundaries, runs the accept test and publishes the
-//    decision in the request's state words (accepted-row mask, first
-//    non-accepted row).  Whoever completes "rows 0..f-1 accepted, row f not"
-//    resolves the request: a rejection or bonus row queues one race item per
-//    chunk of row f, which re-reads that row (from L2: it was just streamed)
-//    and races over the kept tokens only; the last race item writes the
-//    request's outputs.
+//  * One persistent CTA per SM with three roles: a producer warp, two groups
+//    of eight consumer warps and three finisher warps.  The producer takes
+//    work tickets from counters in the workspace and pulls each item into a
+//    ring of shared-memory stages with 1-D TMA bulk copies (cp.async.bulk,
+//    one mbarrier per stage); item n goes to consumer group n % 2, so while
+//    one group waits at a barrier or on latency the other computes.  The
+//    consumers hand each stage back through an "empty" mbarrier and pass
+//    their results to the finishers through a small shared-memory ring; the
+//    finishers do everything that waits on global memory (partials, arrival
+//    counters, merges, the request resolution), so the consumers only
+//    compute.  No CTA ever waits on another CTA's shared memory.
+//  * Three kinds of items, all one vocabulary chunk of one row pair (target
+//    row i and, for i < k_b, draft row i of request b):
+//      - row items (first pass, static tickets in (position, request, chunk)
+//        order): the chunk's maxima and weight sums relative to them;
+//      - window items (bf16 logit rows with top_p < 1): once the first pass
+//        of a row pair is merged its maxima are exact, and each chunk is read
+//        again (from L2) to count the bf16 values in a band of at most 256
+//        keys just below them; a boundary below the band asks for the next
+//        band down;
+//      - race items: the exponential race of a resolved request's rejection
+//        or bonus row over that chunk.
+//    Window and race items come from a queue of slots that the producers
+//    serve before any static ticket, so the rows on the critical path move
+//    first.  Rows of a request behind a known rejection are never loaded.
+//  * The finisher that completes a row pair's first pass merges the chunk
+//    partials; without top-p it runs the accept test at once, else it queues
+//    the window.  The finisher that completes the window finds the top-p
+//    boundaries, runs the accept test and publishes the decision in the
+//    request's state words.  Whoever completes "rows 0..f-1 accepted, row f
+//    not" resolves the request: a rejection or bonus row queues the race, and
+//    the last race item writes the request's outputs.
 //  * Per-call state lives in two halves of the workspace used on alternate
 //    calls: each call zeroes the half the next call will use.
 #include "verify_kernel.cuh"
@@ -51,16 +47,19 @@
 namespace sv {
 namespace stream {
 
-constexpr int kCW = 16;              // consumer warps (warps 0-15)
-constexpr int kCT = kCW * 32;        // consumer threads
+constexpr int kNG = 2;               // consumer groups, each on its own items
+constexpr int kGW = 8;               // warps per consumer group
+constexpr int kGT = kGW * 32;        // threads per consumer group
+constexpr int kCW = kNG * kGW;       // consumer warps (warps 0-15; group g: warps 8g .. 8g+7)
 constexpr int kProducerWarp = kCW;   // warp 16
 constexpr int kFinisherWarp = kCW + 1;  // warps 17 .. 17 + kFW - 1
-constexpr int kFW = 2;               // finisher warps; hand-off slot f goes to finisher f % kFW
-constexpr int kAllThreads = kCT + 32 + 32 * kFW;
-constexpr int kNF = 4;               // finisher hand-off slots
-static_assert(kNF % kFW == 0, "finisher slots split evenly");
+constexpr int kFW = 3;               // finisher warps; hand-off slot f goes to finisher f % kFW
+constexpr int kAllThreads = kCW * 32 + 32 + 32 * kFW;
+constexpr int kNF = 6;               // finisher hand-off slots; item n uses slot n % kNF
+static_assert(kNF % kFW == 0 && kNF % kNG == 0, "slots split evenly over finishers and groups");
+static_assert(kNF / kNG >= kFW, "each group's slots reach every finisher");
 constexpr int kBins = 256;
-constexpr int kMaxNs = 4;
+constexpr int kMaxNs = 6;
 constexpr int kMaxChunks = 32;
 constexpr uint32_t kNA = 1024u;      // request word na = kNA - first non-accepted row (0: none)
 constexpr float kDepthMargin = 1.0f; // log2 units added to the deepest nucleus seen
@@ -76,34 +75,40 @@ constexpr float kDepthMargin = 1.0f; // log2 units added to the deepest nucleus 
 #endif
 constexpr int kStreamUnroll = SV_STREAM_UNROLL;
 
+// Items are one chunk of a row pair: 32 KB of stage for every dtype mix.
 template <int EBT, int EBD>
 __host__ __device__ constexpr int chunk_elems() {
-  return (EBT == 2 && EBD == 2) ? 16384 : 8192;
+  return (EBT == 2 && EBD == 2) ? 8192 : 4096;
 }
 template <int EBT, int EBD>
 __host__ __device__ constexpr int stage_bytes() {
   return chunk_elems<EBT, EBD>() * (EBT + EBD);
 }
+// Item n uses stage n % NS; a multiple of kNG, so each group has its own stages.
 template <int EBT, int EBD>
 __host__ __device__ constexpr int num_stages() {
-  return stage_bytes<EBT, EBD>() <= 49152 ? 4 : 3;
+  return 6;
 }
+static_assert(6 % kNG == 0 && 6 <= kMaxNs, "stages split evenly over the groups");
 
-enum : int { kEnd = 0, kRowItem = 1, kRaceItem = 2, kBadItem = 3 };
-enum : int { kRaceResidual = 1, kRaceBonus = 2 };
+enum : int { kEnd = 0, kRowItem = 1, kRaceItem = 2, kBadItem = 3, kWinItem = 4 };
+enum : int { kRaceResidual = 1, kRaceBonus = 2, kWindowSlot = 3 };  // queue slot kinds
 
 // ---------------------------------------------------------------------------
 // Workspace records
 // ---------------------------------------------------------------------------
 struct Hdr {            // fixed words at byte 64 of the workspace header
   uint32_t parity;      // which state half this call uses
-  uint32_t ticket;      // next work ticket
+  uint32_t ticket;      // next static ticket (row items)
   uint32_t exit_cnt;    // CTAs finished
-  uint32_t pad[13];
+  uint32_t dticket;     // next queued ticket (window and race items: slot * n_ch + chunk)
+  uint32_t depth_t;     // deepest nuclei of the previous call (log2 units, float bits):
+  uint32_t depth_d;     // the first bands of a call start from them
+  uint32_t pad[10];
 };
 
 struct CallSt {         // per call, zeroed by the previous call
-  unsigned long long cnt;  // (requests resolved << 32) | race slots claimed
+  unsigned long long cnt;  // (requests resolved << 32) | queue slots claimed
   uint32_t n_done;      // requests whose outputs are written
   uint32_t depth_t;     // deepest target nucleus seen, log2 units (float bits)
   uint32_t depth_d;
@@ -130,16 +135,35 @@ struct ReqSt {
 };
 static_assert(sizeof(ReqSt) == 64, "");
 
+// A queue slot: two 64-bit words, each written once per call, so that a
+// reader that sees both non-zero sees the slot complete.
+//   w0: bit 63 set | row << 32 | b << 8 | kind
+//   w1: window: lo_t | hi_t << 16 | lo_d << 32 | hi_d << 48 (hi_t > 0)
+//       race:   pos | request id << 32 (pos > 0)
 struct Slot {
-  uint32_t b, row, kind, ready;
+  unsigned long long w0, w1;
 };
+constexpr unsigned long long kSlotFilled = 1ull << 63;
 
 struct PairSt {
-  uint32_t arrive;      // chunks finished
-  uint32_t tkey, dkey;  // largest chunk maxima published (order keys)
+  uint32_t arrive;      // first-pass chunks finished
+  uint32_t warrive;     // window chunks finished (this band)
   uint32_t state;       // SV_ROW_* once decided
-  uint32_t pad[4];
+  uint32_t wside;       // bits 0/1: target/draft counted in this band; bits 8+: band index
+  uint32_t lo_t, hi_t;  // the band's bf16 order keys, target
+  uint32_t lo_d, hi_d;  // and draft
 };
+constexpr int kMaxBands = 2;  // bands per row before the exact descent takes over
+
+// A row pair's first-pass statistics, kept for its window.
+struct PairStats {
+  float Mt, St, Md, Sd;  // maxima and weight sums (relative to them)
+  float vt, vd;          // the values at the proposal
+  float above_t, above_d;  // mass of the keys above the current band
+  uint32_t y_ok;
+  uint32_t pad[7];
+};
+static_assert(sizeof(PairStats) == 64, "");
 
 // One side (target or draft) of a decided row: everything the race and the
 // normalised-row writer need to evaluate prob(v).
@@ -153,12 +177,9 @@ struct RowRec {
 };
 static_assert(sizeof(RowRec) == 64, "");
 
-struct PartHdr {        // one side of a chunk partial
-  float m, S;
-  uint32_t ref, floor;  // window reference and floor keys (bf16 order keys)
-};
-// chunk partial: PartHdr target | PartHdr draft | (vt, vd, has_y, 0) | bins
-constexpr int kPartHead = 48;
+// chunk partial: (Mt, St, Md, Sd) | (vt, vd, has_y, 0) | window counts of
+// the band, 2 x 256 u16 (bin j: key hi - j)
+constexpr int kPartHead = 32;
 
 // ---------------------------------------------------------------------------
 // Kernel parameters
@@ -188,17 +209,24 @@ struct SParams {
   char* state[2];       // per-call state halves
   size_t state_words;   // u32 words per half
   RowRec* rows;         // [B][kmax+1]
+  PairStats* pstats;    // [B][kmax+1]
   char* parts;          // [B][kmax+1][n_ch] partials
   int part_bytes;       // kPartHead, plus 2 * 512 with histograms
   int hist;             // partials carry window histograms
+  uint32_t n_slots;     // queue slots: kMaxBands windows per row pair, one race per request
   int* err;
   unsigned long long slot_wait_ns;  // bound of a wait for a race slot
-  uint32_t n_static;    // (kmax + 1) * B * n_ch
+  uint32_t n_static;    // static tickets: (kmax + 1) * B * n_blk
+  int n_blk;            // tickets per row: blocks of up to kBatch chunks
 };
+constexpr int kBatch = 4;  // chunks per ticket (one round trip of the producer settles them all)
 
-// state-half layout: CallSt | ReqSt[B] | Slot[B] | PairSt[B][kmax+1]
+// state-half layout: CallSt | ReqSt[B] | Slot[n_slots] | PairSt[B][kmax+1]
+__host__ __device__ inline size_t slots_for(int B, int kmax) {
+  return (size_t)B * (size_t)(kmax + 1) * kMaxBands + (size_t)B;
+}
 __host__ __device__ inline size_t state_bytes_for(int B, int kmax) {
-  return sizeof(CallSt) + (size_t)B * sizeof(ReqSt) + (size_t)B * sizeof(Slot) +
+  return sizeof(CallSt) + (size_t)B * sizeof(ReqSt) + slots_for(B, kmax) * sizeof(Slot) +
          (size_t)B * (size_t)(kmax + 1) * sizeof(PairSt);
 }
 __device__ __forceinline__ CallSt* call_st(char* s) { return reinterpret_cast<CallSt*>(s); }
@@ -208,8 +236,9 @@ __device__ __forceinline__ ReqSt* req_st(char* s, int b) {
 __device__ __forceinline__ Slot* slot_st(char* s, int B, int q) {
   return reinterpret_cast<Slot*>(s + sizeof(CallSt) + (size_t)B * sizeof(ReqSt)) + q;
 }
-__device__ __forceinline__ PairSt* pair_st(char* s, int B, size_t pair) {
-  return reinterpret_cast<PairSt*>(s + sizeof(CallSt) + (size_t)B * (sizeof(ReqSt) + sizeof(Slot))) +
+__device__ __forceinline__ PairSt* pair_st(char* s, const SParams& P, size_t pair) {
+  return reinterpret_cast<PairSt*>(s + sizeof(CallSt) + (size_t)P.B * sizeof(ReqSt) +
+                                   (size_t)P.n_slots * sizeof(Slot)) +
          pair;
 }
 
@@ -223,7 +252,9 @@ struct SHdr {           // one stage's item, written by the producer
   int race, pos;
   uint32_t rid;
   int y;                // the row's proposal (draft rows)
-  int pad[2];
+  int win;              // window items: bit 0 target, bit 1 draft
+  uint32_t lo_t, hi_t, lo_d, hi_d;  // window items: the band's keys
+  int pad;
   RowRec rr;            // race items: the decided row
 };
 
@@ -234,14 +265,13 @@ struct alignas(16) Fin {
   float T, top_p;
   uint32_t rid;
   int y;
-  float Mt, St, Md, Sd;
-  uint32_t ref_t, flo_t, ref_d, flo_d;
   float vt, vd;         // the values at y when y lies in this chunk
   int has_y, win;       // win: bit 0 target window, bit 1 draft window
   float rw, rE;         // race items: the chunk's winner
   int ridx, pad;
   RowRec rr;            // race items: the decided row
-  uint32_t hist[2][kBins];  // window counts by ring index (-key) & 255
+  float4 wp[kGW];       // row items: per consumer warp (max, sum) of target and draft
+  uint32_t hist[2][kBins];  // window items: counts, bin j = key hi - j
 };
 
 struct alignas(16) SSmem {
@@ -249,20 +279,18 @@ struct alignas(16) SSmem {
   unsigned long long fin_full[kNF], fin_empty[kNF];
   SHdr hdr[kMaxNs];
   Fin fin[kNF];
-  float fh[kFW][kBins]; // finisher scratch: row-bin masses / descent histogram
-  float red[kCW][4];
-  uint32_t hint[4];     // row items: max hints and nucleus depths, as thread 0 read them
+  float fh[kFW][kBins]; // finisher scratch: descent histogram
   RacePart rp[kCW];
-  union {
-    uint16_t idx[kCW][256];  // race candidates
-    uint8_t bin[kCW][512];   // window bins
-  } wb;
+  uint16_t wb[kCW][256];  // per consumer warp: race candidates / window groups
 };
 
 // ---------------------------------------------------------------------------
 // small helpers
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"n"(kCT) : "memory"); }
+// Barrier of consumer group g (named barrier 1 + g).
+__device__ __forceinline__ void gbar(int g) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "n"(kGT) : "memory");
+}
 
 __device__ __forceinline__ void fence_sc() { asm volatile("fence.sc.gpu;" ::: "memory"); }
 
@@ -270,6 +298,20 @@ __device__ __forceinline__ unsigned long long ld_relaxed64(const unsigned long l
   unsigned long long v;
   asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_relaxed64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 __device__ __forceinline__ void mbar_init_n(unsigned long long* bar, int n) {
@@ -338,7 +380,7 @@ __device__ __forceinline__ void trace_ev(uint32_t ev, uint32_t a, uint32_t b) {
 #define SV_TR(ev, a, b) ((void)0)
 #endif
 
-// Release the stage: each consumer warp arrives once after its last read.
+// Release the stage: each warp of the consuming group arrives once after its last read.
 __device__ __forceinline__ void release_stage(SSmem& sm, int s) {
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive1(&sm.empty[s]);
@@ -494,77 +536,6 @@ __device__ __noinline__ void exact_top_p_warp(const char* row, int V, RowP& r, f
   r.Z = z;
   r.invZ = 1.0f / z;
   r.vstar = vkey_value<EB>(prefix);
-}
-
-// Window merge and scan of one bf16 row by one warp.  Lane c < n_ch holds
-// chunk c's header (ref, floor).  Row bin j is the key K - j (K = key of the
-// row maximum); only bins with key >= Fstar are complete.  Lane l loads ring
-// bins 8l .. 8l+7 of every chunk (ring index (-key) & 255) and counts a chunk
-// only for keys at or below its reference.  Returns the boundary bin j (or
-// -1 when the kept mass does not reach R inside the complete window) and the
-// kept mass through it in Z.
-__device__ __forceinline__ int window_boundary(const SParams& P, const char* parts, int side,
-                                               uint32_t my_ref, uint32_t K, uint32_t Fstar,
-                                               const RowP& r, float R, float* fh, float& Z) {
-  const int lane = threadIdx.x & 31;
-  const int jmax = K >= Fstar ? (int)min(255u, K - Fstar) : -1;
-  const uint32_t rK = (0u - K) & 255u;
-  uint32_t cnt[8];
-#pragma unroll
-  for (int q = 0; q < 8; ++q) cnt[q] = 0u;
-  const char* base = parts + kPartHead + side * 512 + 16 * lane;
-  for (int c0 = 0; c0 < P.n_ch; c0 += 8) {
-    uint4 v[8];  // issue the loads of 8 chunks together (one round trip)
-#pragma unroll
-    for (int u = 0; u < 8; ++u)
-      v[u] = c0 + u < P.n_ch ? __ldcg(reinterpret_cast<const uint4*>(base + (size_t)(c0 + u) * P.part_bytes))
-                             : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const uint32_t refc = __shfl_sync(0xffffffffu, my_ref, (c0 + u) & 31);
-      if (c0 + u >= P.n_ch) continue;
-      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const uint32_t j = ((uint32_t)(8 * lane + q) - rK) & 255u;
-        const uint32_t key = K - j;
-        if (key <= refc) cnt[q] += (w[q >> 1] >> (16 * (q & 1))) & 0xFFFFu;
-      }
-    }
-  }
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const uint32_t j = ((uint32_t)(8 * lane + q) - rK) & 255u;
-    const uint32_t key = K - j;
-    float mass = 0.0f;
-    if ((int)j <= jmax && j <= K && cnt[q]) mass = (float)cnt[q] * weight<false>(vkey_value<2>(key), r);
-    fh[j] = mass;
-  }
-  __syncwarp();
-  float h[8], inc[8], t = 0.0f;
-#pragma unroll
-  for (int q = 0; q < 8; ++q) h[q] = fh[8 * lane + q], t += h[q], inc[q] = t;
-  float off = t;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float v = __shfl_up_sync(0xffffffffu, off, o);
-    if (lane >= o) off += v;
-  }
-  off -= t;
-  int first = 8;
-#pragma unroll
-  for (int q = 7; q >= 0; --q)
-    if (8 * lane + q <= jmax && off + inc[q] >= R) first = q;
-  const uint32_t hit = __ballot_sync(0xffffffffu, first < 8);
-  __syncwarp();  // fh is reused by the caller
-  if (!hit) return -1;
-  const int src = __ffs(hit) - 1;
-  float z = 0.0f;
-#pragma unroll
-  for (int q = 0; q < 8; ++q)
-    if (q == first) z = off + inc[q];
-  Z = __shfl_sync(0xffffffffu, z, src);
-  return 8 * src + __shfl_sync(0xffffffffu, first, src);
 }
 
 }  // namespace stream

@@ -21,12 +21,16 @@ from tests import parity
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module")
-def ver():
+@pytest.fixture(scope="module", params=["cluster", "stream"])
+def ver(request):
+    """Every test runs on both kernels behind spec_verify: the cluster-resident
+    one (the default) and the streaming one (SV_FLAG_STREAM_PATH; calls it
+    does not serve stay on the cluster kernel)."""
     if not os.path.exists(binding.LIB_PATH):
         from speculative_decoding_verification_07_gb300 import build
         build.build()
     v = binding.Verifier(0)
+    v.path_flags = binding.FLAG_STREAM_PATH if request.param == "stream" else 0
     yield v
     v.close()
 
@@ -297,10 +301,10 @@ def test_verify_b64_k4(ver, top_p):
 @pytest.mark.parametrize("name", ["verify_b64_k4", "greedy_shared", "paged_bf16", "sweep"])
 def test_streaming_and_cluster_kernels_agree(ver, name):
     """The two kernels behind spec_verify (the streaming kernel, which serves
-    these calls, and the cluster-resident one that top-k and the repetition
-    penalty use) give the same outputs and the same per-row debug records."""
+    these calls when asked, and the cluster-resident one, the default) give the
+    same outputs and the same per-row debug records."""
     inp = W.build(name) if name != "sweep" else W.sweep(B=64, V=128256, sigma=1.0)
-    a, da, _, _ = run(ver, inp, debug=True)
+    a, da, _, _ = run(ver, inp, flags=binding.FLAG_STREAM_PATH, debug=True)
     b, db, _, _ = run(ver, inp, flags=binding.FLAG_CLUSTER_PATH, debug=True)
     for key in ("accepted", "out_tokens", "num_emitted", "status"):
         assert torch.equal(a[key], b[key]), key
