@@ -1073,10 +1073,15 @@ __device__ __forceinline__ float race_weight(const char* st, const char* sd, int
 // candidate, the fast E first and an accurate logf only for contenders.  The
 // threshold rises with the warp's best after every flush.
 template <int EBT, int EBD, bool PROBS>
-__device__ __noinline__ void race_slice(const char* st, const char* sd, const SliceIter& it,
-                                        bool residual, const RowP& rt, const RowP& rd,
+__device__ __noinline__ void race_slice(const char* st, const char* sd, const SliceIter& it_ref,
+                                        bool residual, const RowP& rt_ref, const RowP& rd_ref,
                                         uint32_t pos, uint32_t rid, uint32_t k0, uint32_t k1,
                                         uint16_t* wb, RacePart& best) {
+  // Register copies of the caller's records: they live in its stack frame
+  // (their address is passed), and the candidate loop would otherwise reload
+  // them from local memory, which misses L1 beside the large slices.
+  const SliceIter it = it_ref;
+  const RowP rt = rt_ref, rd = rd_ref;
   const int lane = threadIdx.x & 31;
   float bw = best.w, bE = best.E;
   int bidx = best.idx;
@@ -1394,8 +1399,10 @@ __device__ __forceinline__ int warp_wait_earlier(const KParams& P, int b, int i,
 // (target row i and draft row i of request b) at a time, every CTA on its
 // slice of both rows in shared memory.
 // ---------------------------------------------------------------------------
+// Two CTAs per SM (128 registers, no spills) rather than three (80 registers,
+// spills in the row loop): fewer clusters, but each row's phases run faster.
 template <int EBT, int EBD, bool PROBS, bool TOPK>
-__global__ void __launch_bounds__(kThreads, 3) verify_kernel(const KParams P) {
+__global__ void __launch_bounds__(kThreads, 2) verify_kernel(const KParams P) {
   cg::cluster_group cluster = cg::this_cluster();
   __shared__ Smem sm;
   extern __shared__ __align__(128) char dyn[];
