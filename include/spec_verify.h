@@ -278,10 +278,9 @@ sv_status spec_verify(sv_handle* handle, const sv_verify_args* args, void* works
  *  - Set-up: the first call on a device (the current one) looks up the
  *    array's address with cudaGetSymbolAddress and reads the SM count; make
  *    that first call before any stream capture on that device.
- *  - Sharing: every call on a device uses the same array, which keeps the
- *    previous call's contents.  Each call clears the counters that must start
- *    at zero with an 8-byte cudaMemsetAsync on `stream`, then launches the
- *    kernel.  Calls whose GPU work overlaps (two streams without ordering
+ *  - Sharing: every call on a device uses the same array.  Each call clears
+ *    the counters and its own rows' decision words with one cudaMemsetAsync
+ *    on `stream` (at most 64 KB), then launches the kernel.  Calls whose GPU work overlaps (two streams without ordering
  *    between them) race on the array and give wrong results; issue them on
  *    one stream or order them with events.
  *  - Errors: no handle, so no device error word; device-side conditions are

@@ -39,6 +39,13 @@ __device__ __forceinline__ void report(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }
 
+// Raise a kernel's dynamic shared-memory limit to at least `bytes`, once per
+// (kernel, size), under a process-wide mutex.  The attribute is per function:
+// it is only ever raised, so a launch sized for an earlier limit stays valid
+// whatever other threads set meanwhile (occupancy follows each launch's own
+// dynamic size).
+sv_status sv_raise_dyn_smem(const void* fn, size_t bytes);
+
 // ---------------------------------------------------------------------------
 // Acquire / release accesses at GPU scope (row states written by one cluster
 // and polled by others).

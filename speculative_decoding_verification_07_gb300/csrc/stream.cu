@@ -160,7 +160,10 @@ sv_status stream_launch(sv_handle* h, const sv_verify_args* a, void* ws, size_t 
   P.n_blk = n_blk;
 
   const StreamFn fn = v->fn();
-  SV_CUDA_TRY(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, v->dyn_smem));
+  {
+    const sv_status rs = sv_raise_dyn_smem((const void*)fn, (size_t)v->dyn_smem);
+    if (rs != SV_OK) return rs;
+  }
   if (sv_launch_pdl(fn, dim3((unsigned)h->num_sms), dim3(stream::kAllThreads), (size_t)v->dyn_smem,
                     stream, P) != cudaSuccess) {
     (void)cudaGetLastError();

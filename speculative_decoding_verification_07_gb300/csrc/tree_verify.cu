@@ -103,7 +103,10 @@ extern "C" sv_status spec_verify_tree(sv_handle* h, const sv_tree_args* a, sv_st
   for (int i = 0; i < h->occ_n; ++i)
     if (h->occ_fn[i] == (const void*)fn && h->occ_c[i] == C && h->occ_smem[i] == dyn)
       max_clusters = h->occ_val[i];
-  SV_CUDA_TRY(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
+  {
+    const sv_status rs = sv_raise_dyn_smem((const void*)fn, dyn);
+    if (rs != SV_OK) return rs;
+  }
   if (max_clusters == 0) {
     if (C > 8) SV_CUDA_TRY(cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
     cfg.gridDim = dim3((unsigned)C);

@@ -165,9 +165,10 @@ extern "C" sv_status spec_verify(sv_handle* h, const sv_verify_args* a, void* ws
   for (int i = 0; i < h->occ_n; ++i)
     if (h->occ_fn[i] == (const void*)fn && h->occ_c[i] == C && h->occ_smem[i] == dyn)
       max_clusters = h->occ_val[i];
-  // the attribute is per function: set it for every launch (other shapes may
-  // have lowered it since the occupancy of this shape was cached)
-  SV_CUDA_TRY(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn));
+  {
+    const sv_status rs = sv_raise_dyn_smem((const void*)fn, dyn);
+    if (rs != SV_OK) return rs;
+  }
   if (max_clusters == 0) {
     if (C > 8)
       SV_CUDA_TRY(cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));

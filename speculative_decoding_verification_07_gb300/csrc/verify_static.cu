@@ -16,8 +16,9 @@
 //  * Every GPU that loads this library keeps the array (about 64 KB) until the
 //    process exits.
 //  * All calls in the process share the one array per device.  Each call
-//    clears the counters that must start at zero (an 8-byte cudaMemsetAsync on
-//    its stream) and leaves the rest for the next call.  Two calls whose work
+//    clears the counters and its own rows' decision words (one
+//    cudaMemsetAsync on its stream, at most 64 KB), so no word from an older
+//    call can carry a matching epoch tag.  Two calls whose work
 //    overlaps on the GPU (for example on two streams without ordering) race
 //    on the array and give wrong results: order them on one stream.
 //  * The first call on a device looks up the array's address with
@@ -172,10 +173,9 @@ extern "C" sv_status spec_verify_static(const sv_verify_args* a, sv_stream_t str
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = dyn;
   cfg.stream = (cudaStream_t)stream;
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn) !=
-      cudaSuccess) {
-    (void)cudaGetLastError();
-    return SV_ERR_CUDA;
+  {
+    const sv_status rs = sv_raise_dyn_smem((const void*)fn, dyn);
+    if (rs != SV_OK) return rs;
   }
   int max_clusters = 0;
   for (int i = 0; i < d->occ_n; ++i)
@@ -200,8 +200,10 @@ extern "C" sv_status spec_verify_static(const sv_verify_args* a, sv_stream_t str
       ++d->occ_n;
     }
   }
-  // the ticket and done counters must start at zero (the epoch word stays)
-  if (cudaMemsetAsync((char*)d->ws + 4, 0, 8, (cudaStream_t)stream) != cudaSuccess) {
+  // the ticket and done counters must start at zero, and so must this call's
+  // row words (the epoch word stays): a word left from a call 2^28 epochs ago
+  // would otherwise carry a matching tag
+  if (cudaMemsetAsync((char*)d->ws + 4, 0, kHdrBytes - 4 + rows * 4, (cudaStream_t)stream) != cudaSuccess) {
     (void)cudaGetLastError();
     return SV_ERR_CUDA;
   }
