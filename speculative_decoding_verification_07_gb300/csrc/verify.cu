@@ -117,14 +117,16 @@ extern "C" sv_status spec_verify(sv_handle* h, const sv_verify_args* a, void* ws
   if (!var) return SV_ERR_UNSUPPORTED;
   const KernelFn fn = a->top_k ? var->fn_topk : var->fn;
 
-  // Cluster size: smallest power of two whose slices fit kMaxBlk TMA blocks,
-  // then grown while the grid would leave SMs idle.
+  // Cluster size: the smallest whose slices fit kMaxBlk TMA blocks (any size,
+  // not only powers of two: V = 151936 takes 10 CTAs rather than 16, so more
+  // clusters are in flight), then doubled, up to 8, while the grid would leave
+  // SMs idle.
   const int cap = kMaxBlk * kBlk;
-  int C = 1;
-  while (C < kMaxCluster && (size_t)C * cap < (size_t)a->V) C <<= 1;
-  if ((size_t)C * cap < (size_t)a->V) return SV_ERR_UNSUPPORTED;
+  const size_t need = ((size_t)a->V + cap - 1) / cap;
+  if (need > (size_t)kMaxCluster) return SV_ERR_UNSUPPORTED;
+  int C = need < 1 ? 1 : (int)need;
   const size_t rows = n_tickets;
-  while (C < 8 && rows * (size_t)C < (size_t)h->num_sms * 2) C <<= 1;
+  while (2 * C <= 8 && rows * (size_t)C < (size_t)h->num_sms * 2) C <<= 1;
   int slice = (int)(((size_t)a->V + C - 1) / C);
   slice = (slice + kGroup - 1) / kGroup * kGroup;
   const int d_off = (slice * ebt + 127) / 128 * 128;

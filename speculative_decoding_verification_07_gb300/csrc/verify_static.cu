@@ -132,10 +132,10 @@ extern "C" sv_status spec_verify_static(const sv_verify_args* a, sv_stream_t str
 
   // cluster size and slice, as for spec_verify
   const int cap = kMaxBlk * kBlk;
-  int C = 1;
-  while (C < kMaxCluster && (size_t)C * cap < (size_t)a->V) C <<= 1;
-  if ((size_t)C * cap < (size_t)a->V) return SV_ERR_UNSUPPORTED;
-  while (C < 8 && rows * (size_t)C < (size_t)d->num_sms * 2) C <<= 1;
+  const size_t need = ((size_t)a->V + cap - 1) / cap;
+  if (need > (size_t)kMaxCluster) return SV_ERR_UNSUPPORTED;
+  int C = need < 1 ? 1 : (int)need;
+  while (2 * C <= 8 && rows * (size_t)C < (size_t)d->num_sms * 2) C <<= 1;
   int slice = (int)(((size_t)a->V + C - 1) / C);
   slice = (slice + kGroup - 1) / kGroup * kGroup;
   const int d_off = (slice * ebt + 127) / 128 * 128;
