@@ -55,3 +55,14 @@ def test_null_handle_is_rejected_before_any_launch(lib):
     st = binding.BflState()
     assert lib.bfl_init(None, ctypes.byref(st), None) == binding.SV_ERR_INVALID
     assert lib.kv_rollback_contig(None, 1, None, None, None) == binding.SV_ERR_INVALID
+
+
+def test_flag_and_status_constants_match_header():
+    """The binding's flag and status constants are the header's values (the
+    kernel selection flags included)."""
+    text = open(HEADER).read()
+    defs = dict(re.findall(r"#define\s+(SV_(?:FLAG|ST)_\w+)\s+(\d+)u", text))
+    assert "SV_FLAG_STREAM_PATH" in defs and "SV_FLAG_CLUSTER_PATH" in defs
+    for name, value in defs.items():
+        py = name[3:]  # SV_FLAG_X -> FLAG_X, SV_ST_X -> ST_X
+        assert getattr(binding, py) == int(value), name
