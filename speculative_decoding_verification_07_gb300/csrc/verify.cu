@@ -153,7 +153,7 @@ extern "C" sv_status spec_verify(sv_handle* h, const sv_verify_args* a, void* ws
   P.rep_draft = a->draft_kind == SV_DRAFT_LOGITS;
 
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)C;
   attr[0].val.clusterDim.y = 1;
@@ -190,6 +190,11 @@ extern "C" sv_status spec_verify(sv_handle* h, const sv_verify_args* a, void* ws
   }
   const size_t nclusters = rows < (size_t)max_clusters ? rows : (size_t)max_clusters;
   cfg.gridDim = dim3((unsigned)(nclusters * C));
+  // programmatic dependent launch: the kernel waits for its predecessor in
+  // its first instruction (griddepcontrol.wait), so only its launch overlaps
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs = 2;
   if (cudaLaunchKernelEx(&cfg, fn, P) != cudaSuccess) {
     (void)cudaGetLastError();
     return SV_ERR_CUDA;

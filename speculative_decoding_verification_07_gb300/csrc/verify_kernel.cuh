@@ -1403,6 +1403,14 @@ __device__ __forceinline__ int warp_wait_earlier(const KParams& P, int b, int i,
 // spills in the row loop): fewer clusters, but each row's phases run faster.
 template <int EBT, int EBD, bool PROBS, bool TOPK>
 __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const KParams P) {
+  // Launched as a programmatic dependent (spec_verify), this grid may start
+  // while the previous kernel (the lookahead reserve, or the previous call)
+  // still runs: wait for it before anything at all is read, the workspace's
+  // epoch included.  A programmatically dependent kernel that follows (the
+  // commit) may then be scheduled, on an SM this grid leaves free; it reads
+  // nothing of this call before its own griddepcontrol.wait.
+  pdl_wait();
+  pdl_trigger();
   cg::cluster_group cluster = cg::this_cluster();
   __shared__ Smem sm;
   extern __shared__ __align__(128) char dyn[];

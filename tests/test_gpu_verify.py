@@ -375,6 +375,24 @@ def test_repeated_calls_reuse_workspace(ver):
     parity.compare(small, out)
 
 
+def test_back_to_back_calls_without_sync(ver):
+    """Calls issued back to back on one stream with no host synchronisation
+    between them share the workspace safely: a call's kernel may be scheduled
+    while the previous call's kernel still runs (programmatic dependent
+    launch), and must still see only its own call's state."""
+    a = W.verify_b64_k4(B=16, V=32000, index=11)
+    b = W.verify_b64_k4(B=16, V=32000, index=12)
+    da, db = device_io.to_device(a, "cuda:0"), device_io.to_device(b, "cuda:0")
+    outs = [ver.verify(**(da if j % 2 == 0 else db)) for j in range(8)]
+    torch.cuda.synchronize()
+    assert ver.error() == 0
+    report("back to back (a)", parity.compare(a, outs[0]))
+    report("back to back (b)", parity.compare(b, outs[1]))
+    for j in range(2, 8):
+        for key in outs[j]:
+            assert torch.equal(outs[j][key], outs[j % 2][key]), (j, key)
+
+
 # --------------------------------------------------------------------------- #
 # laws on small vocabularies
 # --------------------------------------------------------------------------- #
