@@ -546,6 +546,34 @@ def e2e_run(ver, sets, dev, args, pool, table, seq, kk, B, k):
             "overlap": "H2D of step i+1 on a copy stream while step i computes (two input buffers)"}
 
 
+def graph_us_per_call(fn, n_calls, replays, dev):
+    """Microseconds per call of fn(i, stream), i = 0 .. n_calls - 1, captured
+    once in a CUDA graph on a side stream and replayed `replays` times after
+    two untimed replays: the host's launch cost stays out of the timed region."""
+    import torch
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for i in range(n_calls):
+                fn(i, s)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        for _ in range(2):
+            g.replay()
+        e0.record(s)
+        for _ in range(replays):
+            g.replay()
+        e1.record(s)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) / (replays * n_calls) * 1e3
+    del g
+    return us
+
+
 def commit_copy_run(ver, sets, outs, dev, peak):
     """The commit-by-copy kernel at the workload's KV shape (32 layers x 8 KV
     heads x d128 bf16, block 16): entries 0..a_b of every request move from a
@@ -569,9 +597,9 @@ def commit_copy_run(ver, sets, outs, dev, peak):
     kv = torch.zeros(2 * B, L, 2, H, BS, D, dtype=torch.bfloat16, device=dev)
     stages = [torch.randn(B, kmax + 1, L, 2, H, D, device=dev).to(torch.bfloat16) for _ in sets]
     acc = [o["accepted"].clone() for o in outs]
-    run = lambda i: binding.kv_commit_copy(ver.handle, acc[i % len(sets)], S[i % len(sets)],
-                                           tables[i % len(sets)], BS, 2 * B,
-                                           stages[i % len(sets)], kv)
+    run = lambda i, st=None: binding.kv_commit_copy(ver.handle, acc[i % len(sets)], S[i % len(sets)],
+                                                    tables[i % len(sets)], BS, 2 * B,
+                                                    stages[i % len(sets)], kv, stream=st)
     for i in range(8):
         run(i)
     torch.cuda.synchronize()
@@ -582,12 +610,21 @@ def commit_copy_run(ver, sets, outs, dev, peak):
         run(i)
     e1.record()
     torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) / n * 1e3
+    us_eager = e0.elapsed_time(e1) / n * 1e3
+    # the launches one by one from Python are bound by the host's call rate:
+    # the kernel's own time comes from a graph of the same 64 launches
+    try:
+        us, launch = graph_us_per_call(run, n, 4, dev), f"CUDA graph of {n} launches, 4 replays"
+    except Exception as exc:  # keep the eager figure, say why
+        torch.cuda.synchronize()
+        us, launch = us_eager, f"eager ({type(exc).__name__}: graph capture failed)"
+    assert ver.error() == 0, "device error in the commit-by-copy leg"
     per_tok = L * 2 * H * D * 2
     nbytes = float(np.mean([2 * ((a.cpu().numpy().astype(np.int64) + 1).clip(min=0).sum()) * per_tok
                             for a in acc]))
     gbs = nbytes / (us * 1e-6) / 1e9
     return {"us": us, "bytes_per_launch": nbytes, "GB/s": gbs, "peak": peak, "frac": gbs / peak,
+            "launch": launch, "us_eager_launches": us_eager,
             "shape": "32 layers x 8 KV heads x d128 bf16, block 16, staged entries 0..a_b"}
 
 
@@ -674,7 +711,9 @@ def config_legs(ver, dev, peak, budget_s=90.0):
     """Throughput of spec_verify on every configuration of the benchmark set
     (device-generated inputs, rotated over enough sets to exceed L2): rows/s,
     GB/s of the full and of the needed bytes, and fractions of the measured
-    peak and of 8 TB/s.  Per leg: the mean of CUDA-event-timed launches."""
+    peak and of 8 TB/s.  Per leg: CUDA-event time per call over replays of a
+    graph of the calls (`us`), and over the same calls launched one by one from
+    Python (`us_eager_calls`, bound by the host's call rate on small batches)."""
     import torch
 
     from speculative_decoding_verification_07_gb300 import binding
@@ -737,7 +776,19 @@ def config_legs(ver, dev, peak, budget_s=90.0):
         e1.record()
         torch.cuda.synchronize()
         assert ver.error() == 0, f"device error in config leg {name}"
-        us = e0.elapsed_time(e1) / n * 1e3
+        us_eager = e0.elapsed_time(e1) / n * 1e3
+        # small configurations are bound by the host's call rate when launched
+        # one by one: time a graph of the same calls (all sets, at least 8)
+        n_calls = len(sets) * max(1, -(-8 // len(sets)))
+        try:
+            us = graph_us_per_call(lambda i, st: binding.spec_verify(ver.handle, args[i % len(args)],
+                                                                      wsp, st),
+                                   n_calls, max(1, -(-n // n_calls)), dev)
+            launch = f"CUDA graph of {n_calls} calls"
+        except Exception as exc:  # keep the eager figure, say why
+            torch.cuda.synchronize()
+            us, launch = us_eager, f"eager ({type(exc).__name__}: graph capture failed)"
+        assert ver.error() == 0, f"device error in config leg {name} (graph)"
         rows = float(np.mean([(d["k"].long() + 1).sum().item() for d in sets]))
         bfull = float(np.mean([DW.full_bytes(d) for d in sets]))
         bneed = float(np.mean([DW.needed_bytes(d, o["accepted"]) for d, o in zip(sets, outs)]))
@@ -748,7 +799,7 @@ def config_legs(ver, dev, peak, budget_s=90.0):
                       "bytes_full": bfull, "bytes_needed": bneed, "GBs_full": gfull,
                       "GBs_needed": gneed, "frac_full": gfull / peak, "frac_of_8tbs": gfull / 8000.0,
                       "l2": f"{len(sets)} input sets of {per / 1e6:.1f} MB rotate",
-                      "launches": n}
+                      "launches": n, "launch": launch, "us_eager_calls": us_eager}
         del sets, outs, args, one
         torch.cuda.empty_cache()
     return legs

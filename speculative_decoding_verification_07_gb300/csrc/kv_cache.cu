@@ -415,14 +415,17 @@ __global__ void kv_cow_copy_kernel(int B, const int32_t* cow, kv_payload kv, int
 // ---------------------------------------------------------------------------
 // Commit by copy: staged K/V of positions S_b .. S_b + a_b into paged slots.
 // kCopySplit CTAs per (request, entry) share its layers x 2 x heads runs of
-// head_dim elements; every thread keeps 8 16-byte loads in flight.
+// head_dim elements; every thread keeps 4 16-byte loads in flight.  The
+// register cap (32 a thread, eight CTAs per SM) is what makes the paged
+// destination as fast as a contiguous one: at 74 registers only three CTAs fit
+// on an SM, most of the grid waits for a slot, and the copy took 30 % longer.
 // ---------------------------------------------------------------------------
 constexpr int kCopySplit = 8;
 
 // rows: positions S_b .. S_b + rows - 1 considered per request; entries: the
 // stage's entries per request; path (tree commits) [B][path_ld]: the entry of
 // position S_b + i is path[b][i - 1] for i >= 1 (NULL: entry i).
-__global__ void __launch_bounds__(256) kv_commit_copy_kernel(int B, int rows, int entries,
+__global__ void __launch_bounds__(256, 8) kv_commit_copy_kernel(int B, int rows, int entries,
                                                              const int32_t* path, int path_ld,
                                                              const int32_t* accepted,
                                                              const int32_t* seq_len,
@@ -460,7 +463,7 @@ __global__ void __launch_bounds__(256) kv_commit_copy_kernel(int B, int rows, in
               (size_t)(p % block_size) * kv.head_dim * kv.elem_bytes;
   const int n = runs * vrun;
   const int v0 = (int)((long long)n * part / kCopySplit), v1 = (int)((long long)n * (part + 1) / kCopySplit);
-  constexpr int kU = 8;
+  constexpr int kU = 4;
   for (int base = v0 + threadIdx.x; base < v1; base += kU * blockDim.x) {
     uint4 r[kU];
 #pragma unroll
