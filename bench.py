@@ -135,10 +135,11 @@ def full_bytes(inp):
 
 def needed_bytes(inp, accepted):
     """B_min: the rows the method must read -- target rows 0..a_b and draft rows
-    0..min(a_b, k_b - 1) (every row after the first rejection is discarded)."""
+    0..min(a_b, k_b - 1) (every row after the first rejection is discarded); a
+    request refused at row 0 (a_b = -1) still had row 0 read."""
     V = inp["target"].shape[-1]
     k = inp["k"].astype(np.int64)
-    a = np.asarray(accepted, np.int64)
+    a = np.maximum(np.asarray(accepted, np.int64), 0)
     return int(((a + 1) * V * 2 + np.minimum(a + 1, k) * V * 2).sum())
 
 
@@ -173,7 +174,7 @@ def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
-    nproc = os.cpu_count() or 1
+    nproc = args.ref_procs if args.ref_procs > 0 else (os.cpu_count() or 1)
     B = 64
     with mp.get_context("spawn").Pool(nproc, initializer=_ref_init) as pool:
         def step(t):
@@ -821,6 +822,8 @@ def main():
     ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-procs", type=int, default=0,
+                    help="host processes of the reference arm (0: one per core)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-legs", action="store_true")
     args = ap.parse_args()
