@@ -19,7 +19,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from oracle import philox, sampling as S
+from oracle import sampling as S
 
 TOL = 1e-5
 PROB_TOL = 1e-6
